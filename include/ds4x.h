@@ -1,0 +1,154 @@
+/*
+ * ds4x.h — C ABI of libds4x.so, the GB300 (sm_103a) implementation of the
+ * DeepSeek V4 Flash sparse-attention "lightning indexer" hot path:
+ *
+ *     score  ->  top-k (k_top = 512)  ->  sparse multi-query attention
+ *
+ * Sources for what the path computes:
+ *   [K]  "How I made DeepSeek 12x faster on a Mac Studio", section "1: the kernels":
+ *        the lightning indexer scores compressed KV and keeps the top 512 rows per
+ *        token (PRs #830/#831 = the scorer, #832 = the streaming top-k whose output
+ *        is byte-identical to a full sort).
+ *   [S]  "How I turned one oversized DeepSeek optimization into three merged oMLX
+ *        PRs", section "The three changes that merged", item 3 (PR #2563): when every
+ *        pooled row fits inside index_topk, scoring and top-k are skipped and the
+ *        sequential indices are emitted.
+ *   [A]  same page, item 1 (PR #2559): attention over pooled compressed rows chosen
+ *        by an index list.
+ *   The pages never print the indexer formula; this library's definition is
+ *        score[t,s] = sum_h w[t,h] * ReLU( q[t,h,:] . k[s,:] )
+ *   with row s visible to a token at position p iff (s+1)*ratio <= p+1, top-k ties
+ *   broken toward the lower row index, indices emitted in ascending row order, and
+ *   the attention  out[t,h,:] = sum_j softmax_j(scale * q_attn[t,h,:].kv[idx_j,:]) kv[idx_j,:]
+ *   (kv is both key and value; softmax in fp32).
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor argument is a DEVICE pointer to a dense row-major array owned by the
+ *     caller; the library allocates nothing and keeps no state between calls.
+ *     Pointers must be 16-byte aligned.
+ *   - fp16 / bf16 tensors are passed as raw 16-bit storage (const void*).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     Every call is asynchronous on that stream; calls on different streams that
+ *     write disjoint outputs may run concurrently.
+ *   - Arguments are validated on the host before anything is launched. On a
+ *     validation error nothing is launched and no output is touched.
+ *   - Return value: DS4X_OK, or a negative ds4x_status (see ds4x_status_string).
+ *     DS4X_ERR_CUDA is returned when a launch fails (the CUDA error is left for the
+ *     caller to inspect with cudaGetLastError / cudaPeekAtLastError).
+ *   - There is no CPU fallback: unsupported shapes return DS4X_ERR_UNSUPPORTED.
+ *
+ * Visibility:  n_vis(p) = min(S, floor((p+1)/ratio)) rows are visible to a token at
+ *              position p (positions are int32, p >= 0).
+ */
+#ifndef DS4X_H
+#define DS4X_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { DS4X_F16 = 0, DS4X_BF16 = 1 } ds4x_dtype;
+
+typedef enum {
+  DS4X_OK = 0,
+  DS4X_ERR_INVALID = -1,     /* null/misaligned pointer, negative size, bad ld, ...  */
+  DS4X_ERR_UNSUPPORTED = -2, /* a shape this build has no kernel for                 */
+  DS4X_ERR_CUDA = -3,        /* a kernel launch or device query failed              */
+  DS4X_ERR_WORKSPACE = -4,   /* workspace_bytes smaller than the *_workspace_bytes() */
+  DS4X_ERR_TIMEOUT = -5      /* a bounded device-side wait gave up                  */
+} ds4x_status;
+
+/* Shapes the kernels accept (anything else -> DS4X_ERR_UNSUPPORTED):
+ *   indexer heads H in {16, 32, 64, 128}, indexer dim D in {64, 128}
+ *   attention heads Hq = 64, attention dim Dkv = 512
+ *   1 <= k_top <= DS4X_MAX_KTOP                                                  */
+#define DS4X_MAX_KTOP 1024
+
+/* ---------------------------------------------------------------------------
+ * ds4x_indexer_score — the lightning-indexer scorer ([K] #830/#831).
+ *
+ *   scores[t*ld_scores + s] = sum_h w[t,h] * max(0, sum_d q[t,h,d]*k[s,d])  if s < n_vis(positions[t])
+ *                           = -INFINITY                                      if n_vis <= s < S
+ *   columns S..ld_scores-1 are not written.
+ *
+ *   q          [T, H, D] fp16          w  [T, H] fp16        k [S, D] fp16
+ *   positions  [T] int32 (>= 0)        scores [T, ld_scores] fp32, ld_scores >= S
+ *   ratio >= 1.  The head products are accumulated in fp32 on the tensor cores and the
+ *   head sum in fp32; the full T x H x S product tensor never reaches memory.
+ *   T == 0 or S == 0 is a no-op.
+ * ------------------------------------------------------------------------- */
+int ds4x_indexer_score(const void* q, const void* w, const void* k, const int32_t* positions,
+                       int32_t T, int32_t H, int32_t D, int32_t S, int32_t ratio,
+                       float* scores, int64_t ld_scores, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * ds4x_topk — per-token exact top-k_top of the visible scores ([K] #832, [S] #2563).
+ *
+ *   For token t with n = n_vis(positions[t]):
+ *     n <= k_top : indices[t,:] = 0, 1, ..., n-1, then -1 padding (scores are not read)
+ *     n >  k_top : the k_top rows s < n with the largest scores[t*ld+s], ties broken by
+ *                  the lower row index, emitted in ascending row order.
+ *   counts[t] = min(n, k_top) when counts != NULL.
+ *
+ *   scores [T, ld_scores] fp32 (only s < n_vis is read)   indices [T, k_top] int32
+ *   counts [T] int32 or NULL
+ *   workspace: device scratch of at least ds4x_topk_workspace_bytes(T, S, k_top) bytes
+ *   (may be NULL when that is 0).  Undefined for NaN scores.
+ * ------------------------------------------------------------------------- */
+int ds4x_topk(const float* scores, int64_t ld_scores, const int32_t* positions,
+              int32_t T, int32_t S, int32_t ratio, int32_t k_top,
+              int32_t* indices, int32_t* counts,
+              void* workspace, size_t workspace_bytes, void* stream);
+
+size_t ds4x_topk_workspace_bytes(int32_t T, int32_t S, int32_t k_top);
+
+/* ---------------------------------------------------------------------------
+ * ds4x_sparse_attn — multi-query attention over the selected compressed rows ([A]).
+ *
+ *   For token t, head h, over the valid entries j of indices[t, 0..k_top-1]
+ *   (valid = 0 <= idx < S; -1 padding and out-of-range entries are skipped):
+ *     l_j          = scale * sum_d q_attn[t,h,d] * kv[idx_j, d]
+ *     out[t,h,:]   = sum_j exp(l_j - m) kv[idx_j,:] / sum_j exp(l_j - m),   m = max_j l_j
+ *     lse[t,h]     = m + log(sum_j exp(l_j - m))
+ *   A token with no valid entry gets out = 0 and lse = -INFINITY.
+ *
+ *   q_attn [T, Hq, Dkv] and kv [S, Dkv] and out [T, Hq, Dkv] all of `dtype`
+ *   indices [T, k_top] int32      lse [T, Hq] fp32 or NULL
+ *   Softmax statistics in fp32; the probabilities enter the second product in `dtype`;
+ *   out is rounded to `dtype` with round-to-nearest-even.
+ * ------------------------------------------------------------------------- */
+int ds4x_sparse_attn(const void* q_attn, const void* kv, ds4x_dtype dtype,
+                     const int32_t* indices, int32_t T, int32_t Hq, int32_t Dkv,
+                     int32_t S, int32_t k_top, float scale,
+                     void* out, float* lse, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * ds4x_index_and_attend — the whole path for one chunk of query tokens:
+ *   score (only for tokens with n_vis > k_top: the [S] shortcut) -> top-k -> attention.
+ *   Equal to ds4x_indexer_score + ds4x_topk + ds4x_sparse_attn with the same arguments;
+ *   the scores live only in `workspace` (at least ds4x_workspace_bytes(T, S, k_top)).
+ *   q, w, k fp16 as in ds4x_indexer_score; q_attn, kv, out of kv_dtype.
+ * ------------------------------------------------------------------------- */
+int ds4x_index_and_attend(const void* q, const void* w, const void* k, const int32_t* positions,
+                          const void* q_attn, const void* kv, ds4x_dtype kv_dtype,
+                          int32_t T, int32_t H, int32_t D, int32_t S, int32_t ratio,
+                          int32_t k_top, int32_t Hq, int32_t Dkv, float scale,
+                          int32_t* indices, void* out, float* lse,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+size_t ds4x_workspace_bytes(int32_t T, int32_t S, int32_t k_top);
+
+/* Human-readable name of a ds4x_status value (static storage, never NULL). */
+const char* ds4x_status_string(int status);
+
+/* Number of kernel launches issued by the most recent successful call on this host
+ * thread (for launch accounting in benchmarks). */
+int ds4x_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DS4X_H */

@@ -1,0 +1,327 @@
+/*
+ * ds4x_oracle.c — plain, slow, obviously-correct CPU oracle of the lightning-indexer
+ * path.  TEST INFRASTRUCTURE ONLY: it exists to check the CUDA library and is called
+ * only by the tests, the smoke check and the benchmark's CPU-baseline leg.  It shares
+ * no code, header, table or helper with the CUDA path.
+ *
+ * Every floating-point step is done in IEEE double and rounded once at the end.
+ * Argument order mirrors the C ABI (include/ds4x.h) but every pointer is a HOST pointer.
+ *
+ * What it follows:
+ *  - Scoring and the top-512 selection: "How I made DeepSeek 12x faster on a Mac
+ *    Studio", section "1: the kernels" (the lightning indexer scores compressed KV and
+ *    keeps the top 512 rows per token; the streaming top-k of #832 is byte-identical to
+ *    a full sort, so the selection is the exact, deterministic one computed here by a
+ *    full sort).
+ *  - The shortcut: "How I turned one oversized DeepSeek optimization into three merged
+ *    oMLX PRs", section "The three changes that merged", item 3: when every pooled row
+ *    fits inside index_topk nothing can be eliminated, scoring is skipped and the
+ *    sequential indices are built directly.
+ *  - A CPU path kept only to verify accuracy: the ds4.c overview (id.news.hada.io,
+ *    sections "Gambaran proyek dan filosofi desain" and "Backend").
+ *  - The formula (which the pages leave unstated) is this library's definition:
+ *    score[t,s] = sum_h w[t,h] * ReLU(q[t,h,:] . k[s,:]), row s visible iff
+ *    (s+1)*ratio <= p+1, ties to the lower row index, indices ascending, attention with
+ *    softmax over the selected rows and kv as both key and value.
+ *
+ * Parity pins (tests/test_oracle.py): brute force in numpy on tiny inputs, an int64
+ * recomputation of 4*score on integer inputs, a hand-worked example
+ * (tests/golden/indexer_worked_example.txt), the dominance / mask / shortcut
+ * invariants of the selection, and the closed-form attention cases (zero query ->
+ * mean of the rows, one row -> that row, two rows -> logistic weights).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define REF_F16 0
+#define REF_BF16 1
+
+/* ---- 16-bit float decoding / encoding, from the IEEE 754 binary16 and the bfloat16
+ *      bit layouts (sign | exponent | fraction). ------------------------------------ */
+
+static double ref_f16_to_double(uint16_t h) {
+  int sign = h >> 15;
+  int e = (h >> 10) & 0x1f;
+  int f = h & 0x3ff;
+  double v;
+  if (e == 0) v = ldexp((double)f, -24);               /* subnormal: f * 2^-24 */
+  else if (e == 31) v = f ? NAN : INFINITY;
+  else v = ldexp((double)(f + 1024), e - 25);          /* (1 + f/1024) * 2^(e-15) */
+  return sign ? -v : v;
+}
+
+static double ref_bf16_to_double(uint16_t b) {
+  int sign = b >> 15;
+  int e = (b >> 7) & 0xff;
+  int f = b & 0x7f;
+  double v;
+  if (e == 0) v = ldexp((double)f, -133);              /* subnormal: f * 2^-133 */
+  else if (e == 255) v = f ? NAN : INFINITY;
+  else v = ldexp((double)(f + 128), e - 134);          /* (1 + f/128) * 2^(e-127) */
+  return sign ? -v : v;
+}
+
+static double ref_to_double(uint16_t x, int dtype) {
+  return dtype == REF_F16 ? ref_f16_to_double(x) : ref_bf16_to_double(x);
+}
+
+/* Round a double to the nearest binary format value with `mant` fraction bits,
+ * exponent field width `ebits`, ties to even.  Returns the bit pattern. */
+static uint16_t ref_encode(double x, int mant, int ebits) {
+  const int bias = (1 << (ebits - 1)) - 1;
+  const int emin = 1 - bias;                         /* smallest normal exponent */
+  const int emax = bias;                             /* largest normal exponent  */
+  uint16_t sign = signbit(x) ? (uint16_t)(1u << (mant + ebits)) : 0;
+  uint16_t inf = (uint16_t)(((1u << ebits) - 1) << mant);
+  if (isnan(x)) return (uint16_t)(inf | (1u << (mant - 1)));
+  double a = fabs(x);
+  if (isinf(a)) return sign | inf;
+  int e;
+  frexp(a, &e);                                      /* a = f * 2^e, f in [0.5, 1) */
+  int E = e - 1;                                     /* a in [2^E, 2^(E+1))        */
+  if (a == 0.0 || E < emin) {                        /* subnormal quantum 2^(emin-mant) */
+    double r = nearbyint(ldexp(a, mant - emin));     /* default mode: ties to even  */
+    /* r == 2^mant rolls over to the smallest normal, which the same packing encodes */
+    return sign | (uint16_t)r;
+  }
+  double r = nearbyint(ldexp(a, mant - E));          /* in [2^mant, 2^(mant+1)]     */
+  if (r >= ldexp(1.0, mant + 1)) { r = ldexp(r, -1); E += 1; }
+  if (E > emax) return sign | inf;
+  return sign | (uint16_t)(((E + bias) << mant) | ((uint32_t)r - (1u << mant)));
+}
+
+static uint16_t ref_from_double(double x, int dtype) {
+  return dtype == REF_F16 ? ref_encode(x, 10, 5) : ref_encode(x, 7, 8);
+}
+
+/* Exposed for the oracle's own pins (exhaustive round trips in the tests). */
+double ds4x_ref_decode16(uint16_t x, int dtype) { return ref_to_double(x, dtype); }
+uint16_t ds4x_ref_encode16(double x, int dtype) { return ref_from_double(x, dtype); }
+
+/* ---- visibility ------------------------------------------------------------------ */
+
+/* Number of compressed rows visible at position p: row s is visible iff
+ * (s+1)*ratio <= p+1, clamped to the S rows that exist. */
+int64_t ds4x_ref_n_visible(int64_t p, int64_t ratio, int64_t S) {
+  if (p < 0) return 0;
+  int64_t n = (p + 1) / ratio;
+  return n < S ? n : S;
+}
+
+/* ---- scoring ----------------------------------------------------------------------- */
+
+/* Decode n 16-bit values of the given format into doubles (exact). */
+static void ref_decode_n(const uint16_t* x, int64_t n, int dtype, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = ref_to_double(x[i], dtype);
+}
+
+/* One token's scores over rows 0..S-1:
+ *   row[s] = (float) sum_h w[h] * max(0, sum_d q[h,d]*k[s,d])   for s < n,
+ *   row[s] = -INFINITY                                           for n <= s < S.
+ * qd [H*D], wd [H], kd [S*D] are the decoded inputs. */
+static void ref_score_token(const double* qd, const double* wd, const double* kd, int64_t n,
+                            int32_t H, int32_t D, int64_t S, float* row) {
+  for (int64_t s = 0; s < S; ++s) {
+    if (s >= n) { row[s] = -INFINITY; continue; }
+    const double* ks = kd + s * D;
+    double acc = 0.0;
+    for (int32_t h = 0; h < H; ++h) {
+      const double* qh = qd + (int64_t)h * D;
+      double dot = 0.0;
+      for (int32_t d = 0; d < D; ++d) dot += qh[d] * ks[d];
+      double relu = dot > 0.0 ? dot : 0.0;
+      acc += wd[h] * relu;
+    }
+    row[s] = (float)acc;                               /* one rounding, to nearest even */
+  }
+}
+
+int ds4x_ref_indexer_score(const uint16_t* q, const uint16_t* w, const uint16_t* k,
+                           const int32_t* positions, int32_t T, int32_t H, int32_t D,
+                           int32_t S, int32_t ratio, float* scores, int64_t ld_scores) {
+  if (T < 0 || H <= 0 || D <= 0 || S < 0 || ratio < 1 || ld_scores < S) return -1;
+  double* kd = (double*)malloc(sizeof(double) * (size_t)((int64_t)S * D + 1));
+  ref_decode_n(k, (int64_t)S * D, REF_F16, kd);
+#pragma omp parallel
+  {
+    double* qd = (double*)malloc(sizeof(double) * (size_t)H * D);
+    double* wd = (double*)malloc(sizeof(double) * (size_t)H);
+#pragma omp for schedule(dynamic, 1)
+    for (int32_t t = 0; t < T; ++t) {
+      ref_decode_n(q + (int64_t)t * H * D, (int64_t)H * D, REF_F16, qd);
+      ref_decode_n(w + (int64_t)t * H, H, REF_F16, wd);
+      int64_t n = ds4x_ref_n_visible(positions[t], ratio, S);
+      ref_score_token(qd, wd, kd, n, H, D, S, scores + (int64_t)t * ld_scores);
+    }
+    free(qd); free(wd);
+  }
+  free(kd);
+  return 0;
+}
+
+/* ---- top-k ------------------------------------------------------------------------- */
+
+typedef struct { float score; int32_t idx; } ref_pair;
+
+/* Order used for the selection: higher score first, equal scores -> lower row first. */
+static int ref_cmp_pair(const void* a, const void* b) {
+  const ref_pair* x = (const ref_pair*)a;
+  const ref_pair* y = (const ref_pair*)b;
+  if (x->score > y->score) return -1;
+  if (x->score < y->score) return 1;
+  return (x->idx > y->idx) - (x->idx < y->idx);
+}
+
+static int ref_cmp_int(const void* a, const void* b) {
+  int32_t x = *(const int32_t*)a, y = *(const int32_t*)b;
+  return (x > y) - (x < y);
+}
+
+/* Full selection for one token: sort all n visible (score, s) pairs, keep the first
+ * k_top, emit them in ascending row order, pad with -1.  Returns the count. */
+static int32_t ref_select_one(const float* row, int64_t n, int32_t k_top, int32_t* out) {
+  ref_pair* pairs = (ref_pair*)malloc(sizeof(ref_pair) * (size_t)(n > 0 ? n : 1));
+  for (int64_t s = 0; s < n; ++s) { pairs[s].score = row[s]; pairs[s].idx = (int32_t)s; }
+  qsort(pairs, (size_t)n, sizeof(ref_pair), ref_cmp_pair);
+  int32_t c = (int32_t)(n < k_top ? n : k_top);
+  for (int32_t i = 0; i < c; ++i) out[i] = pairs[i].idx;
+  qsort(out, (size_t)c, sizeof(int32_t), ref_cmp_int);
+  for (int32_t i = c; i < k_top; ++i) out[i] = -1;
+  free(pairs);
+  return c;
+}
+
+/* use_shortcut = 1: a token with n_vis <= k_top emits 0..n-1 without reading scores
+ * (the oMLX #2563 shortcut).  use_shortcut = 0 runs the full selection for every token
+ * (used by the tests to show that both give the same indices). */
+int ds4x_ref_topk_ex(const float* scores, int64_t ld_scores, const int32_t* positions,
+                     int32_t T, int32_t S, int32_t ratio, int32_t k_top,
+                     int32_t* indices, int32_t* counts, int use_shortcut) {
+  if (T < 0 || S < 0 || ratio < 1 || k_top < 1 || ld_scores < S) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int32_t t = 0; t < T; ++t) {
+    int64_t n = ds4x_ref_n_visible(positions[t], ratio, S);
+    int32_t* out = indices + (int64_t)t * k_top;
+    int32_t c;
+    if (use_shortcut && n <= k_top) {
+      for (int64_t i = 0; i < n; ++i) out[i] = (int32_t)i;
+      for (int64_t i = n; i < k_top; ++i) out[i] = -1;
+      c = (int32_t)n;
+    } else {
+      c = ref_select_one(scores + (int64_t)t * ld_scores, n, k_top, out);
+    }
+    if (counts) counts[t] = c;
+  }
+  return 0;
+}
+
+int ds4x_ref_topk(const float* scores, int64_t ld_scores, const int32_t* positions,
+                  int32_t T, int32_t S, int32_t ratio, int32_t k_top,
+                  int32_t* indices, int32_t* counts) {
+  return ds4x_ref_topk_ex(scores, ld_scores, positions, T, S, ratio, k_top, indices, counts, 1);
+}
+
+/* ---- sparse multi-query attention -------------------------------------------------- */
+
+/* One token: qd [Hq*Dkv] decoded query, rd [nv*Dkv] decoded selected rows.
+ *   l_j = scale * q[h,:] . row_j,  p_j = exp(l_j - max l) / sum exp(l - max l)
+ *   out[h,:] = sum_j p_j row_j (rounded once to dtype), lse[h] = max l + log(sum). */
+static void ref_attend_token(const double* qd, const double* rd, int32_t nv, int32_t Hq,
+                             int32_t Dkv, double scale, int dtype, uint16_t* out, float* lse,
+                             double* logit, double* acc) {
+  for (int32_t h = 0; h < Hq; ++h) {
+    const double* qh = qd + (int64_t)h * Dkv;
+    uint16_t* oh = out + (int64_t)h * Dkv;
+    if (nv == 0) {
+      for (int32_t d = 0; d < Dkv; ++d) oh[d] = ref_from_double(0.0, dtype);
+      if (lse) lse[h] = -INFINITY;
+      continue;
+    }
+    double m = -INFINITY;
+    for (int32_t j = 0; j < nv; ++j) {
+      const double* r = rd + (int64_t)j * Dkv;
+      double dot = 0.0;
+      for (int32_t d = 0; d < Dkv; ++d) dot += qh[d] * r[d];
+      logit[j] = scale * dot;
+      if (logit[j] > m) m = logit[j];
+    }
+    double sum = 0.0;
+    for (int32_t d = 0; d < Dkv; ++d) acc[d] = 0.0;
+    for (int32_t j = 0; j < nv; ++j) {
+      double p = exp(logit[j] - m);
+      sum += p;
+      const double* r = rd + (int64_t)j * Dkv;
+      for (int32_t d = 0; d < Dkv; ++d) acc[d] += p * r[d];
+    }
+    for (int32_t d = 0; d < Dkv; ++d) oh[d] = ref_from_double(acc[d] / sum, dtype);
+    if (lse) lse[h] = (float)(m + log(sum));
+  }
+}
+
+/* Attention for every token over its valid selected rows (0 <= idx < S; -1 and
+ * out-of-range entries are skipped).  No valid row: out = 0, lse = -inf. */
+int ds4x_ref_sparse_attn(const uint16_t* q_attn, const uint16_t* kv, int dtype,
+                         const int32_t* indices, int32_t T, int32_t Hq, int32_t Dkv,
+                         int32_t S, int32_t k_top, float scale, uint16_t* out, float* lse) {
+  if (T < 0 || Hq <= 0 || Dkv <= 0 || S < 0 || k_top < 1) return -1;
+#pragma omp parallel
+  {
+    double* qd = (double*)malloc(sizeof(double) * (size_t)Hq * Dkv);
+    double* rd = (double*)malloc(sizeof(double) * (size_t)k_top * Dkv);
+    double* logit = (double*)malloc(sizeof(double) * (size_t)k_top);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)Dkv);
+#pragma omp for schedule(dynamic, 1)
+    for (int32_t t = 0; t < T; ++t) {
+      const int32_t* sel = indices + (int64_t)t * k_top;
+      int32_t nv = 0;
+      for (int32_t j = 0; j < k_top; ++j)
+        if (sel[j] >= 0 && sel[j] < S)
+          ref_decode_n(kv + (int64_t)sel[j] * Dkv, Dkv, dtype, rd + (int64_t)(nv++) * Dkv);
+      ref_decode_n(q_attn + (int64_t)t * Hq * Dkv, (int64_t)Hq * Dkv, dtype, qd);
+      ref_attend_token(qd, rd, nv, Hq, Dkv, (double)scale, dtype,
+                       out + (int64_t)t * Hq * Dkv, lse ? lse + (int64_t)t * Hq : NULL,
+                       logit, acc);
+    }
+    free(qd); free(rd); free(logit); free(acc);
+  }
+  return 0;
+}
+
+/* ---- the whole path ----------------------------------------------------------------- */
+
+/* score -> top-k (with the shortcut) -> attention.  A token covered by the shortcut
+ * (n_vis <= k_top) is never scored. */
+int ds4x_ref_index_and_attend(const uint16_t* q, const uint16_t* w, const uint16_t* k,
+                              const int32_t* positions, const uint16_t* q_attn,
+                              const uint16_t* kv, int kv_dtype, int32_t T, int32_t H,
+                              int32_t D, int32_t S, int32_t ratio, int32_t k_top,
+                              int32_t Hq, int32_t Dkv, float scale, int32_t* indices,
+                              uint16_t* out, float* lse) {
+  if (T < 0 || H <= 0 || D <= 0 || S < 0 || ratio < 1 || k_top < 1) return -1;
+  double* kd = (double*)malloc(sizeof(double) * (size_t)((int64_t)S * D + 1));
+  ref_decode_n(k, (int64_t)S * D, REF_F16, kd);
+#pragma omp parallel
+  {
+    double* qd = (double*)malloc(sizeof(double) * (size_t)H * D);
+    double* wd = (double*)malloc(sizeof(double) * (size_t)H);
+    float* row = (float*)malloc(sizeof(float) * (size_t)(S > 0 ? S : 1));
+#pragma omp for schedule(dynamic, 1)
+    for (int32_t t = 0; t < T; ++t) {
+      int64_t n = ds4x_ref_n_visible(positions[t], ratio, S);
+      int32_t* sel = indices + (int64_t)t * k_top;
+      if (n <= k_top) {                                  /* shortcut: nothing to rank */
+        for (int64_t i = 0; i < k_top; ++i) sel[i] = i < n ? (int32_t)i : -1;
+        continue;
+      }
+      ref_decode_n(q + (int64_t)t * H * D, (int64_t)H * D, REF_F16, qd);
+      ref_decode_n(w + (int64_t)t * H, H, REF_F16, wd);
+      ref_score_token(qd, wd, kd, n, H, D, S, row);
+      ref_select_one(row, n, k_top, sel);
+    }
+    free(qd); free(wd); free(row);
+  }
+  free(kd);
+  return ds4x_ref_sparse_attn(q_attn, kv, kv_dtype, indices, T, Hq, Dkv, S, k_top, scale, out, lse);
+}

@@ -1,0 +1,362 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each check takes an ``oracle.Oracle`` and raises AssertionError when the oracle
+disagrees with the independent fact. tests/test_oracle.py runs them on the real oracle;
+tests/test_oracle_mutants.py runs them on copies of the oracle with one planted
+mistake each and requires that some check fails.
+
+Independent facts used:
+  * the IEEE binary16 / bfloat16 encodings (numpy's float16, the float32 bit layout,
+    exact rational rounding with fractions.Fraction);
+  * a hand-worked example (tests/golden/indexer_worked_example.txt);
+  * an int64 recomputation of 4*score on integer inputs (exact closed form);
+  * a float64 numpy evaluation of the definition (different summation order);
+  * brute-force ranking with Python's sorted() on tiny inputs;
+  * the selection invariants (dominance, mask, count, ascending order, shortcut);
+  * closed-form attention cases (zero query, single row, two rows) and a textbook
+    float64 numpy softmax-attention.
+"""
+from __future__ import annotations
+
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                      "indexer_worked_example.txt")
+
+
+# ----------------------------------------------------------------------------- helpers
+def _f16(x):
+    return synth.to_f16_bits(np.asarray(x, dtype=np.float64))
+
+
+def _f16_val(bits):
+    return synth.f16_bits_to_f32(bits).astype(np.float64)
+
+
+def _bits_val(bits, dtype):
+    return synth.bits_to_f32(bits, dtype).astype(np.float64)
+
+
+def parse_golden(path=GOLDEN):
+    vals = {}
+    for line in open(path):
+        line = line.split("#", 1)[0].strip()
+        if not line:
+            continue
+        key, rest = line.split(":", 1)
+        vals[key.strip()] = [float(v) for v in rest.split()]
+    return vals
+
+
+def _rand_int_case(seed, T, H, D, S, lo=-3, hi=3, w_pow2=True):
+    q = synth.uniform_int(seed, "pin/q", T * H * D, lo, hi).reshape(T, H, D)
+    k = synth.uniform_int(seed, "pin/k", S * D, lo, hi).reshape(S, D)
+    sel = synth.uniform_int(seed, "pin/w", T * H, 0, 2)
+    w4 = np.array([1, 2, 4])[sel].reshape(T, H)  # 4*w with w in {1/4, 1/2, 1}
+    return q, k, w4
+
+
+def _brute_topk(row, n, k_top):
+    order = sorted(range(n), key=lambda s: (-row[s], s))
+    sel = sorted(order[:k_top])
+    return sel + [-1] * (k_top - len(sel))
+
+
+# ------------------------------------------------------------------- number formats
+def check_f16_decode_exhaustive(o):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([o.decode16(int(b), "f16") for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def check_bf16_decode_exhaustive(o):
+    bits = np.arange(65536, dtype=np.uint32)
+    with np.errstate(invalid="ignore"):
+        ref = (bits << 16).astype(np.uint32).view(np.float32).astype(np.float64)
+    got = np.array([o.decode16(int(b), "bf16") for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def _rne_fraction(x: Fraction, mant: int, ebits: int):
+    """Exact round-to-nearest-even of a rational into a binary format, as a Fraction
+    (or +-inf)."""
+    bias = (1 << (ebits - 1)) - 1
+    emin, emax = 1 - bias, bias
+    a = abs(x)
+    if a == 0:
+        return Fraction(0)
+    E = math.floor(math.log2(a))
+    while Fraction(2) ** E > a:
+        E -= 1
+    while Fraction(2) ** (E + 1) <= a:
+        E += 1
+    E = max(E, emin)
+    q = Fraction(2) ** (E - mant)
+    m = a / q
+    r = math.floor(m)
+    rem = m - r
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and r % 2 == 1):
+        r += 1
+    val = r * q
+    if val >= Fraction(2) ** (emax + 1):
+        return math.inf if x > 0 else -math.inf
+    return val if x > 0 else -val
+
+
+def check_encode_rne(o):
+    rng = np.random.default_rng(7)
+    # random magnitudes across the normal and subnormal ranges, plus exact ties
+    xs = list(rng.standard_normal(400) * np.exp2(rng.integers(-30, 18, 400)))
+    xs += [1 + 2 ** -11, 1 + 3 * 2 ** -11, 2 ** -25, 3 * 2 ** -25, 65519.0, 65520.0, 1e-9, -0.0,
+           0.880797077977882, 1 + 2 ** -8, 1 + 3 * 2 ** -8, 2 ** -134, 3 * 2 ** -134]
+    for x in xs:
+        for dtype, mant, ebits in (("f16", 10, 5), ("bf16", 7, 8)):
+            got = o.decode16(o.encode16(float(x), dtype), dtype)
+            want = _rne_fraction(Fraction(float(x)), mant, ebits)
+            if isinstance(want, float):
+                assert got == want, (x, dtype, got, want)
+            else:
+                assert Fraction(got) == want, (x, dtype, got, float(want))
+    # numpy's double -> half conversion (round to nearest even) as a second witness
+    ys = rng.standard_normal(2000) * np.exp2(rng.integers(-26, 16, 2000))
+    with np.errstate(over="ignore"):
+        ref = ys.astype(np.float16).view(np.uint16)
+    got = np.array([o.encode16(float(y), "f16") for y in ys], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+
+
+# ------------------------------------------------------------------------ visibility
+def check_visibility(o):
+    # row s visible iff (s+1)*ratio <= p+1, counted by brute force
+    for ratio in (1, 2, 4, 128):
+        for S in (0, 1, 7, 300):
+            for p in list(range(0, 40)) + [511, 512, 4095, 65535]:
+                brute = sum(1 for s in range(S) if (s + 1) * ratio <= p + 1)
+                assert o.n_visible(p, ratio, S) == brute, (p, ratio, S)
+
+
+# ------------------------------------------------------------------ worked example
+def check_golden_example(o):
+    g = parse_golden()
+    T, H, D, S = (int(g[k][0]) for k in ("T", "H", "D", "S"))
+    ratio, k_top = int(g["ratio"][0]), int(g["k_top"][0])
+    pos = np.array(g["positions"], dtype=np.int32)
+    q = _f16(np.array(g["q"]).reshape(T, H, D))
+    w = _f16(np.array(g["w"]).reshape(T, H))
+    k = _f16(np.array(g["k"]).reshape(S, D))
+    sc = o.indexer_score(q, w, k, pos, ratio)
+    want = np.array(g["scores"], dtype=np.float32).reshape(T, S)
+    assert np.array_equal(sc, want), (sc, want)
+    idx, cnt = o.topk(sc, pos, S, ratio, k_top)
+    assert np.array_equal(idx, np.array(g["indices"], dtype=np.int32).reshape(T, k_top)), idx
+    assert np.array_equal(cnt, np.array(g["counts"], dtype=np.int32)), cnt
+    Hq, Dkv = int(g["attn_Hq"][0]), int(g["attn_Dkv"][0])
+    kv = _f16(np.array(g["attn_kv"]).reshape(-1, Dkv))
+    qa = _f16(np.array(g["attn_q"]).reshape(T, Hq, Dkv))
+    ai = np.array(g["attn_indices"], dtype=np.int32).reshape(T, -1)
+    out, lse = o.sparse_attn(qa, kv, "f16", ai, kv.shape[0], float(g["attn_scale"][0]))
+    want_out = np.array(g["attn_out"]).reshape(T, Hq, Dkv)
+    assert np.array_equal(_f16_val(out), want_out), (_f16_val(out), want_out)
+    want_lse = np.array(g["attn_lse"], dtype=np.float64).reshape(T, Hq)
+    fin = np.isfinite(want_lse)
+    assert np.array_equal(np.isinf(lse), ~fin)
+    assert np.allclose(lse[fin], want_lse[fin], rtol=1e-6, atol=0)
+    idx2, out2, lse2 = o.index_and_attend(q, w, k, pos, _f16(np.zeros((T, 64, 8))),
+                                          _f16(np.zeros((S, 8))), "f16", S, ratio, k_top, 1.0)
+    assert np.array_equal(idx2, idx)
+
+
+# ------------------------------------------------------------------------- scoring
+def check_scores_int64_closed_form(o):
+    T, H, D, S, ratio = 9, 16, 64, 70, 4
+    q, k, w4 = _rand_int_case(11, T, H, D, S)
+    pos = np.array([0, 3, 4, 100, 150, 255, 279, 280, 400], dtype=np.int32)
+    sc = o.indexer_score(_f16(q), _f16(w4 / 4.0), _f16(k), pos, ratio, ld=S + 3)
+    dots = np.einsum("thd,sd->ths", q.astype(np.int64), k.astype(np.int64))
+    four = (w4[:, :, None].astype(np.int64) * np.maximum(dots, 0)).sum(axis=1)  # 4*score
+    for t in range(T):
+        n = min(S, (int(pos[t]) + 1) // ratio)
+        assert np.array_equal(sc[t, :n].astype(np.float64) * 4.0, four[t, :n].astype(np.float64))
+        assert np.all(np.isneginf(sc[t, n:S]))
+        assert np.all(np.isnan(sc[t, S:]))  # columns past S are never written
+
+
+def check_scores_float_vs_numpy(o):
+    T, H, D, S, ratio = 5, 8, 32, 40, 2
+    rng = np.random.default_rng(3)
+    q = _f16(rng.standard_normal((T, H, D)))
+    k = _f16(rng.standard_normal((S, D)))
+    w = _f16(rng.standard_normal((T, H)))         # signed weights
+    pos = np.array([10, 30, 50, 79, 200], dtype=np.int32)
+    sc = o.indexer_score(q, w, k, pos, ratio)
+    qf, kf, wf = _f16_val(q), _f16_val(k), _f16_val(w)
+    ref = np.einsum("th,ths->ts", wf, np.maximum(np.einsum("thd,sd->ths", qf, kf), 0.0))
+    for t in range(T):
+        n = min(S, (int(pos[t]) + 1) // ratio)
+        assert np.allclose(sc[t, :n], ref[t, :n], rtol=2e-7, atol=1e-12)
+        assert np.all(np.isneginf(sc[t, n:]))
+
+
+# --------------------------------------------------------------------------- top-k
+def check_topk_brute_force(o):
+    rng = np.random.default_rng(5)
+    for trial in range(12):
+        T = 6
+        S = int(rng.integers(1, 60))
+        ratio = int(rng.choice([1, 2, 4]))
+        k_top = int(rng.choice([1, 2, 5, 8, 16]))
+        # few distinct values -> many ties
+        sc = rng.integers(-4, 5, size=(T, S)).astype(np.float32) * 0.5
+        pos = rng.integers(0, S * ratio + 5, size=T).astype(np.int32)
+        idx, cnt = o.topk(sc, pos, S, ratio, k_top)
+        for t in range(T):
+            n = min(S, (int(pos[t]) + 1) // ratio)
+            want = _brute_topk(list(sc[t]), n, k_top)
+            assert list(idx[t]) == want, (trial, t, list(idx[t]), want)
+            assert cnt[t] == min(n, k_top)
+
+
+def check_topk_invariants(o):
+    wl = synth.WORKLOADS["tiny_exact"]
+    inp = synth.make_inputs(wl, seed=0, T=24)
+    sc = o.indexer_score(inp.q, inp.w, inp.k, inp.positions, wl.ratio, S=wl.S)
+    idx, cnt = o.topk(sc, inp.positions, wl.S, wl.ratio, wl.k_top)
+    for t in range(idx.shape[0]):
+        n = min(wl.S, (int(inp.positions[t]) + 1) // wl.ratio)
+        sel = idx[t][idx[t] >= 0]
+        assert len(sel) == min(n, wl.k_top) == cnt[t]
+        assert np.all(np.diff(sel) > 0)                      # ascending, distinct
+        assert np.all(sel < n)                               # masked rows never chosen
+        if n > wl.k_top:
+            chosen = np.zeros(n, dtype=bool)
+            chosen[sel] = True
+            lo = sc[t, :n][chosen].min()
+            hi = sc[t, :n][~chosen].max()
+            assert lo >= hi                                  # dominance
+            if lo == hi:                                     # ties go to the lower row
+                assert np.nonzero(chosen & (sc[t, :n] == lo))[0].max() < \
+                    np.nonzero(~chosen & (sc[t, :n] == hi))[0].min()
+
+
+def check_shortcut(o):
+    S, ratio, k_top = 600, 1, 512
+    rng = np.random.default_rng(9)
+    sc = rng.standard_normal((8, S)).astype(np.float32)
+    pos = np.array([0, 1, 2, 100, 510, 511, 512, 599], dtype=np.int32)  # n = 1,2,3,101,511,512,513,600
+    a, ca = o.topk(sc, pos, S, ratio, k_top, shortcut=True)
+    b, cb = o.topk(sc, pos, S, ratio, k_top, shortcut=False)
+    for t in range(8):
+        n = min(S, int(pos[t]) + 1)
+        if n <= k_top:
+            assert list(a[t]) == list(range(n)) + [-1] * (k_top - n)
+    assert np.array_equal(a, b) and np.array_equal(ca, cb)
+    # a token that sees nothing
+    z, cz = o.topk(sc[:1], np.array([-1], dtype=np.int32), S, ratio, k_top)
+    assert np.all(z == -1) and cz[0] == 0
+
+
+# ----------------------------------------------------------------------- attention
+def check_attn_zero_query_is_mean(o):
+    rng = np.random.default_rng(1)
+    S, Dkv, Hq = 40, 16, 3
+    kv = synth.to_bf16_bits(rng.standard_normal((S, Dkv)))
+    qa = np.zeros((2, Hq, Dkv), dtype=np.uint16)           # +0.0 bits
+    ind = np.array([[3, 7, 11, 20, 39, -1], [0, 1, 2, 5, 8, 13]], dtype=np.int32)
+    out, lse = o.sparse_attn(qa, kv, "bf16", ind, S, 0.3)
+    kvf = _bits_val(kv, "bf16")
+    for t in range(2):
+        rows = [i for i in ind[t] if i >= 0]
+        # equal logits -> equal weights: the exact rational mean, rounded to nearest even
+        mean = [_rne_fraction(sum(Fraction(float(v)) for v in kvf[rows, d]) / len(rows), 7, 8)
+                for d in range(Dkv)]
+        for h in range(Hq):
+            got = _bits_val(out[t, h], "bf16")
+            assert all(Fraction(float(g)) == m for g, m in zip(got, mean)), (got, mean)
+            assert abs(lse[t, h] - math.log(len(rows))) < 1e-6
+
+
+def check_attn_single_row(o):
+    rng = np.random.default_rng(2)
+    S, Dkv, Hq = 10, 32, 4
+    kv = synth.to_f16_bits(rng.standard_normal((S, Dkv)))
+    qa = synth.to_f16_bits(rng.standard_normal((3, Hq, Dkv)))
+    ind = np.array([[4, -1, -1], [-1, 9, -1], [-1, -1, 0]], dtype=np.int32)
+    out, lse = o.sparse_attn(qa, kv, "f16", ind, S, 0.125)
+    for t, r in enumerate([4, 9, 0]):
+        for h in range(Hq):
+            assert np.array_equal(out[t, h], kv[r])          # softmax of one logit is 1
+            logit = 0.125 * float(np.dot(_f16_val(qa[t, h]), _f16_val(kv[r])))
+            assert abs(lse[t, h] - logit) <= 1e-6 * max(1.0, abs(logit))
+
+
+def check_attn_two_rows_logistic(o):
+    # rows e0 and e1, q = [a, b]: p1 = 1/(1 + exp(-(b-a)*scale)), out = [1-p1, p1]
+    S, Dkv = 2, 8
+    kv = np.zeros((S, Dkv)); kv[0, 0] = 1; kv[1, 1] = 1
+    cases = [(0.0, 1.0), (2.0, -1.0), (0.5, 0.5), (-3.0, 4.0)]
+    qa = np.zeros((len(cases), 1, Dkv))
+    for i, (a, b) in enumerate(cases):
+        qa[i, 0, 0], qa[i, 0, 1] = a, b
+    ind = np.array([[0, 1]] * len(cases), dtype=np.int32)
+    out, lse = o.sparse_attn(_f16(qa), _f16(kv), "f16", ind, S, 0.75)
+    for i, (a, b) in enumerate(cases):
+        p1 = 1.0 / (1.0 + math.exp(-(b - a) * 0.75))
+        want = np.zeros(Dkv); want[0], want[1] = 1 - p1, p1
+        assert np.array_equal(out[i, 0], _f16(want)), (out[i, 0], want)
+        assert abs(lse[i, 0] - math.log(math.exp(0.75 * a) + math.exp(0.75 * b))) < 1e-6
+
+
+def check_attn_vs_textbook(o):
+    rng = np.random.default_rng(4)
+    S, Dkv, Hq, T, k_top = 50, 64, 8, 3, 12
+    kv = synth.to_bf16_bits(rng.standard_normal((S, Dkv)))
+    qa = synth.to_bf16_bits(rng.standard_normal((T, Hq, Dkv)))
+    ind = np.stack([rng.choice(S, k_top, replace=False) for _ in range(T)]).astype(np.int32)
+    ind[1, -3:] = -1
+    ind[2, 0] = S + 5                                        # out of range -> skipped
+    scale = 1.0 / math.sqrt(Dkv)
+    out, lse = o.sparse_attn(qa, kv, "bf16", ind, S, scale)
+    kvf, qf = _bits_val(kv, "bf16"), _bits_val(qa, "bf16")
+    for t in range(T):
+        rows = [int(i) for i in ind[t] if 0 <= i < S]
+        V = kvf[rows]
+        logits = scale * qf[t] @ V.T                         # [Hq, n]
+        m = logits.max(axis=1, keepdims=True)
+        p = np.exp(logits - m)
+        ref = (p / p.sum(axis=1, keepdims=True)) @ V
+        assert np.allclose(_bits_val(out[t], "bf16"), ref, rtol=2 ** -8, atol=1e-6)
+        assert np.allclose(lse[t], (m[:, 0] + np.log(p.sum(axis=1))), rtol=1e-6, atol=1e-6)
+
+
+def check_index_and_attend_composes(o):
+    wl = synth.WORKLOADS["tiny_exact"]
+    inp = synth.make_inputs(wl, seed=0, T=6, S=1024)
+    # include tokens that take the shortcut (positions below k_top*ratio)
+    pos = np.array([5, 2047, 2048, 2051, 4000, 4095], dtype=np.int32)
+    idx, out, lse = o.index_and_attend(inp.q, inp.w, inp.k, pos, inp.q_attn, inp.kv, "f16",
+                                       wl.S, wl.ratio, wl.k_top, wl.scale)
+    sc = o.indexer_score(inp.q, inp.w, inp.k, pos, wl.ratio, S=wl.S)
+    idx2, _ = o.topk(sc, pos, wl.S, wl.ratio, wl.k_top)
+    out2, lse2 = o.sparse_attn(inp.q_attn, inp.kv, "f16", idx2, wl.S, wl.scale)
+    assert np.array_equal(idx, idx2)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+ALL_CHECKS = [
+    check_f16_decode_exhaustive, check_bf16_decode_exhaustive, check_encode_rne,
+    check_visibility, check_golden_example, check_scores_int64_closed_form,
+    check_scores_float_vs_numpy, check_topk_brute_force, check_topk_invariants,
+    check_shortcut, check_attn_zero_query_is_mean, check_attn_single_row,
+    check_attn_two_rows_logistic, check_attn_vs_textbook, check_index_and_attend_composes,
+]

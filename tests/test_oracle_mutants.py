@@ -1,0 +1,59 @@
+"""Each planted mistake in a copy of the oracle must make at least one pin fail.
+
+The mutants are plausible slips (a dropped term, a wrong sign or index, a reversed
+tie-break, a transposed operand, ...). They are compiled from a textual edit of
+oracle/ds4x_oracle.c into a temporary library; the oracle source itself is untouched.
+"""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "ds4x_oracle.c")
+
+MUTANTS = {
+    "relu_after_weight": ("double relu = dot > 0.0 ? dot : 0.0;\n      acc += wd[h] * relu;",
+                          "acc += (wd[h] * dot > 0.0 ? wd[h] * dot : 0.0);"),
+    "no_relu": ("double relu = dot > 0.0 ? dot : 0.0;", "double relu = dot;"),
+    "visibility_off_by_one": ("int64_t n = (p + 1) / ratio;", "int64_t n = p / ratio;"),
+    "tie_to_higher_row": ("return (x->idx > y->idx) - (x->idx < y->idx);",
+                          "return (x->idx < y->idx) - (x->idx > y->idx);"),
+    "ascending_order_dropped": ("qsort(out, (size_t)c, sizeof(int32_t), ref_cmp_int);", ";"),
+    "dropped_last_dim": ("for (int32_t d = 0; d < D; ++d) dot += qh[d] * ks[d];",
+                         "for (int32_t d = 0; d + 1 < D; ++d) dot += qh[d] * ks[d];"),
+    "transposed_q_index": ("const double* qh = qd + (int64_t)h * D;", "const double* qh = qd + h;"),
+    "mask_not_applied": ("if (s >= n) { row[s] = -INFINITY; continue; }", ";"),
+    "attn_scale_dropped": ("logit[j] = scale * dot;", "logit[j] = dot;"),
+    "attn_not_normalised": ("oh[d] = ref_from_double(acc[d] / sum, dtype);",
+                            "oh[d] = ref_from_double(acc[d], dtype);"),
+    "attn_max_sign": ("double p = exp(logit[j] - m);", "double p = exp(m - logit[j]);"),
+    "lse_without_max": ("lse[h] = (float)(m + log(sum));", "lse[h] = (float)(log(sum));"),
+    "encode_truncates": ("double r = nearbyint(ldexp(a, mant - E));",
+                         "double r = floor(ldexp(a, mant - E));"),
+    "f16_exponent_bias": ("else v = ldexp((double)(f + 1024), e - 25);",
+                          "else v = ldexp((double)(f + 1024), e - 24);"),
+    "shortcut_wrong_count": ("for (int64_t i = 0; i < n; ++i) out[i] = (int32_t)i;",
+                             "for (int64_t i = 0; i < n; ++i) out[i] = (int32_t)(i + 1);"),
+    "w_index_transposed": ("ref_decode_n(w + (int64_t)t * H, H, REF_F16, wd);\n      int64_t n",
+                           "ref_decode_n(w + (int64_t)t, H, REF_F16, wd);\n      int64_t n"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(src.replace(old, new, 1))
+    lib = oracle.build(force=True, src=str(mutated), out=str(tmp_path / "libmutant.so"))
+    o = oracle.Oracle(lib)
+    failed = []
+    for check in oracle_pins.ALL_CHECKS:
+        try:
+            check(o)
+        except (AssertionError, ValueError, IndexError):
+            failed.append(check.__name__)
+    assert failed, f"no pin catches the planted mistake {name}"
