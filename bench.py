@@ -1,0 +1,423 @@
+"""Benchmark of the lightning-indexer path: score -> top-512 -> sparse MQA.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one pass of the whole path over one 2048-token prefill chunk (default workload
+prefill_8k: 2048 query tokens at positions 6144..8191, 2048 compressed rows, 64 indexer heads
+x 128 dims, 64 attention heads x 512 dims, k_top = 512).  Inputs are synthetic (seeded), held
+in HBM before the timed region; L2 is flushed (a 256 MiB write) before every timed step.
+
+Printed (one JSON line, rank 0): the whole-job throughput in query tokens/s timed with CUDA
+events on the launching stream, per-stage times, the dominant kernel against its roofline
+(peaks from MEASURED_PEAKS.json), the same metric end to end through the C ABI with pinned
+host buffers (copies inside the timed region), the oracle timed on the host cores as a
+reported baseline, SM clocks sampled during the timed region, and the launch count.
+
+With --impl reference the oracle (plain C, fp64) is timed instead, on a bounded sample of
+the same workload per step.  Under torchrun (--gpus N), every rank runs its own chunk (the
+path shards over query tokens with no exchange), the timed region is bracketed by barriers
+and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "indexed query tokens/s (score+top-512+sparse attn) at 8k–64k ctx; % roofline"
+UNIT = "query tokens/s"
+DEFAULT_WORKLOAD = "prefill_8k"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ds4x", choices=["ds4x", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--seed", type=int, default=0)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_config(wl: synth.Workload, l2_note: str) -> dict:
+    return {
+        "workload": f"{wl.name}: {wl.T} query tokens at positions {wl.pos0}..{wl.pos0 + wl.T - 1}, "
+                    f"ratio {wl.ratio} -> {wl.S} compressed rows; indexer q[{wl.T},{wl.H},{wl.D}] fp16, "
+                    f"k[{wl.S},{wl.D}] fp16, w[{wl.T},{wl.H}] fp16; top-{wl.k_top}; sparse MQA "
+                    f"{wl.Hq} heads x {wl.Dkv} over kv[{wl.S},{wl.Dkv}] {wl.kv_dtype}",
+        "T": wl.T, "S": wl.S, "H": wl.H, "D": wl.D, "ratio": wl.ratio, "k_top": wl.k_top,
+        "Hq": wl.Hq, "Dkv": wl.Dkv, "kv_dtype": wl.kv_dtype, "seed": 0,
+        "l2": l2_note,
+    }
+
+
+def visible_rows(wl: synth.Workload) -> np.ndarray:
+    p = wl.pos0 + np.arange(wl.T, dtype=np.int64)
+    return np.minimum(wl.S, (p + 1) // wl.ratio)
+
+
+def algorithmic(wl: synth.Workload) -> dict:
+    nv = visible_rows(wl)
+    scored = nv[nv > wl.k_top]
+    sel = np.minimum(nv, wl.k_top)
+    return {
+        # scoring: one multiply-add per (token, head, dim, visible row)
+        "score_flops": float(2 * wl.H * wl.D * scored.sum()),
+        # top-k: read every visible score once, write k_top indices per token
+        "topk_bytes": float(4 * scored.sum() + 4 * wl.k_top * wl.T),
+        # attention: two products of 2*Hq*Dkv flops per (token, selected row)
+        "attn_flops": float(4 * wl.Hq * wl.Dkv * sel.sum()),
+        "attn_gather_bytes": float(2 * wl.Dkv * sel.sum()),
+    }
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current
+    kernel source (a source hash is stored beside the counters)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path))
+        e = d[workload][kernel]
+        src = os.path.join(ROOT, "deepseek_v4_sparse_gb300", "csrc", e["source"])
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return float(e["dram_bytes_per_launch"]) if h == e["source_sha256_16"] else None
+    except (KeyError, ValueError, OSError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="ds4x_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+def cpu_baseline(wl: synth.Workload, inp, target_s: float = 12.0, first: int = 16):
+    """The oracle as it stands (whole path, fp64, OpenMP over tokens) on a bounded sample of
+    the workload's tokens; returns (tokens/s, threads, description)."""
+    import oracle
+    o = oracle.default()
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+    def run(n):
+        sel = np.linspace(0, wl.T - 1, n).astype(np.int64)
+        t0 = time.perf_counter()
+        o.index_and_attend(inp.q[sel], inp.w[sel], inp.k, inp.positions[sel], inp.q_attn[sel], inp.kv,
+                           wl.kv_dtype, wl.S, wl.ratio, wl.k_top, wl.scale)
+        return time.perf_counter() - t0
+
+    dt = run(first)
+    n = int(min(wl.T, max(first, first * target_s / max(dt, 1e-3))))
+    n = max(threads, (n // threads) * threads)
+    n = min(n, wl.T)
+    dt = run(n)
+    return n / dt, threads, f"{n} of the {wl.T} tokens (evenly spaced), whole path, OpenMP {threads} threads"
+
+
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    inp = synth.make_inputs(wl, seed=args.seed)
+    import oracle
+    o = oracle.default()
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    per_step = max(threads, 16)
+    rng = np.random.default_rng(0)
+
+    def step():
+        sel = np.sort(rng.choice(wl.T, per_step, replace=False))
+        o.index_and_attend(inp.q[sel], inp.w[sel], inp.k, inp.positions[sel], inp.q_attn[sel], inp.kv,
+                           wl.kv_dtype, wl.S, wl.ratio, wl.k_top, wl.scale)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = per_step * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(wl, "host run (no GPU)"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{per_step} random tokens of the {wl.T}-token chunk per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------- GPU arm
+def main():
+    args = parse()
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+
+    import torch
+    import torch.distributed as dist
+
+    import deepseek_v4_sparse_gb300 as ds4x
+    from deepseek_v4_sparse_gb300 import build as ds4x_build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or not os.path.exists(ds4x.LIB_PATH):
+        ds4x_build.build()
+    if world > 1:
+        dist.barrier()
+    ds4x.load()
+
+    # every rank processes its own chunk: same shapes, its own seed
+    inp = synth.make_inputs(wl, seed=args.seed + rank)
+    # inputs on the host (pinned, for the end-to-end leg) and on the device
+    def pinned16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory()
+    h = {"q": pinned16(inp.q), "w": pinned16(inp.w), "k": pinned16(inp.k), "q_attn": pinned16(inp.q_attn),
+         "kv": pinned16(inp.kv), "positions": torch.from_numpy(inp.positions.copy()).pin_memory()}
+    kvt = torch.bfloat16 if wl.kv_dtype == "bf16" else torch.float16
+    dt_of = {"q": torch.float16, "w": torch.float16, "k": torch.float16, "q_attn": kvt, "kv": kvt,
+             "positions": torch.int32}
+    d = {n: h[n].to(dev).view(dt_of[n]) for n in h}
+    T, S, k_top = wl.T, wl.S, wl.k_top
+    scores = torch.empty((T, S), dtype=torch.float32, device=dev)
+    idx = torch.empty((T, k_top), dtype=torch.int32, device=dev)
+    cnt = torch.empty((T,), dtype=torch.int32, device=dev)
+    out = torch.empty_like(d["q_attn"])
+    lse = torch.empty((T, wl.Hq), dtype=torch.float32, device=dev)
+    ws = torch.empty((max(1, ds4x.workspace_bytes(T, S, k_top)),), dtype=torch.uint8, device=dev)
+    tws_n = ds4x.topk_workspace_bytes(T, S, k_top)
+    tws = torch.empty((max(1, tws_n),), dtype=torch.uint8, device=dev) if tws_n else None
+    flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def fused():
+        ds4x.index_and_attend(d["q"], d["w"], d["k"], d["positions"], d["q_attn"], d["kv"], wl.ratio, k_top,
+                              S=S, scale=wl.scale, indices=idx, out=out, lse=lse, workspace=ws, stream=stream)
+        return ds4x.last_launch_count()
+
+    def staged(ev):
+        ev[0].record(stream)
+        ds4x.indexer_score(d["q"], d["w"], d["k"], d["positions"], wl.ratio, scores=scores, S=S, stream=stream)
+        n = ds4x.last_launch_count()
+        ev[1].record(stream)
+        ds4x.topk(scores, d["positions"], S, wl.ratio, k_top, indices=idx, counts=cnt, workspace=tws,
+                  stream=stream)
+        n += ds4x.last_launch_count()
+        ev[2].record(stream)
+        ds4x.sparse_attn(d["q_attn"], d["kv"], idx, S=S, scale=wl.scale, out=out, lse=lse, stream=stream)
+        n += ds4x.last_launch_count()
+        ev[3].record(stream)
+        return n
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---------------------------------------------------------------- warm-up
+    for _ in range(max(3, args.warmup)):
+        fused()
+        staged([torch.cuda.Event(enable_timing=True) for _ in range(4)])
+    torch.cuda.synchronize()
+    assert ds4x.device_status() == ds4x.OK, "a bounded device wait timed out during warm-up"
+
+    # ------------------------------------------------- timed region (device-resident)
+    launches = 0
+    sampler = ClockSampler(local)
+    with sampler:
+        barrier()
+        fused_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in range(args.steps)]
+        stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            fused_ev[i][0].record(stream)
+            launches += fused()
+            fused_ev[i][1].record(stream)
+        for i in range(args.steps):
+            flush.zero_()
+            launches += staged(stage_ev[i])
+        barrier()
+    fused_ms = [a.elapsed_time(b) for a, b in fused_ev]
+    stage_ms = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in stage_ev])
+    step_ms = float(np.mean(fused_ms))
+    if world > 1:
+        t = torch.tensor([step_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    assert ds4x.device_status() == ds4x.OK, "a bounded device wait timed out during the timed region"
+
+    # ------------------------------------------- end to end through the C ABI (host buffers)
+    e2e = None
+    if not args.no_e2e:
+        h_out = torch.empty(out.shape, dtype=torch.int16).pin_memory()
+        h_idx = torch.empty(idx.shape, dtype=torch.int32).pin_memory()
+        h_lse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        h2d = sum(h[n].numel() * h[n].element_size() for n in h)
+        d2h = h_out.numel() * 2 + h_idx.numel() * 4 + h_lse.numel() * 4
+        e_steps = max(3, min(args.steps, 10))
+
+        def e2e_step():
+            for n in h:
+                d[n].view(h[n].dtype).copy_(h[n], non_blocking=True)
+            fused()
+            h_out.copy_(out.view(torch.int16), non_blocking=True)
+            h_idx.copy_(idx, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+
+        e2e_step()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e_ms = e0.elapsed_time(e1) / e_steps
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * T / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms}
+
+    # ------------------------------------------------------------------ roofline
+    alg = algorithmic(wl)
+    peaks = load_peaks()
+    st_mean = stage_ms.mean(axis=0)
+    stages = {"score_ms": float(st_mean[0]), "topk_ms": float(st_mean[1]), "attn_ms": float(st_mean[2])}
+    dom = int(np.argmax(st_mean))
+    if dom == 0:
+        ach = alg["score_flops"] / (st_mean[0] / 1e3) / 1e12
+        roof = {"kernel": "score_kernel (tcgen05)", "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "algorithmic": alg["score_flops"], "traffic": profiled_traffic("score", wl.name)}
+    elif dom == 1:
+        ach = alg["topk_bytes"] / (st_mean[1] / 1e3) / 1e9
+        roof = {"kernel": "topk_row_kernel", "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "algorithmic": alg["topk_bytes"], "traffic": profiled_traffic("topk", wl.name)}
+    else:
+        ach = alg["attn_flops"] / (st_mean[2] / 1e3) / 1e12
+        roof = {"kernel": "sparse_mqa_kernel (tcgen05)", "bound": "tensor", "achieved": ach,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "algorithmic": alg["attn_flops"],
+                "traffic": profiled_traffic("attn", wl.name)}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["peak_source"] = f"{peaks['source']} (burst)"
+    others = {
+        "score_tflops": alg["score_flops"] / (st_mean[0] / 1e3) / 1e12,
+        "topk_gbs": alg["topk_bytes"] / (st_mean[1] / 1e3) / 1e9,
+        "attn_tflops": alg["attn_flops"] / (st_mean[2] / 1e3) / 1e12,
+        "attn_gather_gbs": alg["attn_gather_bytes"] / (st_mean[2] / 1e3) / 1e9,
+    }
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        v, cores, desc = cpu_baseline(wl, inp)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": world * T / (step_ms / 1e3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16+bf16 (fp32 accumulate)",
+            "data": "synthetic",
+            "config": dict(workload_config(wl, "flushed before every timed step (256 MiB write)"),
+                           parallelism=f"dp{world} (independent chunks per GPU)" if world > 1 else "single GPU"),
+            "roofline": roof, "stage_ms": stages, "stage_rates": others,
+            "staged_ms_per_step": float(stage_ms.sum(axis=1).mean()),
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
+            "clocks": sampler.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

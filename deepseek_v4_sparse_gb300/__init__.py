@@ -1,0 +1,230 @@
+"""Python binding of libds4x.so — the GB300 lightning-indexer path.
+
+Thin argument marshalling over the C ABI declared in include/ds4x.h: torch tensors
+(device memory) are passed as raw pointers together with the current CUDA stream; every
+step of the computation runs in the library's CUDA kernels. There is no fallback: if
+libds4x.so has not been built (``python -c "import __graft_entry__ as g; g.build()"``)
+every call raises.
+
+Entry points (same names as the C ABI, without the ``ds4x_`` prefix):
+  indexer_score, topk, sparse_attn, index_and_attend, workspace_bytes,
+  topk_workspace_bytes, device_status, selftest_bounded_wait, last_launch_count
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libds4x.so")
+
+OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
+F16, BF16 = 0, 1
+MAX_KTOP = 1024
+EXPORTS = (
+    "ds4x_indexer_score", "ds4x_topk", "ds4x_topk_workspace_bytes", "ds4x_sparse_attn",
+    "ds4x_index_and_attend", "ds4x_workspace_bytes", "ds4x_status_string",
+    "ds4x_last_launch_count", "ds4x_device_status", "ds4x_selftest_bounded_wait",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Ds4xError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+        self.status = status
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libds4x.so (once) and declare the C signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"libds4x.so is not built ({path}); run deepseek_v4_sparse_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        lib.ds4x_indexer_score.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P, i64, P]
+        lib.ds4x_topk.argtypes = [P, i64, P, i32, i32, i32, i32, P, P, P, sz, P]
+        lib.ds4x_topk_workspace_bytes.argtypes = [i32, i32, i32]
+        lib.ds4x_topk_workspace_bytes.restype = sz
+        lib.ds4x_sparse_attn.argtypes = [P, P, ctypes.c_int, P, i32, i32, i32, i32, i32, f32, P, P, P]
+        lib.ds4x_index_and_attend.argtypes = [P, P, P, P, P, P, ctypes.c_int, i32, i32, i32, i32, i32,
+                                              i32, i32, i32, f32, P, P, P, P, sz, P]
+        lib.ds4x_workspace_bytes.argtypes = [i32, i32, i32]
+        lib.ds4x_workspace_bytes.restype = sz
+        lib.ds4x_status_string.argtypes = [ctypes.c_int]
+        lib.ds4x_status_string.restype = ctypes.c_char_p
+        lib.ds4x_last_launch_count.argtypes = []
+        lib.ds4x_device_status.argtypes = [P, ctypes.c_int]
+        lib.ds4x_selftest_bounded_wait.argtypes = [i64, P]
+        for f in ("ds4x_indexer_score", "ds4x_topk", "ds4x_sparse_attn", "ds4x_index_and_attend",
+                  "ds4x_last_launch_count", "ds4x_device_status", "ds4x_selftest_bounded_wait"):
+            getattr(lib, f).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().ds4x_status_string(status).decode()
+
+
+def _check(fn: str, rc: int):
+    if rc != OK:
+        raise Ds4xError(fn, rc)
+
+
+# ---------------------------------------------------------------------------- torch helpers
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    torch = _torch()
+    if isinstance(t, torch.Tensor):
+        if not t.is_cuda:
+            raise ValueError("tensors passed to libds4x must live on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensors passed to libds4x must be contiguous")
+        return ctypes.c_void_p(t.data_ptr())
+    return ctypes.c_void_p(int(t))
+
+
+def _stream(stream):
+    if stream is None:
+        torch = _torch()
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if hasattr(stream, "cuda_stream"):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _kv_dtype(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float16:
+        return F16
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise ValueError(f"kv / q_attn must be float16 or bfloat16, got {t.dtype}")
+
+
+def _need(t, dtype, name):
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+# ------------------------------------------------------------------------------ entry points
+def workspace_bytes(T: int, S: int, k_top: int) -> int:
+    return int(load().ds4x_workspace_bytes(T, S, k_top))
+
+
+def topk_workspace_bytes(T: int, S: int, k_top: int) -> int:
+    return int(load().ds4x_topk_workspace_bytes(T, S, k_top))
+
+
+def last_launch_count() -> int:
+    return int(load().ds4x_last_launch_count())
+
+
+def indexer_score(q, w, k, positions, ratio: int, scores=None, S: int | None = None, stream=None):
+    """scores[t, s] = sum_h w[t,h] relu(q[t,h,:] . k[s,:]) for visible s, -inf for masked.
+    q [T,H,D] fp16, w [T,H] fp16, k [>=S, D] fp16, positions [T] int32 (CUDA tensors)."""
+    torch = _torch()
+    _need(q, torch.float16, "q"); _need(w, torch.float16, "w"); _need(k, torch.float16, "k")
+    _need(positions, torch.int32, "positions")
+    T, H, D = q.shape
+    S = k.shape[0] if S is None else S
+    if scores is None:
+        scores = torch.empty((T, S), dtype=torch.float32, device=q.device)
+    _need(scores, torch.float32, "scores")
+    rc = load().ds4x_indexer_score(_ptr(q), _ptr(w), _ptr(k), _ptr(positions), T, H, D, S, ratio,
+                                   _ptr(scores), scores.shape[1] if scores.dim() == 2 else S,
+                                   _stream(stream))
+    _check("ds4x_indexer_score", rc)
+    return scores
+
+
+def topk(scores, positions, S: int, ratio: int, k_top: int = 512, indices=None, counts=None,
+         workspace=None, stream=None):
+    """Exact per-token top-k of the visible scores, ascending row order, -1 padded."""
+    torch = _torch()
+    _need(scores, torch.float32, "scores")
+    T, ld = scores.shape
+    dev = scores.device
+    if indices is None:
+        indices = torch.empty((T, k_top), dtype=torch.int32, device=dev)
+    if counts is None:
+        counts = torch.empty((T,), dtype=torch.int32, device=dev)
+    need = topk_workspace_bytes(T, S, k_top)
+    if workspace is None and need > 0:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().ds4x_topk(_ptr(scores), ld, _ptr(positions), T, S, ratio, k_top, _ptr(indices),
+                          _ptr(counts), _ptr(workspace), wbytes, _stream(stream))
+    _check("ds4x_topk", rc)
+    return indices, counts
+
+
+def sparse_attn(q_attn, kv, indices, S: int | None = None, scale: float | None = None, out=None,
+                lse=None, want_lse: bool = True, stream=None):
+    """64-head MQA over the selected rows. q_attn [T,64,512], kv [>=S,512] (fp16 or bf16)."""
+    torch = _torch()
+    dt = _kv_dtype(q_attn)
+    if kv.dtype != q_attn.dtype:
+        raise ValueError("kv and q_attn must have the same dtype")
+    T, Hq, Dkv = q_attn.shape
+    S = kv.shape[0] if S is None else S
+    k_top = indices.shape[1]
+    scale = 1.0 / math.sqrt(Dkv) if scale is None else scale
+    if out is None:
+        out = torch.empty_like(q_attn)
+    if lse is None and want_lse:
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=q_attn.device)
+    rc = load().ds4x_sparse_attn(_ptr(q_attn), _ptr(kv), dt, _ptr(indices), T, Hq, Dkv, S, k_top,
+                                 scale, _ptr(out), _ptr(lse), _stream(stream))
+    _check("ds4x_sparse_attn", rc)
+    return out, lse
+
+
+def index_and_attend(q, w, k, positions, q_attn, kv, ratio: int, k_top: int = 512, S: int | None = None,
+                     scale: float | None = None, indices=None, out=None, lse=None, workspace=None,
+                     want_lse: bool = True, stream=None):
+    """The whole path: score -> top-k -> sparse MQA. Returns (indices, out, lse)."""
+    torch = _torch()
+    dt = _kv_dtype(q_attn)
+    T, H, D = q.shape
+    _, Hq, Dkv = q_attn.shape
+    S = k.shape[0] if S is None else S
+    scale = 1.0 / math.sqrt(Dkv) if scale is None else scale
+    dev = q.device
+    if indices is None:
+        indices = torch.empty((T, k_top), dtype=torch.int32, device=dev)
+    if out is None:
+        out = torch.empty_like(q_attn)
+    if lse is None and want_lse:
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
+    need = workspace_bytes(T, S, k_top)
+    if workspace is None and need > 0:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().ds4x_index_and_attend(_ptr(q), _ptr(w), _ptr(k), _ptr(positions), _ptr(q_attn), _ptr(kv),
+                                      dt, T, H, D, S, ratio, k_top, Hq, Dkv, scale, _ptr(indices),
+                                      _ptr(out), _ptr(lse), _ptr(workspace), wbytes, _stream(stream))
+    _check("ds4x_index_and_attend", rc)
+    return indices, out, lse
+
+
+def device_status(stream=None, clear: bool = True) -> int:
+    return int(load().ds4x_device_status(_stream(stream), 1 if clear else 0))
+
+
+def selftest_bounded_wait(timeout_ns: int, stream=None):
+    _check("ds4x_selftest_bounded_wait", load().ds4x_selftest_bounded_wait(timeout_ns, _stream(stream)))

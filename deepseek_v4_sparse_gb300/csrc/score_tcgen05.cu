@@ -1,0 +1,409 @@
+// score_tcgen05.cu — the lightning-indexer scorer on the 5th-generation tensor cores.
+//
+//   score[t,s] = sum_h w[t,h] * max(0, q[t,h,:] . k[s,:])     (s < n_vis(t); -inf beyond)
+//
+// Source of the operation: "How I made DeepSeek 12x faster on a Mac Studio", section
+// "1: the kernels", PRs #830 (stage Q/K tiles on chip once instead of re-reading ~1 KB per
+// scored pair) and #831 (register blocking: keep operand tiles resident so that each load
+// feeds more MMAs).  On sm_103a both ideas become: TMA-staged, 128B-swizzled shared-memory
+// tiles feeding tcgen05.mma, with a q tile resident across a run of k tiles and the
+// accumulator in TMEM.  The full T x H x S product never leaves the SM.
+//
+// Mapping (one UMMA per 16-wide K step, M=128, N=256, fp16 in, fp32 accumulate):
+//   A = k tile    [128 rows s] x [D]       (M axis = compressed rows = TMEM lanes)
+//   B = q tile    [256 = TPT tokens x H heads] x [D]    (N axis = TMEM columns)
+//   D = TMEM      [128 lanes] x [256 columns] fp32, double-buffered (2 x 256 = 512 columns)
+// so each epilogue thread owns one row s and reduces the H head columns of a token in its
+// own registers: relu, multiply by w[t,h] (from shared memory, broadcast), sum, mask, store.
+//
+// Warp roles (384 threads, one CTA per SM, persistent over a contiguous range of tiles):
+//   warp 0      TMA producer (one lane): q tile per token group, k tile per (group, s-tile)
+//   warp 1      MMA issuer (one lane) + TMEM allocation
+//   warps 4..11 epilogue: warp%4 selects the 32-lane TMEM quadrant, (warp-4)/4 the half of
+//               the tile's tokens
+// The k pipeline stage is one 128-row x 64-column block (16 KB) so that D=128 tiles stream
+// as two stages; q is double-buffered so that a new token group loads while the previous
+// group's MMAs drain.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "ds4x_internal.h"
+#include "ds4x_ptx.cuh"
+
+namespace ds4x {
+namespace {
+
+constexpr int kTileS = 128;   // compressed rows per tile (UMMA M)
+constexpr int kTileN = 256;   // token x head columns per tile (UMMA N)
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (4 + kEpiWarps);
+constexpr int kBlockBytes = kTileS * 128;  // one k stage: 128 rows x 64 fp16
+constexpr uint32_t kTmemCols = 512;
+
+template <int H, int D>
+struct Cfg {
+  static constexpr int TPT = kTileN / H;          // tokens per tile
+  static constexpr int HALF = TPT / 2;            // tokens per epilogue warp
+  static constexpr int KB = D / 64;               // 64-wide blocks along D
+  static constexpr int Q_BYTES = kTileN * D * 2;  // one q tile
+  static constexpr int QB_BYTES = kTileN * 128;   // one 64-wide block of the q tile
+  static constexpr int NK = (D == 128) ? 5 : 8;   // k stages (one 64-wide block each)
+  static constexpr int SMEM = 2 * Q_BYTES + NK * kBlockBytes + kEpiWarps * 128 * 4 + 512 + 1024;
+  static_assert(TPT >= 2 && TPT * H == kTileN, "H must divide 128");
+  static_assert(D % 64 == 0, "D must be a multiple of 64");
+};
+
+struct Params {
+  const __half* w;
+  const int32_t* positions;
+  float* scores;
+  int64_t ld;
+  int T, S, ratio;
+  int n_stiles;
+  long long total_items;
+  int skip_k_top;
+  int write_masked;
+  int* status;
+};
+
+__device__ __forceinline__ int n_visible(const Params& p, int t) {
+  int pos = __ldg(p.positions + t);
+  if (pos < 0) return 0;
+  long long n = ((long long)pos + 1) / p.ratio;
+  return n < p.S ? (int)n : p.S;
+}
+
+// Rows a token needs scored: all visible rows, or none when the shortcut covers it.
+__device__ __forceinline__ int rows_needed(const Params& p, int t) {
+  int n = n_visible(p, t);
+  return (p.skip_k_top > 0 && n <= p.skip_k_top) ? 0 : n;
+}
+
+template <int TPT>
+__device__ __forceinline__ int group_rows(const Params& p, int g) {
+  int m = 0;
+#pragma unroll 1
+  for (int j = 0; j < TPT; ++j) {
+    int t = g * TPT + j;
+    if (t < p.T) m = max(m, rows_needed(p, t));
+  }
+  return m;
+}
+
+template <int H, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const Params p) {
+  using C = Cfg<H, D>;
+  constexpr uint32_t kIdesc = idesc_f16(kTileS, kTileN, 0, 0, 0);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sq = smem;                                   // 2 x Q_BYTES
+  uint8_t* sk = sq + 2 * C::Q_BYTES;                    // NK x kBlockBytes
+  float* sw = reinterpret_cast<float*>(sk + C::NK * kBlockBytes);  // kEpiWarps x 128
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sw + kEpiWarps * 128);
+  uint64_t* kfull = bars;
+  uint64_t* kempty = kfull + C::NK;
+  uint64_t* qfull = kempty + C::NK;
+  uint64_t* qempty = qfull + 2;
+  uint64_t* afull = qempty + 2;
+  uint64_t* aempty = afull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aempty + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NK; ++i) {
+      mbar_init(&kfull[i], 1);
+      mbar_init(&kempty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&qfull[i], 1);
+      mbar_init(&qempty[i], 1);
+      mbar_init(&afull[i], 1);
+      mbar_init(&aempty[i], kEpiWarps);
+    }
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const long long beg = (long long)blockIdx.x * p.total_items / gridDim.x;
+  const long long end = (long long)(blockIdx.x + 1) * p.total_items / gridDim.x;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int cur_g = -1, rows = 0;
+      bool started = false;
+      uint32_t q_it = 0, k_it = 0;
+      for (long long it = beg; it < end; ++it) {
+        const int g = (int)(it / p.n_stiles), st = (int)(it % p.n_stiles);
+        if (g != cur_g) {
+          cur_g = g;
+          rows = group_rows<C::TPT>(p, g);
+          started = false;
+        }
+        if (st * kTileS >= rows) continue;
+        if (!started) {
+          const int b = q_it & 1;
+          if (!mbar_wait(&qempty[b], ((q_it >> 1) & 1) ^ 1, p.status, 1)) break;
+          mbar_arrive_expect_tx(&qfull[b], C::Q_BYTES);
+#pragma unroll
+          for (int kb = 0; kb < C::KB; ++kb)
+            tma_load_2d(sq + b * C::Q_BYTES + kb * C::QB_BYTES, &tm_q, &qfull[b], kb * 64, g * kTileN);
+          ++q_it;
+          started = true;
+        }
+        bool ok = true;
+#pragma unroll
+        for (int kb = 0; kb < C::KB; ++kb) {
+          const int s = k_it % C::NK;
+          if (!mbar_wait(&kempty[s], ((k_it / C::NK) & 1) ^ 1, p.status, 2)) { ok = false; break; }
+          mbar_arrive_expect_tx(&kfull[s], kBlockBytes);
+          tma_load_2d(sk + s * kBlockBytes, &tm_k, &kfull[s], kb * 64, st * kTileS);
+          ++k_it;
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int cur_g = -1, rows = 0, qb = -1;
+      bool started = false;
+      uint32_t q_it = 0, k_it = 0, a_it = 0;
+      for (long long it = beg; it < end; ++it) {
+        const int g = (int)(it / p.n_stiles), st = (int)(it % p.n_stiles);
+        if (g != cur_g) {
+          cur_g = g;
+          rows = group_rows<C::TPT>(p, g);
+          started = false;
+        }
+        if (st * kTileS >= rows) continue;
+        if (!started) {
+          if (qb >= 0) tc_commit(&qempty[qb]);  // previous group's q tile is free once its MMAs finish
+          qb = q_it & 1;
+          if (!mbar_wait(&qfull[qb], (q_it >> 1) & 1, p.status, 3)) break;
+          ++q_it;
+          started = true;
+          tc_fence_after();
+        }
+        const int ab = a_it & 1;
+        if (!mbar_wait(&aempty[ab], ((a_it >> 1) & 1) ^ 1, p.status, 4)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + ab * kTileN;
+        const uint32_t q_addr = smem_u32(sq + qb * C::Q_BYTES);
+        bool ok = true;
+#pragma unroll
+        for (int kb = 0; kb < C::KB; ++kb) {
+          const int s = k_it % C::NK;
+          if (!mbar_wait(&kfull[s], (k_it / C::NK) & 1, p.status, 5)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sk + s * kBlockBytes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t adesc = desc_sw128(a_addr + kk * 32, 16, 1024);
+            const uint64_t bdesc = desc_sw128(q_addr + kb * C::QB_BYTES + kk * 32, 16, 1024);
+            tc_mma_f16(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0);
+          }
+          tc_commit(&kempty[s]);  // k stage is free once these MMAs complete
+          ++k_it;
+        }
+        if (!ok) break;
+        tc_commit(&afull[ab]);
+        ++a_it;
+      }
+    }
+  } else if (warp >= 4) {
+    // --------------------------------------------------------------------- epilogue
+    const int e = warp - 4;
+    const int quad = warp & 3;   // TMEM lanes 32*quad .. 32*quad+31
+    const int half = e >> 2;     // which half of the tile's tokens
+    float* my_w = sw + e * 128;  // this warp's w[t, h] for its tokens, fp32
+    int cur_g = -1, rows = 0;
+    bool loaded = false;
+    uint32_t a_it = 0;
+    int nvis[C::HALF];
+    for (long long it = beg; it < end; ++it) {
+      const int g = (int)(it / p.n_stiles), st = (int)(it % p.n_stiles);
+      if (g != cur_g) {
+        cur_g = g;
+        rows = group_rows<C::TPT>(p, g);
+        loaded = false;
+      }
+      const int row = st * kTileS + quad * 32 + lane;
+      const int t0 = g * C::TPT + half * C::HALF;
+      if (st * kTileS >= rows) {
+        if (p.write_masked && row < p.S) {
+#pragma unroll
+          for (int j = 0; j < C::HALF; ++j)
+            if (t0 + j < p.T) p.scores[(int64_t)(t0 + j) * p.ld + row] = -INFINITY;
+        }
+        continue;
+      }
+      if (!loaded) {
+        __syncwarp();
+        for (int i = lane; i < C::HALF * H; i += 32) {
+          const int t = t0 + i / H;
+          my_w[i] = t < p.T ? __half2float(p.w[(int64_t)t * H + (i % H)]) : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < C::HALF; ++j) nvis[j] = (t0 + j < p.T) ? n_visible(p, t0 + j) : 0;
+        __syncwarp();
+        loaded = true;
+      }
+      const int ab = a_it & 1;
+      if (!mbar_wait(&afull[ab], (a_it >> 1) & 1, p.status, 6)) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + ab * kTileN;
+#pragma unroll
+      for (int j = 0; j < C::HALF; ++j) {
+        const uint32_t col = (half * C::HALF + j) * H;
+        float acc = 0.f;
+        if constexpr (H >= 32) {
+#pragma unroll
+          for (int c = 0; c < H; c += 32) {
+            float v[32];
+            tmem_ld32(t_row + col + c, v);
+            tc_wait_ld();
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+            for (int h = 0; h < 32; h += 4) {
+              a0 = fmaf(my_w[j * H + c + h + 0], fmaxf(v[h + 0], 0.f), a0);
+              a1 = fmaf(my_w[j * H + c + h + 1], fmaxf(v[h + 1], 0.f), a1);
+              a2 = fmaf(my_w[j * H + c + h + 2], fmaxf(v[h + 2], 0.f), a2);
+              a3 = fmaf(my_w[j * H + c + h + 3], fmaxf(v[h + 3], 0.f), a3);
+            }
+            acc += (a0 + a1) + (a2 + a3);
+          }
+        } else {
+          float v[16];
+          tmem_ld16(t_row + col, v);
+          tc_wait_ld();
+          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+          for (int h = 0; h < 16; h += 4) {
+            a0 = fmaf(my_w[j * H + h + 0], fmaxf(v[h + 0], 0.f), a0);
+            a1 = fmaf(my_w[j * H + h + 1], fmaxf(v[h + 1], 0.f), a1);
+            a2 = fmaf(my_w[j * H + h + 2], fmaxf(v[h + 2], 0.f), a2);
+            a3 = fmaf(my_w[j * H + h + 3], fmaxf(v[h + 3], 0.f), a3);
+          }
+          acc = (a0 + a1) + (a2 + a3);
+        }
+        if (t0 + j < p.T && row < p.S) p.scores[(int64_t)(t0 + j) * p.ld + row] = row < nvis[j] ? acc : -INFINITY;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&aempty[ab]);
+      ++a_it;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2-D fp16 tensor [rows, cols] (cols contiguous), box = 64 columns x box_rows rows, 128B swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int H, int D>
+int launch_impl(const ScoreArgs& a, cudaStream_t stream) {
+  using C = Cfg<H, D>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(score_kernel<H, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+        cudaSuccess)
+      return DS4X_ERR_CUDA;
+    attr_set = true;
+  }
+  CUtensorMap tq, tk;
+  if (!make_map(&tq, a.q, (uint64_t)a.T * H, D, kTileN) || !make_map(&tk, a.k, (uint64_t)a.S, D, kTileS))
+    return DS4X_ERR_CUDA;
+  Params p;
+  p.w = static_cast<const __half*>(a.w);
+  p.positions = a.positions;
+  p.scores = a.scores;
+  p.ld = a.ld;
+  p.T = a.T;
+  p.S = a.S;
+  p.ratio = a.ratio;
+  p.n_stiles = (a.S + kTileS - 1) / kTileS;
+  const long long n_groups = (a.T + C::TPT - 1) / C::TPT;
+  p.total_items = n_groups * p.n_stiles;
+  p.skip_k_top = a.skip_k_top;
+  p.write_masked = a.write_masked;
+  p.status = device_status_ptr();
+  const int sms = device_sm_count();
+  const int grid = (int)(p.total_items < sms ? p.total_items : sms);
+  score_kernel<H, D><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, p);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? DS4X_OK : DS4X_ERR_CUDA;
+}
+
+}  // namespace
+
+bool score_shape_supported(int H, int D) {
+  return (H == 16 || H == 32 || H == 64 || H == 128) && (D == 64 || D == 128);
+}
+
+int launch_score(const ScoreArgs& a, cudaStream_t stream) {
+  if (a.T == 0 || a.S == 0) return DS4X_OK;
+#define DS4X_SCORE_CASE(HH, DD) \
+  if (a.H == HH && a.D == DD) return launch_impl<HH, DD>(a, stream);
+  DS4X_SCORE_CASE(16, 64)
+  DS4X_SCORE_CASE(16, 128)
+  DS4X_SCORE_CASE(32, 64)
+  DS4X_SCORE_CASE(32, 128)
+  DS4X_SCORE_CASE(64, 64)
+  DS4X_SCORE_CASE(64, 128)
+  DS4X_SCORE_CASE(128, 64)
+  DS4X_SCORE_CASE(128, 128)
+#undef DS4X_SCORE_CASE
+  return DS4X_ERR_UNSUPPORTED;
+}
+
+}  // namespace ds4x

@@ -38,7 +38,7 @@
  *   - There is no CPU fallback: unsupported shapes return DS4X_ERR_UNSUPPORTED.
  *
  * Visibility:  n_vis(p) = min(S, floor((p+1)/ratio)) rows are visible to a token at
- *              position p (positions are int32, p >= 0).
+ *              position p (positions are int32; a negative position sees no row).
  */
 #ifndef DS4X_H
 #define DS4X_H
@@ -75,7 +75,7 @@ typedef enum {
  *   columns S..ld_scores-1 are not written.
  *
  *   q          [T, H, D] fp16          w  [T, H] fp16        k [S, D] fp16
- *   positions  [T] int32 (>= 0)        scores [T, ld_scores] fp32, ld_scores >= S
+ *   positions  [T] int32                scores [T, ld_scores] fp32, ld_scores >= S
  *   ratio >= 1.  The head products are accumulated in fp32 on the tensor cores and the
  *   head sum in fp32; the full T x H x S product tensor never reaches memory.
  *   T == 0 or S == 0 is a no-op.
@@ -147,6 +147,19 @@ const char* ds4x_status_string(int status);
 /* Number of kernel launches issued by the most recent successful call on this host
  * thread (for launch accounting in benchmarks). */
 int ds4x_last_launch_count(void);
+
+/* ---------------------------------------------------------------------------
+ * Device status.  Every wait inside the kernels is bounded (about one second); a wait that
+ * gives up records DS4X_ERR_TIMEOUT in a status word of the current device and the kernel
+ * returns without finishing its work.  ds4x_device_status synchronizes `stream`, returns
+ * DS4X_OK or DS4X_ERR_TIMEOUT, and clears the word when `clear` != 0.
+ * ------------------------------------------------------------------------- */
+int ds4x_device_status(void* stream, int clear);
+
+/* Diagnostic of the timeout path: launches one kernel whose single waiting thread waits on
+ * a barrier that nothing completes, giving up after `timeout_ns` nanoseconds; the status
+ * word then reads DS4X_ERR_TIMEOUT.  No fault, no hang.  timeout_ns in [1000, 2e9]. */
+int ds4x_selftest_bounded_wait(int64_t timeout_ns, void* stream);
 
 #ifdef __cplusplus
 }

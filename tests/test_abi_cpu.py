@@ -1,0 +1,98 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every declared symbol, and
+rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import deepseek_v4_sparse_gb300 as ds4x
+from deepseek_v4_sparse_gb300 import build as ds4x_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ds4x.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ds4x_build.build()
+    return ds4x.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ds4x_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for n in ("ds4x_indexer_score", "ds4x_topk", "ds4x_sparse_attn", "ds4x_index_and_attend"):
+        assert n in names
+    assert set(names) == set(ds4x.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", ds4x.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (ds4x_\w+)", out))
+    assert set(declared_functions()) <= exported
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5):
+        assert ds4x.status_string(code).startswith("DS4X_")
+    assert "UNKNOWN" in ds4x.status_string(-99)
+
+
+def _p(v):
+    return ctypes.c_void_p(v)
+
+
+def test_invalid_arguments_rejected_without_launch(lib):
+    A = 0x10000  # an aligned, never dereferenced address: validation fails before any use
+    # negative sizes
+    assert lib.ds4x_indexer_score(_p(A), _p(A), _p(A), _p(A), -1, 64, 128, 10, 4, _p(A), 10, None) == ds4x.ERR_INVALID
+    # ld < S
+    assert lib.ds4x_indexer_score(_p(A), _p(A), _p(A), _p(A), 4, 64, 128, 10, 4, _p(A), 9, None) == ds4x.ERR_INVALID
+    # ratio < 1
+    assert lib.ds4x_indexer_score(_p(A), _p(A), _p(A), _p(A), 4, 64, 128, 10, 0, _p(A), 10, None) == ds4x.ERR_INVALID
+    # null and misaligned pointers
+    assert lib.ds4x_indexer_score(None, _p(A), _p(A), _p(A), 4, 64, 128, 10, 4, _p(A), 10, None) == ds4x.ERR_INVALID
+    assert lib.ds4x_indexer_score(_p(A + 2), _p(A), _p(A), _p(A), 4, 64, 128, 10, 4, _p(A), 10, None) == ds4x.ERR_INVALID
+    # unsupported head / dim
+    assert lib.ds4x_indexer_score(_p(A), _p(A), _p(A), _p(A), 4, 48, 128, 10, 4, _p(A), 10, None) == ds4x.ERR_UNSUPPORTED
+    assert lib.ds4x_indexer_score(_p(A), _p(A), _p(A), _p(A), 4, 64, 96, 10, 4, _p(A), 10, None) == ds4x.ERR_UNSUPPORTED
+    # top-k: k_top out of range, null output
+    assert lib.ds4x_topk(_p(A), 10, _p(A), 4, 10, 4, 0, _p(A), None, None, 0, None) == ds4x.ERR_INVALID
+    assert lib.ds4x_topk(_p(A), 10, _p(A), 4, 10, 4, 4096, _p(A), None, None, 0, None) == ds4x.ERR_UNSUPPORTED
+    assert lib.ds4x_topk(_p(A), 10, _p(A), 4, 10, 4, 512, None, None, None, 0, None) == ds4x.ERR_INVALID
+    # attention: shapes this build has no kernel for, bad dtype
+    assert lib.ds4x_sparse_attn(_p(A), _p(A), 1, _p(A), 4, 32, 512, 10, 512, 0.1, _p(A), None, None) == ds4x.ERR_UNSUPPORTED
+    assert lib.ds4x_sparse_attn(_p(A), _p(A), 1, _p(A), 4, 64, 256, 10, 512, 0.1, _p(A), None, None) == ds4x.ERR_UNSUPPORTED
+    assert lib.ds4x_sparse_attn(_p(A), _p(A), 7, _p(A), 4, 64, 512, 10, 512, 0.1, _p(A), None, None) == ds4x.ERR_INVALID
+    # fused entry: workspace missing / too small
+    assert lib.ds4x_index_and_attend(_p(A), _p(A), _p(A), _p(A), _p(A), _p(A), 1, 4, 64, 128, 10, 4, 512, 64, 512,
+                                     0.1, _p(A), _p(A), None, None, 0, None) == ds4x.ERR_WORKSPACE
+    assert lib.ds4x_index_and_attend(_p(A), _p(A), _p(A), _p(A), _p(A), _p(A), 1, 4, 64, 128, 10, 4, 512, 64, 512,
+                                     0.1, _p(A), _p(A), None, _p(A), 16, None) == ds4x.ERR_WORKSPACE
+    # self-test argument range
+    assert lib.ds4x_selftest_bounded_wait(10, None) == ds4x.ERR_INVALID
+
+
+def test_empty_calls_are_noops(lib):
+    A = 0x10000
+    assert lib.ds4x_indexer_score(_p(A), _p(A), _p(A), _p(A), 0, 64, 128, 10, 4, _p(A), 10, None) == ds4x.OK
+    assert lib.ds4x_topk(_p(A), 10, _p(A), 0, 10, 4, 512, _p(A), None, None, 0, None) == ds4x.OK
+    assert lib.ds4x_sparse_attn(_p(A), _p(A), 1, _p(A), 0, 64, 512, 10, 512, 0.1, _p(A), None, None) == ds4x.OK
+
+
+def test_workspace_sizes(lib):
+    # the fused entry keeps T x S fp32 scores (rounded up to 256 bytes)
+    assert ds4x.workspace_bytes(2048, 2048, 512) >= 2048 * 2048 * 4
+    assert ds4x.workspace_bytes(0, 2048, 512) == 0
+    # one decode token over a long row is split and needs candidate scratch
+    assert ds4x.topk_workspace_bytes(1, 262208, 512) > 0
+    assert ds4x.topk_workspace_bytes(2048, 16384, 512) == 0

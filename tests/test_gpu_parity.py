@@ -1,0 +1,213 @@
+"""CUDA path (through the C ABI) against the CPU oracle on the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import deepseek_v4_sparse_gb300 as ds4x
+import oracle
+import synth
+from parity import (check_attn, check_index_sets, check_scores, dev16, few_rows_bound, host16, n_vis,
+                    to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from deepseek_v4_sparse_gb300 import build
+    build.build()
+    ds4x.load()
+    yield
+    torch.cuda.synchronize()
+    assert ds4x.device_status() == ds4x.OK, "a bounded device wait timed out during the tests"
+
+
+def run_all(inp, S=None):
+    d = to_device(inp)
+    wl = inp.wl
+    S = wl.S if S is None else S
+    scores = ds4x.indexer_score(d["q"], d["w"], d["k"], d["positions"], wl.ratio, S=S)
+    idx, cnt = ds4x.topk(scores, d["positions"], S, wl.ratio, wl.k_top)
+    out, lse = ds4x.sparse_attn(d["q_attn"], d["kv"], idx, S=S, scale=wl.scale)
+    fidx, fout, flse = ds4x.index_and_attend(d["q"], d["w"], d["k"], d["positions"], d["q_attn"], d["kv"],
+                                             wl.ratio, wl.k_top, S=S, scale=wl.scale)
+    torch.cuda.synchronize()
+    assert ds4x.device_status() == ds4x.OK
+    return dict(scores=scores.cpu().numpy(), idx=idx.cpu().numpy(), cnt=cnt.cpu().numpy(),
+                out=host16(out), lse=lse.cpu().numpy(), fidx=fidx.cpu().numpy(), fout=host16(fout),
+                flse=flse.cpu().numpy())
+
+
+# ------------------------------------------------------------------------ bounded waits
+def test_bounded_wait_reports_timeout():
+    ds4x.device_status(clear=True)
+    ds4x.selftest_bounded_wait(2_000_000)  # 2 ms, nothing ever completes the barrier
+    assert ds4x.device_status(clear=True) == ds4x.ERR_TIMEOUT
+    assert ds4x.device_status(clear=True) == ds4x.OK
+
+
+# ---------------------------------------------------------------- exact-integer config
+def test_tiny_exact_bit_exact():
+    wl = synth.WORKLOADS["tiny_exact"]
+    inp = synth.make_inputs(wl, seed=0)
+    g = run_all(inp)
+    ref_scores = oracle.indexer_score(inp.q, inp.w, inp.k, inp.positions, wl.ratio, S=wl.S)
+    check_scores(g["scores"], ref_scores, inp.positions, wl.ratio, wl.S, exact=True)
+    ref_idx, ref_cnt = oracle.topk(ref_scores, inp.positions, wl.S, wl.ratio, wl.k_top)
+    assert np.array_equal(g["idx"], ref_idx), "indices differ from the oracle"
+    assert np.array_equal(g["cnt"], ref_cnt)
+    assert np.array_equal(g["fidx"], ref_idx), "fused-path indices differ from the oracle"
+    ref_out, ref_lse = oracle.sparse_attn(inp.q_attn, inp.kv, "f16", ref_idx, wl.S, wl.scale)
+    check_attn(g["out"], ref_out, "f16", g["lse"], ref_lse)
+    check_attn(g["fout"], ref_out, "f16", g["flse"], ref_lse)
+
+
+# ---------------------------------------------------------- N(0,1) configs, down-scaled
+@pytest.mark.parametrize("name,T", [("prefill_8k", 160), ("prefill_32k", 40)])
+def test_normal_downscaled(name, T):
+    wl = synth.WORKLOADS[name]
+    # the last T tokens of the chunk (they see the most rows)
+    inp = synth.make_inputs(wl, seed=0, T=T, pos0=wl.pos0 + wl.T - T)
+    g = run_all(inp)
+    ref_scores = oracle.indexer_score(inp.q, inp.w, inp.k, inp.positions, wl.ratio, S=wl.S)
+    check_scores(g["scores"], ref_scores, inp.positions, wl.ratio, wl.S, exact=False)
+    # same fp32 scores in, same decision out: top-k of the GPU's scores is bit-exact
+    idx_on_gpu_scores, cnt = oracle.topk(g["scores"], inp.positions, wl.S, wl.ratio, wl.k_top)
+    assert np.array_equal(g["idx"], idx_on_gpu_scores)
+    assert np.array_equal(g["cnt"], cnt)
+    ref_idx, _ = oracle.topk(ref_scores, inp.positions, wl.S, wl.ratio, wl.k_top)
+    check_index_sets(g["fidx"], ref_idx, ref_scores, inp.positions, wl.ratio, wl.S, wl.k_top)
+    ref_out, ref_lse = oracle.sparse_attn(inp.q_attn, inp.kv, wl.kv_dtype, g["idx"], wl.S, wl.scale)
+    check_attn(g["out"], ref_out, wl.kv_dtype, g["lse"], ref_lse)
+    ref_fout, ref_flse = oracle.sparse_attn(inp.q_attn, inp.kv, wl.kv_dtype, g["fidx"], wl.S, wl.scale)
+    check_attn(g["fout"], ref_fout, wl.kv_dtype, g["flse"], ref_flse)
+
+
+# ----------------------------------------------------------------------------- edge cases
+def _edge_inputs(tag, positions, S, kind="normal", kv_dtype="bf16", H=64, D=128, w_kind="pos", seed=1):
+    T = len(positions)
+    return synth.custom_inputs(seed, tag, T, H, D, S, 64, 512, kind, kv_dtype, np.array(positions), w_kind)
+
+
+@pytest.mark.parametrize("ratio", [1, 4, 128])
+def test_visibility_edges(ratio):
+    # n_vis in {0, 1, 2, 511, 512, 513, ...}; S not a multiple of 128; T not a multiple of
+    # the scorer's token group; a negative position sees no row
+    S = 1000
+    nv = [0, 1, 2, 511, 512, 513, 700, 999, 1000, 1000, 37, 128, 129]
+    positions = [n * ratio - 1 for n in nv]
+    assert [n_vis(p, ratio, S) for p in positions] == nv
+    raw = _edge_inputs(f"edge_r{ratio}", positions, S)
+    wl = synth.Workload(raw.wl.name, T=len(nv), H=64, D=128, S=S, ratio=ratio, pos0=0, kind="normal",
+                        kv_dtype="bf16")
+    inp = synth.Inputs(wl, raw.q, raw.w, raw.k, raw.positions, raw.q_attn, raw.kv)
+    g = run_all(inp)
+    ref_scores = oracle.indexer_score(inp.q, inp.w, inp.k, inp.positions, ratio, S=S)
+    check_scores(g["scores"], ref_scores, inp.positions, ratio, S, exact=False)
+    idx_ref_on_gpu, cnt_ref = oracle.topk(g["scores"], inp.positions, S, ratio, wl.k_top)
+    assert np.array_equal(g["idx"], idx_ref_on_gpu) and np.array_equal(g["cnt"], cnt_ref)
+    ref_idx, _ = oracle.topk(ref_scores, inp.positions, S, ratio, wl.k_top)
+    check_index_sets(g["fidx"], ref_idx, ref_scores, inp.positions, ratio, S, wl.k_top)
+    # tokens here see as few as 1 row: the few-row rounding bound applies on top of the spec's
+    ref_out, ref_lse = oracle.sparse_attn(inp.q_attn, inp.kv, "bf16", g["idx"], S, wl.scale)
+    check_attn(g["out"], ref_out, "bf16", g["lse"], ref_lse,
+               extra=few_rows_bound(inp.kv, g["idx"], ref_out, "bf16", S))
+    ref_fout, ref_flse = oracle.sparse_attn(inp.q_attn, inp.kv, "bf16", g["fidx"], S, wl.scale)
+    check_attn(g["fout"], ref_fout, "bf16", g["flse"], ref_flse,
+               extra=few_rows_bound(inp.kv, g["fidx"], ref_fout, "bf16", S))
+
+
+def test_all_equal_scores_tie_break():
+    # q = 0 -> every visible score is exactly 0 -> the k lowest rows win
+    S, T = 900, 5
+    positions = np.array([899, 600, 513, 512, 100], dtype=np.int32)
+    inp = _edge_inputs("ties", positions, S, kind="int", kv_dtype="f16", H=16, D=64, w_kind="pow2")
+    inp.q[:] = 0
+    wl = synth.Workload("ties", T=T, H=16, D=64, S=S, ratio=1, pos0=0, kind="int", kv_dtype="f16")
+    inp = synth.Inputs(wl, inp.q, inp.w, inp.k, inp.positions, inp.q_attn, inp.kv)
+    g = run_all(inp)
+    for t in range(T):
+        n = min(S, int(positions[t]) + 1)
+        want = list(range(min(n, 512))) + [-1] * (512 - min(n, 512))
+        assert list(g["idx"][t]) == want
+        assert list(g["fidx"][t]) == want
+
+
+def test_integer_config_many_ties_random_k():
+    # small integer scores (many exact ties) with a k_top that is not a multiple of 128
+    wl0 = synth.WORKLOADS["tiny_exact"]
+    inp = synth.make_inputs(wl0, seed=3, T=37, pos0=4000)
+    S, k_top = wl0.S, 300
+    d = to_device(inp)
+    scores = ds4x.indexer_score(d["q"], d["w"], d["k"], d["positions"], wl0.ratio, S=S)
+    idx, cnt = ds4x.topk(scores, d["positions"], S, wl0.ratio, k_top)
+    out, lse = ds4x.sparse_attn(d["q_attn"], d["kv"], idx, S=S, scale=wl0.scale)
+    torch.cuda.synchronize()
+    ref_scores = oracle.indexer_score(inp.q, inp.w, inp.k, inp.positions, wl0.ratio, S=S)
+    check_scores(scores.cpu().numpy(), ref_scores, inp.positions, wl0.ratio, S, exact=True)
+    ref_idx, ref_cnt = oracle.topk(ref_scores, inp.positions, S, wl0.ratio, k_top)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    ref_out, ref_lse = oracle.sparse_attn(inp.q_attn, inp.kv, "f16", ref_idx, S, wl0.scale)
+    check_attn(host16(out), ref_out, "f16", lse.cpu().numpy(), ref_lse)
+
+
+def test_attention_invalid_and_out_of_range_indices():
+    rng = np.random.default_rng(0)
+    S, T = 300, 6
+    inp = _edge_inputs("attn_idx", np.full(T, 10**6), S)
+    idx = np.stack([rng.choice(S, 512, replace=True) for _ in range(T)]).astype(np.int32)
+    idx[0, :] = -1                       # no valid row
+    idx[1, 5:] = -1                      # five rows
+    idx[2, ::3] = S + 7                  # out of range entries are skipped
+    idx[3, :] = 17                       # the same row 512 times
+    d = to_device(inp)
+    out, lse = ds4x.sparse_attn(d["q_attn"], d["kv"], torch.from_numpy(idx).cuda(), S=S)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle.sparse_attn(inp.q_attn, inp.kv, "bf16", idx, S, 1 / np.sqrt(512))
+    check_attn(host16(out), ref_out, "bf16", lse.cpu().numpy(), ref_lse,
+               extra=few_rows_bound(inp.kv, idx, ref_out, "bf16", S))
+    assert np.all(np.isneginf(lse[0].cpu().numpy()))
+
+
+def test_split_topk_decode_row():
+    # one token over a long row: the row is split across CTAs and merged
+    S = 262144 + 37
+    rng = np.random.default_rng(11)
+    scores = rng.standard_normal((1, S)).astype(np.float32)
+    scores[0, 1000:1300] = scores[0, 1000]          # a run of exact ties
+    pos = np.array([4 * S + 3], dtype=np.int32)
+    assert ds4x.topk_workspace_bytes(1, S, 512) > 0
+    idx, cnt = ds4x.topk(torch.from_numpy(scores).cuda(), torch.from_numpy(pos).cuda(), S, 4, 512)
+    torch.cuda.synchronize()
+    ref_idx, ref_cnt = oracle.topk(scores, pos, S, 4, 512)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    assert np.array_equal(cnt.cpu().numpy(), ref_cnt)
+
+
+# --------------------------------------- full-size workloads in the benchmark's launch shape
+@pytest.mark.parametrize("name", ["prefill_8k", "prefill_64k"])
+def test_full_size_sampled(name):
+    wl = synth.WORKLOADS[name]
+    inp = synth.make_inputs(wl, seed=0)
+    d = to_device(inp)
+    fidx, fout, flse = ds4x.index_and_attend(d["q"], d["w"], d["k"], d["positions"], d["q_attn"], d["kv"],
+                                             wl.ratio, wl.k_top, S=wl.S, scale=wl.scale)
+    torch.cuda.synchronize()
+    assert ds4x.device_status() == ds4x.OK
+    sample = np.array([0, 1, 517, 1024, 1500, wl.T - 2, wl.T - 1])
+    gidx = fidx.cpu().numpy()[sample]
+    gout = host16(fout)[sample]
+    glse = flse.cpu().numpy()[sample]
+    q, w, pos = inp.q[sample], inp.w[sample], inp.positions[sample]
+    ref_scores = oracle.indexer_score(q, w, inp.k, pos, wl.ratio, S=wl.S)
+    ref_idx, _ = oracle.topk(ref_scores, pos, wl.S, wl.ratio, wl.k_top)
+    check_index_sets(gidx, ref_idx, ref_scores, pos, wl.ratio, wl.S, wl.k_top)
+    ref_out, ref_lse = oracle.sparse_attn(inp.q_attn[sample], inp.kv, wl.kv_dtype, gidx, wl.S, wl.scale)
+    check_attn(gout, ref_out, wl.kv_dtype, glse, ref_lse)
+    # every token: a valid, ascending selection of k_top visible rows
+    allidx = fidx.cpu().numpy()
+    nv = np.minimum(wl.S, (inp.positions.astype(np.int64) + 1) // wl.ratio)
+    assert np.all(np.diff(allidx, axis=1) > 0)
+    assert np.all(allidx[:, 0] >= 0) and np.all(allidx[:, -1] < nv)
