@@ -27,6 +27,7 @@ EXPORTS = (
     "ds4x_indexer_score", "ds4x_topk", "ds4x_topk_workspace_bytes", "ds4x_sparse_attn",
     "ds4x_index_and_attend", "ds4x_workspace_bytes", "ds4x_status_string",
     "ds4x_last_launch_count", "ds4x_device_status", "ds4x_selftest_bounded_wait",
+    "ds4x_topk_static_scratch",
 )
 
 _lock = threading.Lock()
@@ -228,3 +229,29 @@ def device_status(stream=None, clear: bool = True) -> int:
 
 def selftest_bounded_wait(timeout_ns: int, stream=None):
     _check("ds4x_selftest_bounded_wait", load().ds4x_selftest_bounded_wait(timeout_ns, _stream(stream)))
+
+
+TOPK_STATIC_SCRATCH_BYTES = 4 << 20
+
+
+def topk_static_scratch(scores, positions, S: int, ratio: int, k_top: int = 512, indices=None, counts=None,
+                        stream=None):
+    """ds4x_topk without a workspace, for callers that may not allocate device memory while they
+    run (the split mode's candidate lists use a fixed array inside the library instead). The
+    output tensors must be passed in by such callers; calls overlapping on the GPU must not be
+    issued (they share that array)."""
+    torch = _torch()
+    _need(scores, torch.float32, "scores")
+    T, ld = scores.shape
+    if indices is None:
+        indices = torch.empty((T, k_top), dtype=torch.int32, device=scores.device)
+    if counts is None:
+        counts = torch.empty((T,), dtype=torch.int32, device=scores.device)
+    lib = load()
+    fn = lib.ds4x_topk_static_scratch
+    P = ctypes.c_void_p
+    fn.argtypes = [P, ctypes.c_int64, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, P, P]
+    fn.restype = ctypes.c_int
+    _check("ds4x_topk_static_scratch", fn(_ptr(scores), ld, _ptr(positions), T, S, ratio, k_top, _ptr(indices),
+                                          _ptr(counts), _stream(stream)))
+    return indices, counts

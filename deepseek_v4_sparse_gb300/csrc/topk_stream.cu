@@ -29,6 +29,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "ds4x_internal.h"
 #include "ds4x_ptx.cuh"
 
@@ -436,3 +438,85 @@ int launch_topk(const TopkArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace ds4x
+
+// -----------------------------------------------------------------------------------------
+// Top-k for callers that cannot allocate device memory.
+//
+// ds4x_topk needs a caller-supplied workspace when one long row is split across CTAs (the
+// candidate lists of the split pass).  Some callers cannot provide one: an inference server that
+// hands all of HBM to its KV cache at start-up and forbids any later allocation, or a plugin that
+// runs inside a host framework owning the device allocator.  For them this variant keeps the
+// candidate lists in a fixed array compiled into the library.  The array is file-scope device
+// memory: every GPU that loads the library holds DS4X_TOPK_STATIC_SCRATCH_BYTES of it until the
+// process exits, and every call on that GPU shares it.
+namespace ds4x {
+
+static __device__ __align__(256) unsigned char g_topk_static_scratch[DS4X_TOPK_STATIC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_static_scratch_mutex;
+void* g_static_scratch_addr[64];  // device address of g_topk_static_scratch, per device
+
+// Host code only knows a stand-in for the array's name; the device address is looked up once
+// per device, with that device current.
+void* static_scratch_address() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(g_static_scratch_mutex);
+  if (g_static_scratch_addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_topk_static_scratch) != cudaSuccess) return nullptr;
+    g_static_scratch_addr[dev] = ptr;
+  }
+  return g_static_scratch_addr[dev];
+}
+}  // namespace
+
+}  // namespace ds4x
+
+extern "C" int ds4x_topk_static_scratch(const float* scores, int64_t ld_scores, const int32_t* positions,
+                                        int32_t T, int32_t S, int32_t ratio, int32_t k_top, int32_t* indices,
+                                        int32_t* counts, void* stream) {
+  using namespace ds4x;
+  if (T < 0 || S < 0 || ratio < 1 || ld_scores < S) return DS4X_ERR_INVALID;
+  if (k_top < 1 || k_top > DS4X_MAX_KTOP) return k_top < 1 ? DS4X_ERR_INVALID : DS4X_ERR_UNSUPPORTED;
+  if (T == 0) return DS4X_OK;
+  if (!scores || !positions || !indices) return DS4X_ERR_INVALID;
+  const uintptr_t mis = (reinterpret_cast<uintptr_t>(scores) | reinterpret_cast<uintptr_t>(positions) |
+                         reinterpret_cast<uintptr_t>(indices) | reinterpret_cast<uintptr_t>(counts)) & 15u;
+  if (mis) return DS4X_ERR_INVALID;
+  // the candidate lists must fit the fixed array
+  if (topk_workspace_bytes(T, S, k_top) > (size_t)DS4X_TOPK_STATIC_SCRATCH_BYTES) return DS4X_ERR_WORKSPACE;
+  void* scratch = static_scratch_address();
+  if (scratch == nullptr) return DS4X_ERR_CUDA;
+  const size_t smem = sizeof(Shared) + (size_t)((S + 31) / 32 + 1) * sizeof(uint32_t);
+  if (smem > 220 * 1024) return DS4X_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+      cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return DS4X_ERR_CUDA;
+  KParams p;
+  p.scores = scores;
+  p.ld = ld_scores;
+  p.positions = positions;
+  p.T = T;
+  p.S = S;
+  p.ratio = ratio;
+  p.k_top = k_top;
+  p.indices = indices;
+  p.counts = counts;
+  p.nsplit = split_parts(T, S);
+  p.cand_key = nullptr;
+  p.cand_row = nullptr;
+  if (p.nsplit <= 1) {
+    topk_row_kernel<<<T, kThreads, smem, st>>>(p);
+  } else {
+    // every slot of the candidate lists is written by the split pass (rows or padding), so
+    // nothing left by an earlier call is ever read
+    p.cand_key = static_cast<uint32_t*>(scratch);
+    p.cand_row = p.cand_key + (size_t)T * p.nsplit * k_top;
+    topk_part_kernel<<<dim3(p.nsplit, T), kThreads, sizeof(Shared), st>>>(p);
+    topk_merge_kernel<<<T, kThreads, smem, st>>>(p);
+  }
+  return cudaGetLastError() == cudaSuccess ? DS4X_OK : DS4X_ERR_CUDA;
+}

@@ -106,6 +106,30 @@ int ds4x_topk(const float* scores, int64_t ld_scores, const int32_t* positions,
 size_t ds4x_topk_workspace_bytes(int32_t T, int32_t S, int32_t k_top);
 
 /* ---------------------------------------------------------------------------
+ * ds4x_topk_static_scratch — ds4x_topk for callers that cannot allocate device memory.
+ * No counterpart on the pages: a convenience of this library.
+ *
+ *   Same arguments and results as ds4x_topk, minus the workspace.  Meant for callers that must
+ *   not allocate device memory at call time (a serving process that gave all of HBM to its KV
+ *   cache at start-up, a plugin running under a host framework that owns the allocator) and so
+ *   cannot hand over a workspace.  The candidate lists of the split mode (one long row spread
+ *   over many CTAs) live instead in a fixed array of DS4X_TOPK_STATIC_SCRATCH_BYTES compiled
+ *   into the library; every GPU that loads the library holds that array until the process exits.
+ *   - Calls needing more than that (ds4x_topk_workspace_bytes(T, S, k_top) > the maximum) return
+ *     DS4X_ERR_WORKSPACE and launch nothing.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
+ *     that device current); make that first call before any stream capture.
+ *   - Allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ *   - All calls on a device share the one array: calls that overlap on the GPU (different streams,
+ *     no ordering between them) race on it and must not be issued.  Sequential calls are fine; a
+ *     call never reads what an earlier call left in the array.
+ * ------------------------------------------------------------------------- */
+#define DS4X_TOPK_STATIC_SCRATCH_BYTES (4u << 20)
+int ds4x_topk_static_scratch(const float* scores, int64_t ld_scores, const int32_t* positions,
+                             int32_t T, int32_t S, int32_t ratio, int32_t k_top,
+                             int32_t* indices, int32_t* counts, void* stream);
+
+/* ---------------------------------------------------------------------------
  * ds4x_sparse_attn — multi-query attention over the selected compressed rows ([A]).
  *
  *   For token t, head h, over the valid entries j of indices[t, 0..k_top-1]
