@@ -138,6 +138,13 @@ __device__ __forceinline__ float warp_columns_reduce(float (&v)[32]) {
   return v[0];
 }
 
+// 2^x with the hardware approximation (MUFU.EX2, flushes subnormal results to zero); 2^-inf = 0.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <bool kBf16>
 __device__ __forceinline__ uint32_t pack2(float a, float b, float& ra, float& rb) {
   if constexpr (kBf16) {
@@ -234,24 +241,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       for (int c = 0; c < p.nchunks && ok; ++c, ++gc) {
-        int32_t rid[8];
+        // this thread copies 16-byte column chunk `ch` of rows (pt>>3) + 16 i, i = 0..7, in every
+        // slot: the source row offsets and the swizzled destinations are fixed for the chunk
+        const char* src_row[8];
+        uint32_t dst_off[8], src_bytes[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int j = c * kRows + (pt >> 3) + 16 * i;
+          const int r = (pt >> 3) + 16 * i;
+          const int j = c * kRows + r;
           int32_t idx = -1;
           if (j < p.k_top) idx = __ldg(p.indices + (int64_t)t * p.k_top + j);
-          rid[i] = (idx >= 0 && idx < p.S) ? idx : -1;
+          const bool valid = idx >= 0 && idx < p.S;
+          src_row[i] = valid ? reinterpret_cast<const char*>(p.kv + (int64_t)idx * kDkv) + ch * 16
+                             : reinterpret_cast<const char*>(p.zero_src);
+          src_bytes[i] = valid ? 16u : 0u;
+          dst_off[i] = r * 128 + ((ch ^ (r & 7)) << 4);
         }
         for (int kb = 0; kb < kSlots; ++kb) {
           if (!mbar_wait(&slot_empty[kb], (gc & 1) ^ 1, p.status, 21)) { ok = false; break; }
           const uint32_t base = smem_u32(skv + kb * kSlotBytes);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int r = (pt >> 3) + 16 * i;
-            const uint32_t dst = base + r * 128 + ((ch ^ (r & 7)) << 4);
-            const uint16_t* src = rid[i] >= 0 ? p.kv + (int64_t)rid[i] * kDkv + kb * 64 + ch * 8 : p.zero_src;
-            cp_async16(dst, src, rid[i] >= 0 ? 16u : 0u);
-          }
+          for (int i = 0; i < 8; ++i)
+            cp_async16(base + dst_off[i], src_row[i] + (src_bytes[i] ? kb * 128 : 0), src_bytes[i]);
           cp_async_arrive(&slot_full[kb]);
         }
       }
@@ -316,11 +327,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
     uint32_t gc = 0, tok_i = 0;
     float lpart[32];
-    for (int t = blockIdx.x; t < p.T; t += gridDim.x, ++tok_i) {
-      bool ok = true;
+    bool ok = true;
+    // validity of this thread's row in the next chunk, loaded one chunk ahead
+    auto row_valid = [&](int t, int c) {
+      const int j = c * kRows + quad * 32 + lane;
+      if (t >= p.T || c >= p.nchunks || j >= p.k_top) return false;
+      const int32_t idx = __ldg(p.indices + (int64_t)t * p.k_top + j);
+      return idx >= 0 && idx < p.S;
+    };
+    bool next_valid = row_valid(blockIdx.x, 0);
+    for (int t = blockIdx.x; t < p.T && ok; t += gridDim.x, ++tok_i) {
 #pragma unroll
       for (int i = 0; i < 32; ++i) lpart[i] = 0.f;
       for (int c = 0; c < p.nchunks; ++c, ++gc) {
+        const bool valid = next_valid;
+        next_valid = (c + 1 < p.nchunks) ? row_valid(t, c + 1) : row_valid(t + gridDim.x, 0);
         const int sb = gc & 1;
         ok = named_and(kSoftBar, kSoftThreads, mbar_wait(&sfull[sb], (gc >> 1) & 1, p.status, 40));
         if (!ok) break;
@@ -331,35 +352,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sempty[sb]);
-        const int j = c * kRows + quad * 32 + lane;
-        bool valid = false;
-        if (j < p.k_top) {
-          const int32_t idx = __ldg(p.indices + (int64_t)t * p.k_top + j);
-          valid = idx >= 0 && idx < p.S;
-        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[i] = valid ? x[i] * p.scale_log2 : -INFINITY;
-        float tmp[32];
+        // The running max of a head only has to keep every logit within 2^8 of it (so the
+        // probabilities stay <= 256); the exact column max is taken on a token's first chunk and
+        // again only when some logit overshoots the running max by more than that.
+        bool over = (c == 0);
+        if (c > 0) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) tmp[i] = x[i];
-        red[quad * kHq + hcol + lane] = warp_columns_reduce<true>(tmp);
-        named_sync(kSoftBar, kSoftThreads);
-        bool need = false;
-        if (owner) {
-          const int h = hcol + lane;
-          const float cm = fmaxf(fmaxf(red[h], red[kHq + h]), fmaxf(red[2 * kHq + h], red[3 * kHq + h]));
-          const float mo = (c == 0) ? -INFINITY : m_run[h];
-          float a = 1.f;
-          if (cm > mo + kRescaleLog2 || (mo == -INFINITY && cm > -INFINITY)) {
-            a = (mo == -INFINITY) ? 0.f : exp2f(mo - cm);
-            m_run[h] = cm;
-            need = (c > 0) && (mo != -INFINITY);
-          } else if (c == 0) {
-            m_run[h] = mo;  // -inf: nothing visible yet
+          for (int i = 0; i < 32; i += 4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(&m_run[hcol + i]);
+            over |= (x[i] > m4.x + kRescaleLog2) | (x[i + 1] > m4.y + kRescaleLog2) |
+                    (x[i + 2] > m4.z + kRescaleLog2) | (x[i + 3] > m4.w + kRescaleLog2);
           }
-          alpha[h] = a;
         }
-        const bool rescale = named_or(kSoftBar, kSoftThreads, need);
+        const bool rescan = named_or(kSoftBar, kSoftThreads, over);
+        bool rescale = false;
+        if (rescan) {
+          float tmp[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) tmp[i] = x[i];
+          red[quad * kHq + hcol + lane] = warp_columns_reduce<true>(tmp);
+          named_sync(kSoftBar, kSoftThreads);
+          bool need = false;
+          if (owner) {
+            const int h = hcol + lane;
+            const float cm = fmaxf(fmaxf(red[h], red[kHq + h]), fmaxf(red[2 * kHq + h], red[3 * kHq + h]));
+            const float mo = (c == 0) ? -INFINITY : m_run[h];
+            float a = 1.f;
+            if (cm > mo + kRescaleLog2 || (mo == -INFINITY && cm > -INFINITY)) {
+              a = (mo == -INFINITY) ? 0.f : ex2_approx(mo - cm);
+              m_run[h] = cm;
+              need = (c > 0) && (mo != -INFINITY);
+            } else if (c == 0) {
+              m_run[h] = mo;  // -inf: nothing visible yet
+            }
+            alpha[h] = a;
+          }
+          rescale = named_or(kSoftBar, kSoftThreads, need);
+        }
         if (rescale) {
           // O^T and the partial sums were built with the old max: scale them first, once the
           // previous chunk's O^T product has completed.
@@ -384,14 +415,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         // probabilities, rounded to the kv dtype (the sums use the rounded values)
         uint32_t packed[16];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float m0 = m_run[hcol + i], m1 = m_run[hcol + i + 1];
-          const float p0 = (x[i] == -INFINITY) ? 0.f : exp2f(x[i] - m0);
-          const float p1 = (x[i + 1] == -INFINITY) ? 0.f : exp2f(x[i + 1] - m1);
-          float r0, r1;
-          packed[i >> 1] = pack2<kBf16>(p0, p1, r0, r1);
+        for (int i = 0; i < 32; i += 4) {
+          float4 m4 = *reinterpret_cast<const float4*>(&m_run[hcol + i]);
+          // a head with no visible row yet has m = -inf and only -inf logits: use 0 instead
+          m4.x = m4.x == -INFINITY ? 0.f : m4.x;
+          m4.y = m4.y == -INFINITY ? 0.f : m4.y;
+          m4.z = m4.z == -INFINITY ? 0.f : m4.z;
+          m4.w = m4.w == -INFINITY ? 0.f : m4.w;
+          float r0, r1, r2, r3;
+          packed[(i >> 1) + 0] = pack2<kBf16>(ex2_approx(x[i] - m4.x), ex2_approx(x[i + 1] - m4.y), r0, r1);
+          packed[(i >> 1) + 1] = pack2<kBf16>(ex2_approx(x[i + 2] - m4.z), ex2_approx(x[i + 3] - m4.w), r2, r3);
           lpart[i] += r0;
           lpart[i + 1] += r1;
+          lpart[i + 2] += r2;
+          lpart[i + 3] += r3;
         }
         const int pb = gc & 1;
         ok = named_and(kSoftBar, kSoftThreads, mbar_wait(&pempty[pb], ((gc >> 1) & 1) ^ 1, p.status, 42));
@@ -425,15 +462,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.lse) p.lse[(int64_t)t * kHq + h] = l > 0.f ? (m_run[h] + log2f(l)) * 0.69314718055994531f : -INFINITY;
       }
       named_sync(kSoftBar, kSoftThreads);
-      uint16_t* orow = p.out + (int64_t)t * kHq * kDkv;
+      // out[t, h, d]: lane = d within the 32-row quadrant of a 128-wide d-block.  Lanes pair up
+      // (d, d+1) so that each store writes two values: the even lane stores the even heads, the
+      // odd lane the odd heads.
+      uint32_t* orow = reinterpret_cast<uint32_t*>(p.out + (int64_t)t * kHq * kDkv);
+      const bool odd = lane & 1;
 #pragma unroll 1
       for (int db = 0; db < kDkv / 128; ++db) {
         float v[32];
         tmem_ld32(tmem + t_lane + kColO + db * kHq + hcol, v);
         tc_wait_ld();
-        const int d = db * 128 + quad * 32 + lane;
+        const int d_even = db * 128 + quad * 32 + (lane & ~1);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) orow[(int64_t)(hcol + i) * kDkv + d] = to16<kBf16>(v[i] * alpha[hcol + i]);
+        for (int i = 0; i < 32; i += 2) {
+          const float a0 = v[i] * alpha[hcol + i];          // head hcol+i, this lane's d
+          const float a1 = v[i + 1] * alpha[hcol + i + 1];  // head hcol+i+1
+          // even lane needs the odd lane's value of head i; odd lane needs the even lane's of i+1
+          const float give = odd ? a0 : a1;
+          const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+          const int h = hcol + i + (odd ? 1 : 0);
+          const uint32_t pair = odd ? (uint32_t)to16<kBf16>(got) | ((uint32_t)to16<kBf16>(a1) << 16)
+                                    : (uint32_t)to16<kBf16>(a0) | ((uint32_t)to16<kBf16>(got) << 16);
+          orow[((int64_t)h * kDkv + d_even) >> 1] = pair;
+        }
       }
       tc_fence_before();
       __syncwarp();
