@@ -80,6 +80,21 @@ __device__ __forceinline__ int rows_needed(const Params& p, int t) {
   return (p.skip_k_top > 0 && n <= p.skip_k_top) ? 0 : n;
 }
 
+// Packed fp32 pairs (sm_100 family): d = a * b + c element-wise, round to nearest.
+__device__ __forceinline__ uint64_t pack_f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack_f2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 template <int TPT>
 __device__ __forceinline__ int group_rows(const Params& p, int g) {
   int m = 0;
@@ -230,16 +245,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;   // TMEM lanes 32*quad .. 32*quad+31
     const int half = e >> 2;     // which half of the tile's tokens
     float* my_w = sw + e * 128;  // this warp's w[t, h] for its tokens, fp32
+    constexpr int WPL = (C::HALF * H) / 32;  // w values per lane per group (always 4)
+    // the next group's w and visibility are loaded into registers one group ahead
+    float w_next[WPL];
+    int nvis_next[C::HALF];
+    auto prefetch = [&](int g) {
+      const int t0 = g * C::TPT + half * C::HALF;
+#pragma unroll
+      for (int i = 0; i < WPL; ++i) {
+        const int idx = lane + 32 * i;
+        const int t = t0 + idx / H;
+        w_next[i] = t < p.T ? __half2float(p.w[(int64_t)t * H + (idx % H)]) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < C::HALF; ++j) nvis_next[j] = (t0 + j < p.T) ? n_visible(p, t0 + j) : 0;
+    };
     int cur_g = -1, rows = 0;
-    bool loaded = false;
     uint32_t a_it = 0;
     int nvis[C::HALF];
+    if (beg < end) prefetch((int)(beg / p.n_stiles));
     for (long long it = beg; it < end; ++it) {
       const int g = (int)(it / p.n_stiles), st = (int)(it % p.n_stiles);
       if (g != cur_g) {
         cur_g = g;
         rows = group_rows<C::TPT>(p, g);
-        loaded = false;
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < WPL; ++i) my_w[lane + 32 * i] = w_next[i];
+#pragma unroll
+        for (int j = 0; j < C::HALF; ++j) nvis[j] = nvis_next[j];
+        __syncwarp();
+        const long long next_group_item = (long long)(g + 1) * p.n_stiles;
+        if (next_group_item < end) prefetch(g + 1);
       }
       const int row = st * kTileS + quad * 32 + lane;
       const int t0 = g * C::TPT + half * C::HALF;
@@ -251,17 +288,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      if (!loaded) {
-        __syncwarp();
-        for (int i = lane; i < C::HALF * H; i += 32) {
-          const int t = t0 + i / H;
-          my_w[i] = t < p.T ? __half2float(p.w[(int64_t)t * H + (i % H)]) : 0.f;
-        }
-#pragma unroll
-        for (int j = 0; j < C::HALF; ++j) nvis[j] = (t0 + j < p.T) ? n_visible(p, t0 + j) : 0;
-        __syncwarp();
-        loaded = true;
-      }
       const int ab = a_it & 1;
       if (!mbar_wait(&afull[ab], (a_it >> 1) & 1, p.status, 6)) break;
       tc_fence_after();
@@ -269,37 +295,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < C::HALF; ++j) {
         const uint32_t col = (half * C::HALF + j) * H;
-        float acc = 0.f;
-        if constexpr (H >= 32) {
+        // sum_h w[h] * max(0, acc[h]): ReLU in scalar, products in packed f32x2 pairs
+        uint64_t a01 = 0, a23 = 0;  // two pair accumulators (bit pattern 0 = +0.0f, +0.0f)
+        constexpr int CH = H >= 32 ? 32 : H;
 #pragma unroll
-          for (int c = 0; c < H; c += 32) {
-            float v[32];
-            tmem_ld32(t_row + col + c, v);
-            tc_wait_ld();
-            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-            for (int h = 0; h < 32; h += 4) {
-              a0 = fmaf(my_w[j * H + c + h + 0], fmaxf(v[h + 0], 0.f), a0);
-              a1 = fmaf(my_w[j * H + c + h + 1], fmaxf(v[h + 1], 0.f), a1);
-              a2 = fmaf(my_w[j * H + c + h + 2], fmaxf(v[h + 2], 0.f), a2);
-              a3 = fmaf(my_w[j * H + c + h + 3], fmaxf(v[h + 3], 0.f), a3);
-            }
-            acc += (a0 + a1) + (a2 + a3);
-          }
-        } else {
-          float v[16];
-          tmem_ld16(t_row + col, v);
+        for (int c = 0; c < H; c += CH) {
+          float v[CH];
+          if constexpr (CH == 32) tmem_ld32(t_row + col + c, v);
+          else tmem_ld16(t_row + col + c, v);
           tc_wait_ld();
-          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-          for (int h = 0; h < 16; h += 4) {
-            a0 = fmaf(my_w[j * H + h + 0], fmaxf(v[h + 0], 0.f), a0);
-            a1 = fmaf(my_w[j * H + h + 1], fmaxf(v[h + 1], 0.f), a1);
-            a2 = fmaf(my_w[j * H + h + 2], fmaxf(v[h + 2], 0.f), a2);
-            a3 = fmaf(my_w[j * H + h + 3], fmaxf(v[h + 3], 0.f), a3);
+          for (int h = 0; h < CH; h += 4) {
+            const float4 w4 = *reinterpret_cast<const float4*>(&my_w[j * H + c + h]);
+            a01 = ffma2(pack_f2(w4.x, w4.y), pack_f2(fmaxf(v[h], 0.f), fmaxf(v[h + 1], 0.f)), a01);
+            a23 = ffma2(pack_f2(w4.z, w4.w), pack_f2(fmaxf(v[h + 2], 0.f), fmaxf(v[h + 3], 0.f)), a23);
           }
-          acc = (a0 + a1) + (a2 + a3);
         }
+        float x0, x1, x2, x3;
+        unpack_f2(a01, x0, x1);
+        unpack_f2(a23, x2, x3);
+        const float acc = (x0 + x1) + (x2 + x3);
         if (t0 + j < p.T && row < p.S) p.scores[(int64_t)(t0 + j) * p.ld + row] = row < nvis[j] ? acc : -INFINITY;
       }
       tc_fence_before();
