@@ -7,25 +7,23 @@
 // by an index list, kv rows serving as both key and value), fed by the top-512 of "How I made
 // DeepSeek 12x faster on a Mac Studio", section "1: the kernels".
 //
-// One CTA per SM, persistent over tokens; per token the 512 selected rows are processed in
-// chunks of 128.  Both products run on tcgen05 with M = 128 by putting the selected rows /
-// the value dimension on the M axis:
-//   logits^T [128 rows x 64 heads]  = Ksel [128 x 512] . Q^T           (A, B K-major)
-//   O^T      [512 dims x 64 heads] += Vsel^T [512 x 128] . P^T [128 x 64] (A, B MN-major)
-// with the fp32 accumulators in TMEM (logits double-buffered in columns 0..127, O^T in
-// columns 256..511).  The softmax runs over TMEM lanes (the rows), so the per-head max and sum
-// are cross-lane: each warp does a 31-shuffle transpose-reduction of its 32 rows x 32 heads,
-// then four warps combine through shared memory.  The running max is only raised when a
-// head's max grows by more than 2^8 (then O^T and the partial sums are rescaled in place),
-// so the probabilities written as fp16/bf16 stay <= 256.
+// One CTA per SM, persistent over tokens.  A token's selected rows are processed in chunks of
+// 64, double-buffered in shared memory (each row is gathered with 16-byte cp.async into the
+// 128B-swizzled layout both products read: 8 slots of 64 dims per chunk).  Per chunk:
+//   S   [64 heads x 64 rows] = Q . Ksel^T     tcgen05, M = 64 (heads on TMEM lanes), K-major
+//   O^T [512 x 64 heads]    += Vsel^T . P^T   tcgen05, M = 128 (dims), A MN-major, B K-major
+// S puts each head's 64 scores in one TMEM lane; a 16x256b load spreads them over 4 threads,
+// so a head's max and sum take two shuffles.  The running max of a head is only raised when its logits exceed it by
+// more than 2^8 (then O^T's column and the head's sum are rescaled), so the probabilities
+// written as fp16/bf16 stay <= 256.
 //
-// Rows are gathered with 16-byte cp.async (zero-filled for invalid indices) straight into the
-// 128B-swizzled layout both products read: row j of a chunk occupies one 128-byte line in
-// each of 8 slots (slot = 64 consecutive dims); a slot is refilled as soon as the O^T product
-// that reads it has completed.
-//
-// Warps: 0-3 gather (128 threads; thread 0 also loads Q by TMA), 4-11 softmax and output
-// (warp%4 = TMEM lane quadrant, (warp-4)/4 = which 32 heads), 12 MMA issue + TMEM allocation.
+// Warps: 0-3 gather, 4-7 softmax (heads 16*(warp-4) .. +15, 4 threads a head), 8-11 output
+// (O^T lanes by quadrant), 12 issues the S products, 13 the O^T products, 14 loads q_attn.
+// The two MMA warps run converged and issue with elect.sync in straight runs, so S of chunk
+// c+2 and O^T of chunk c+1 interleave in the tensor pipe.  Buffers are released in 128-dim
+// pieces: a chunk's slot pair as its O^T product completes (the next gather starts early), a
+// pair of q blocks as the token's last S product passes it, a d-block of O^T as soon as the
+// output warps hold it in registers.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -39,30 +37,33 @@ namespace {
 
 constexpr int kHq = 64;
 constexpr int kDkv = 512;
-constexpr int kRows = 128;                      // rows per chunk
+constexpr int kRows = 64;                       // rows per chunk
 constexpr int kSlots = kDkv / 64;               // 8 slots of 64 dims
-constexpr int kSlotBytes = kRows * 128;         // 16 KB
+constexpr int kPairs = kSlots / 2;              // 128-dim blocks of O^T
+constexpr int kSlotBytes = kRows * 128;         // 8 KB
+constexpr int kBufBytes = kSlots * kSlotBytes;  // 64 KB per chunk buffer
 constexpr int kQBlockBytes = kHq * 128;         // 8 KB (64 heads x 64 dims)
 constexpr int kQBytes = kSlots * kQBlockBytes;  // 64 KB
-constexpr int kPBytes = kRows * 128;            // 16 KB (128 rows x 64 heads)
+constexpr int kPBytes = kHq * 128;              // 8 KB: P[h][j], 64 heads x 64 rows
 constexpr int kOffKV = kQBytes;
-constexpr int kOffP = kOffKV + kSlots * kSlotBytes;
-constexpr int kOffRed = kOffP + 2 * kPBytes;          // float[4][64]
-constexpr int kOffM = kOffRed + 4 * kHq * 4;          // float[64] running max (log2 units)
-constexpr int kOffAlpha = kOffM + kHq * 4;            // float[64] rescale factors / 1/l
-constexpr int kOffBars = kOffAlpha + kHq * 4;
-constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 2 + 2 + 2;
+constexpr int kOffP = kOffKV + 2 * kBufBytes;
+constexpr int kOffAlpha = kOffP + 2 * kPBytes;  // float[64] rescale factors of one chunk
+constexpr int kOffLM = kOffAlpha + kHq * 4;     // float[2 tokens][3 (l, m, 1/l)][64]
+constexpr int kOffBars = kOffLM + 2 * 3 * kHq * 4;
+constexpr int kNumBars = 2 * kPairs + 2 * 2 * kPairs + 2 + 2 + 2 + 2 + 2 * kPairs + 2 + 2;
 constexpr int kOffTmemSlot = kOffBars + kNumBars * 8;
 constexpr int kSmem = kOffTmemSlot + 16;
-constexpr int kThreads = 13 * 32;
-constexpr int kMmaWarp = 12;
+constexpr int kThreads = 15 * 32;
+constexpr int kSWarp = 12;   // issues S, allocates TMEM
+constexpr int kOWarp = 13;   // issues O^T
+constexpr int kQWarp = 14;   // loads q_attn of each token by TMA
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.0f;
-constexpr int kSoftBar = 2;      // named barrier of the 8 softmax warps
-constexpr int kSoftThreads = 256;
+constexpr int kSoftBar = 1, kEpiBar = 2, kGroupThreads = 128;
 
 struct Params {
+  const uint16_t* q;         // q_attn [T, 64, 512]; read by TMA (and prefetched to L2 a token ahead)
   const uint16_t* kv;        // [S, 512]; never read through an invalid index
   const uint16_t* zero_src;  // any valid address: source of the zero-filled (size 0) copies
   const int32_t* indices;
@@ -81,6 +82,9 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
 }
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -174,8 +178,8 @@ __device__ __forceinline__ uint16_t to16(float x) {
 template <bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_mqa_kernel(const __grid_constant__ CUtensorMap tm_q, const Params p) {
-  constexpr uint32_t kIdescS = idesc_f16(128, kHq, kBf16 ? 1 : 0, 0, 0);
-  constexpr uint32_t kIdescO = idesc_f16(128, kHq, kBf16 ? 1 : 0, 1, 1);
+  constexpr uint32_t kIdescS = idesc_f16(64, kHq, kBf16 ? 1 : 0, 0, 0);
+  constexpr uint32_t kIdescO = idesc_f16(128, kHq, kBf16 ? 1 : 0, 1, 0);
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {  // the swizzled layouts need a 1024-byte aligned base
     if (threadIdx.x == 0) report_timeout(p.status, 0x7f);
@@ -184,43 +188,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sq = smem;
   uint8_t* skv = smem + kOffKV;
   uint8_t* sp = smem + kOffP;
-  float* red = reinterpret_cast<float*>(smem + kOffRed);
-  float* m_run = reinterpret_cast<float*>(smem + kOffM);
-  float* alpha = reinterpret_cast<float*>(smem + kOffAlpha);
+  float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
+  float* lm = reinterpret_cast<float*>(smem + kOffLM);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
-  uint64_t* qfull = bars;
-  uint64_t* qempty = bars + 1;
-  uint64_t* slot_full = bars + 2;
-  uint64_t* slot_empty = slot_full + kSlots;
-  uint64_t* sfull = slot_empty + kSlots;
+  uint64_t* qfull = bars;                   // [pair of 64-dim blocks]
+  uint64_t* qempty = bars + kPairs;         // [pair]
+  uint64_t* kvfull = bars + 2 * kPairs;     // [buffer][pair]
+  uint64_t* kvempty = kvfull + 2 * kPairs;  // [buffer][pair]
+  uint64_t* sfull = kvempty + 2 * kPairs;
   uint64_t* sempty = sfull + 2;
   uint64_t* pfull = sempty + 2;
   uint64_t* pempty = pfull + 2;
-  uint64_t* ofull = pempty + 2;
-  uint64_t* oempty = ofull + 1;
+  uint64_t* ofull = pempty + 2;             // [d-block]
+  uint64_t* oempty = ofull + kPairs;        // [d-block]
+  uint64_t* lready = oempty + kPairs;            // [token parity] l, m of a token written
+  uint64_t* lfree = lready + 2;             // [token parity] ... and read by the output warps
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int nch = p.nchunks;
   if (threadIdx.x == 0) {
-    mbar_init(qfull, 1);
-    mbar_init(qempty, 1);
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(&slot_full[i], 128);
-      mbar_init(&slot_empty[i], 1);
+    for (int i = 0; i < kPairs; ++i) {
+      mbar_init(&qfull[i], 1);
+      mbar_init(&qempty[i], 1);
+      mbar_init(&ofull[i], 1);
+      mbar_init(&oempty[i], 4);
+    }
+    for (int i = 0; i < 2 * kPairs; ++i) {
+      mbar_init(&kvfull[i], 128);
+      mbar_init(&kvempty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sfull[i], 1);
-      mbar_init(&sempty[i], 8);
-      mbar_init(&pfull[i], 8);
+      mbar_init(&sempty[i], 4);
+      mbar_init(&pfull[i], 4);
       mbar_init(&pempty[i], 1);
+      mbar_init(&lready[i], 4);
+      mbar_init(&lfree[i], 4);
     }
-    mbar_init(ofull, 1);
-    mbar_init(oempty, 8);
     fence_mbarrier_init();
     tma_prefetch_desc(&tm_q);
   }
-  if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == kSWarp) tmem_alloc(tmem_slot, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -228,273 +238,350 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     // ------------------------------------------------------------------------ gather
-    const int pt = threadIdx.x;  // 0..127
-    const int ch = pt & 7;       // 16-byte column chunk within a 128-byte line
+    // thread pt copies 16-byte column chunk `ch` of rows (pt>>3) + 16 i, i = 0..3, in every slot
+    const int pt = threadIdx.x;
+    const int ch = pt & 7;
+    uint32_t dst_off[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = (pt >> 3) + 16 * i;
+      dst_off[i] = r * 128 + ((ch ^ (r & 7)) << 4);
+    }
+    auto load_idx = [&](int t, int c, int32_t (&idx)[4]) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int j = c * kRows + (pt >> 3) + 16 * i;
+        idx[i] = (t < p.T && j < p.k_top) ? __ldg(p.indices + (int64_t)t * p.k_top + j) : -1;
+      }
+    };
     uint32_t gc = 0, tok_i = 0;
     bool ok = true;
+    int32_t idx[4];
+    load_idx(blockIdx.x, 0, idx);
     for (int t = blockIdx.x; t < p.T && ok; t += gridDim.x, ++tok_i) {
-      if (pt == 0) {
-        if (!mbar_wait(qempty, (tok_i & 1) ^ 1, p.status, 20)) { ok = false; }
-        if (ok) {
-          mbar_arrive_expect_tx(qfull, kQBytes);
-          for (int kb = 0; kb < kSlots; ++kb) tma_load_2d(sq + kb * kQBlockBytes, &tm_q, qfull, kb * 64, t * kHq);
-        }
-      }
-      for (int c = 0; c < p.nchunks && ok; ++c, ++gc) {
-        // this thread copies 16-byte column chunk `ch` of rows (pt>>3) + 16 i, i = 0..7, in every
-        // slot: the source row offsets and the swizzled destinations are fixed for the chunk
-        const char* src_row[8];
-        uint32_t dst_off[8], src_bytes[8];
+      for (int c = 0; c < nch && ok; ++c, ++gc) {
+        const char* src[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int r = (pt >> 3) + 16 * i;
-          const int j = c * kRows + r;
-          int32_t idx = -1;
-          if (j < p.k_top) idx = __ldg(p.indices + (int64_t)t * p.k_top + j);
-          const bool valid = idx >= 0 && idx < p.S;
-          src_row[i] = valid ? reinterpret_cast<const char*>(p.kv + (int64_t)idx * kDkv) + ch * 16
-                             : reinterpret_cast<const char*>(p.zero_src);
-          src_bytes[i] = valid ? 16u : 0u;
-          dst_off[i] = r * 128 + ((ch ^ (r & 7)) << 4);
+        for (int i = 0; i < 4; ++i)
+          src[i] = (idx[i] >= 0 && idx[i] < p.S)
+                       ? reinterpret_cast<const char*>(p.kv + (int64_t)idx[i] * kDkv) + ch * 16
+                       : nullptr;
+        // the next chunk's indices are on their way while this chunk is issued
+        {
+          const int nt = (c + 1 < nch) ? t : t + (int)gridDim.x;
+          load_idx(nt, (c + 1 < nch) ? c + 1 : 0, idx);
         }
-        for (int kb = 0; kb < kSlots; ++kb) {
-          if (!mbar_wait(&slot_empty[kb], (gc & 1) ^ 1, p.status, 21)) { ok = false; break; }
-          const uint32_t base = smem_u32(skv + kb * kSlotBytes);
+        const int b = gc & 1;
+        uint8_t* buf = skv + b * kBufBytes;
+        for (int pr = 0; pr < kPairs; ++pr) {
+          if (!mbar_wait(&kvempty[b * kPairs + pr], ((gc >> 1) & 1) ^ 1, p.status, 21)) { ok = false; break; }
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            cp_async16(base + dst_off[i], src_row[i] + (src_bytes[i] ? kb * 128 : 0), src_bytes[i]);
-          cp_async_arrive(&slot_full[kb]);
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int kb = 2 * pr + h2;
+            const uint32_t base = smem_u32(buf + kb * kSlotBytes);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              cp_async16(base + dst_off[i], src[i] ? src[i] + kb * 128 : reinterpret_cast<const char*>(p.zero_src),
+                         src[i] ? 16u : 0u);
+          }
+          cp_async_arrive(&kvfull[b * kPairs + pr]);
         }
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-  } else if (warp == kMmaWarp) {
-    // --------------------------------------------------------------------------- MMA
-    if (lane == 0) {
-      uint32_t gc = 0, tok_i = 0;
-      bool ok = true;
-      const uint32_t q_addr = smem_u32(sq);
-      const uint32_t kv_addr = smem_u32(skv);
-      const uint32_t p_addr = smem_u32(sp);
-      for (int t = blockIdx.x; t < p.T && ok; t += gridDim.x, ++tok_i) {
-        if (!mbar_wait(qfull, tok_i & 1, p.status, 30)) break;
-        tc_fence_after();
-        for (int c = 0; c < p.nchunks; ++c, ++gc) {
-          const int sb = gc & 1;
-          if (!mbar_wait(&sempty[sb], ((gc >> 1) & 1) ^ 1, p.status, 31)) { ok = false; break; }
+  } else if (warp == kSWarp) {
+    // ------------------------------------------------------------------ S = Q Ksel^T
+    uint32_t gc = 0, tok_i = 0;
+    bool ok = true;
+    const uint32_t q_addr = smem_u32(sq);
+    const uint32_t kv_addr = smem_u32(skv);
+    for (int t = blockIdx.x; t < p.T && ok; t += gridDim.x, ++tok_i) {
+      for (int c = 0; c < nch; ++c, ++gc) {
+        const int sb = gc & 1, b = gc & 1;
+        if (!mbar_wait(&sempty[sb], ((gc >> 1) & 1) ^ 1, p.status, 31)) { ok = false; break; }
+        for (int pr = 0; pr < kPairs; ++pr) {
+          if (c == 0 && !mbar_wait(&qfull[pr], tok_i & 1, p.status, 30)) { ok = false; break; }
+          if (!mbar_wait(&kvfull[b * kPairs + pr], (gc >> 1) & 1, p.status, 32)) { ok = false; break; }
+          fence_proxy_async();  // gathered rows -> visible to the tensor core
           tc_fence_after();
-          for (int kb = 0; kb < kSlots && ok; ++kb) {
-            if (!mbar_wait(&slot_full[kb], gc & 1, p.status, 32)) { ok = false; break; }
-            fence_proxy_async();  // cp.async data -> visible to the tensor core
-            tc_fence_after();
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int kb = 2 * pr + h2;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t a = desc_sw128(kv_addr + kb * kSlotBytes + kk * 32, 16, 1024);
-              const uint64_t b = desc_sw128(q_addr + kb * kQBlockBytes + kk * 32, 16, 1024);
-              tc_mma_f16(tmem + sb * kHq, a, b, kIdescS, (kb | kk) != 0);
+              const uint64_t a = desc_sw128(q_addr + kb * kQBlockBytes + kk * 32, 16, 1024);
+              const uint64_t bd = desc_sw128(kv_addr + b * kBufBytes + kb * kSlotBytes + kk * 32, 16, 1024);
+              tc_mma_f16_elect(tmem + sb * kHq, a, bd, kIdescS, (kb | kk) != 0);
             }
           }
-          if (!ok) break;
-          tc_commit(&sfull[sb]);
-          if (c == p.nchunks - 1) tc_commit(qempty);
-          const int pb = gc & 1;
-          if (!mbar_wait(&pfull[pb], (gc >> 1) & 1, p.status, 33)) { ok = false; break; }
-          if (c == 0 && !mbar_wait(oempty, (tok_i & 1) ^ 1, p.status, 34)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll 1
-          for (int db = 0; db < kDkv / 128; ++db) {
-#pragma unroll
-            for (int ks = 0; ks < kRows / 16; ++ks) {
-              const uint64_t a = desc_sw128(kv_addr + (2 * db) * kSlotBytes + ks * 2048, kSlotBytes, 1024);
-              const uint64_t b = desc_sw128(p_addr + pb * kPBytes + ks * 2048, kSlotBytes, 1024);
-              tc_mma_f16(tmem + kColO + db * kHq, a, b, kIdescO, (c > 0 || ks > 0));
-            }
-            tc_commit(&slot_empty[2 * db]);
-            tc_commit(&slot_empty[2 * db + 1]);
-          }
-          tc_commit(&pempty[pb]);
+          if (c == nch - 1) tc_commit_elect(&qempty[pr]);  // the next token's q may replace this pair
         }
         if (!ok) break;
-        tc_commit(ofull);
+        tc_commit_elect(&sfull[sb]);
       }
     }
-  } else if (warp >= 4 && warp < 12) {
-    // ---------------------------------------------------------- softmax and output
-    const int quad = warp & 3;
-    const int hh = (warp - 4) >> 2;  // heads 32*hh .. 32*hh+31
-    const int hcol = hh * 32;
-    const bool owner = (quad == 0);  // lane l of warps 4 and 8 owns head hcol + l
-    const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
+  } else if (warp == kOWarp) {
+    // --------------------------------------------------------------- O^T += V^T P^T
     uint32_t gc = 0, tok_i = 0;
-    float lpart[32];
     bool ok = true;
-    // validity of this thread's row in the next chunk, loaded one chunk ahead
-    auto row_valid = [&](int t, int c) {
-      const int j = c * kRows + quad * 32 + lane;
-      if (t >= p.T || c >= p.nchunks || j >= p.k_top) return false;
-      const int32_t idx = __ldg(p.indices + (int64_t)t * p.k_top + j);
-      return idx >= 0 && idx < p.S;
-    };
-    bool next_valid = row_valid(blockIdx.x, 0);
+    const uint32_t kv_addr = smem_u32(skv);
+    const uint32_t p_addr = smem_u32(sp);
     for (int t = blockIdx.x; t < p.T && ok; t += gridDim.x, ++tok_i) {
+      for (int c = 0; c < nch; ++c, ++gc) {
+        const int pb = gc & 1, b = gc & 1;
+        if (!mbar_wait(&pfull[pb], (gc >> 1) & 1, p.status, 33)) { ok = false; break; }
+        tc_fence_after();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) lpart[i] = 0.f;
-      for (int c = 0; c < p.nchunks; ++c, ++gc) {
-        const bool valid = next_valid;
-        next_valid = (c + 1 < p.nchunks) ? row_valid(t, c + 1) : row_valid(t + gridDim.x, 0);
+        for (int db = 0; db < kPairs; ++db) {
+          // a token's first product overwrites O^T: the previous token's output must have read it
+          if (c == 0) {
+            if (!mbar_wait(&oempty[db], (tok_i & 1) ^ 1, p.status, 34)) { ok = false; break; }
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int ks = 0; ks < kRows / 16; ++ks) {
+            const uint64_t a = desc_sw128(kv_addr + b * kBufBytes + (2 * db) * kSlotBytes + ks * 2048, kSlotBytes, 1024);
+            const uint64_t bd = desc_sw128(p_addr + pb * kPBytes + ks * 32, 16, 1024);
+            tc_mma_f16_elect(tmem + kColO + db * kHq, a, bd, kIdescO, (c > 0 || ks > 0));
+          }
+          tc_commit_elect(&kvempty[b * kPairs + db]);  // this 128-dim slice of the chunk is free
+          if (c == nch - 1) tc_commit_elect(&ofull[db]);
+        }
+        if (!ok) break;
+        tc_commit_elect(&pempty[pb]);
+      }
+    }
+  } else if (warp < 8) {
+    // ---------------------------------------------------------------------- softmax
+    // S holds head 16q + i on TMEM lane 32q + i (i < 16).  The 16x256b load gives thread
+    // (g = lane/4, e = lane%4) the heads hA = 16q + g and hB = hA + 8 and, of each, the
+    // columns 8r + 2e + {0, 1}, r = 0..7: every head's 64 scores are spread over 4 threads.
+    const int quad = warp - 4;
+    const int g = lane >> 2, e = lane & 3;
+    const int hA = 16 * quad + g, hB = hA + 8;
+    const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
+    const float c = p.scale_log2;
+    uint32_t gc = 0, tok_i = 0;
+    bool ok = true;
+    // validity of the 64 rows of a chunk: two ballots over per-lane index loads, one chunk ahead
+    auto load_valid = [&](int t, int ci, int32_t& i0, int32_t& i1) {
+      const int j0 = ci * kRows + lane, j1 = j0 + 32;
+      i0 = (t < p.T && ci < nch && j0 < p.k_top) ? __ldg(p.indices + (int64_t)t * p.k_top + j0) : -1;
+      i1 = (t < p.T && ci < nch && j1 < p.k_top) ? __ldg(p.indices + (int64_t)t * p.k_top + j1) : -1;
+    };
+    int32_t ni0, ni1;
+    load_valid(blockIdx.x, 0, ni0, ni1);
+    for (int t = blockIdx.x; t < p.T && ok; t += gridDim.x, ++tok_i) {
+      float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;  // running max (scaled, log2) and sum
+      for (int ci = 0; ci < nch; ++ci, ++gc) {
+        const uint32_t v0 = __ballot_sync(0xffffffffu, ni0 >= 0 && ni0 < p.S) >> (2 * e);
+        const uint32_t v1 = __ballot_sync(0xffffffffu, ni1 >= 0 && ni1 < p.S) >> (2 * e);
+        {
+          const int nt = (ci + 1 < nch) ? t : t + (int)gridDim.x;
+          load_valid(nt, (ci + 1 < nch) ? ci + 1 : 0, ni0, ni1);
+        }
         const int sb = gc & 1;
-        ok = named_and(kSoftBar, kSoftThreads, mbar_wait(&sfull[sb], (gc >> 1) & 1, p.status, 40));
+        ok = named_and(kSoftBar, kGroupThreads, mbar_wait(&sfull[sb], (gc >> 1) & 1, p.status, 40));
         if (!ok) break;
         tc_fence_after();
         float x[32];
-        tmem_ld32(tmem + t_lane + sb * kHq + hcol, x);
+        tmem_ld_16x256b_x8(tmem + t_lane + sb * kHq, x);
         tc_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sempty[sb]);
+        float mxA = -INFINITY, mxB = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = valid ? x[i] * p.scale_log2 : -INFINITY;
-        // The running max of a head only has to keep every logit within 2^8 of it (so the
-        // probabilities stay <= 256); the exact column max is taken on a token's first chunk and
-        // again only when some logit overshoots the running max by more than that.
-        bool over = (c == 0);
-        if (c > 0) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 m4 = *reinterpret_cast<const float4*>(&m_run[hcol + i]);
-            over |= (x[i] > m4.x + kRescaleLog2) | (x[i + 1] > m4.y + kRescaleLog2) |
-                    (x[i + 2] > m4.z + kRescaleLog2) | (x[i + 3] > m4.w + kRescaleLog2);
-          }
+        for (int r = 0; r < 8; ++r) {
+          const uint32_t bits = (r < 4 ? v0 : v1) >> (8 * (r & 3));
+          const bool ok0 = (bits & 1u) != 0, ok1 = (bits & 2u) != 0;
+          x[4 * r] = ok0 ? x[4 * r] : -INFINITY;
+          x[4 * r + 2] = ok0 ? x[4 * r + 2] : -INFINITY;
+          x[4 * r + 1] = ok1 ? x[4 * r + 1] : -INFINITY;
+          x[4 * r + 3] = ok1 ? x[4 * r + 3] : -INFINITY;
+          mxA = fmaxf(mxA, fmaxf(x[4 * r], x[4 * r + 1]));
+          mxB = fmaxf(mxB, fmaxf(x[4 * r + 2], x[4 * r + 3]));
         }
-        const bool rescan = named_or(kSoftBar, kSoftThreads, over);
-        bool rescale = false;
-        if (rescan) {
-          float tmp[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) tmp[i] = x[i];
-          red[quad * kHq + hcol + lane] = warp_columns_reduce<true>(tmp);
-          named_sync(kSoftBar, kSoftThreads);
-          bool need = false;
-          if (owner) {
-            const int h = hcol + lane;
-            const float cm = fmaxf(fmaxf(red[h], red[kHq + h]), fmaxf(red[2 * kHq + h], red[3 * kHq + h]));
-            const float mo = (c == 0) ? -INFINITY : m_run[h];
-            float a = 1.f;
-            if (cm > mo + kRescaleLog2 || (mo == -INFINITY && cm > -INFINITY)) {
-              a = (mo == -INFINITY) ? 0.f : ex2_approx(mo - cm);
-              m_run[h] = cm;
-              need = (c > 0) && (mo != -INFINITY);
-            } else if (c == 0) {
-              m_run[h] = mo;  // -inf: nothing visible yet
-            }
-            alpha[h] = a;
-          }
-          rescale = named_or(kSoftBar, kSoftThreads, need);
+        mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 1));
+        mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 1));
+        mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 2)) * c;
+        mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 2)) * c;
+        // lazy running max: raised only when a logit exceeds it by more than 2^8 (or the head
+        // saw its first valid row; alpha = 0 then, and nothing was accumulated for it yet)
+        float aA = 1.f, aB = 1.f;
+        bool needA = false, needB = false;
+        if (mxA > mA + kRescaleLog2) {
+          needA = mA != -INFINITY;
+          aA = needA ? ex2_approx(mA - mxA) : 0.f;
+          mA = mxA;
         }
-        if (rescale) {
-          // O^T and the partial sums were built with the old max: scale them first, once the
-          // previous chunk's O^T product has completed.
+        if (mxB > mB + kRescaleLog2) {
+          needB = mB != -INFINITY;
+          aB = needB ? ex2_approx(mB - mxB) : 0.f;
+          mB = mxB;
+        }
+        if (named_or(kSoftBar, kGroupThreads, needA || needB)) {
+          if (e == 0) {
+            alpha_s[hA] = needA ? aA : 1.f;
+            alpha_s[hB] = needB ? aB : 1.f;
+          }
+          named_sync(kSoftBar, kGroupThreads);
+          // O^T must hold all of the previous chunk before its columns are rescaled
           const uint32_t prev = gc - 1;
-          ok = named_and(kSoftBar, kSoftThreads, mbar_wait(&pempty[prev & 1], (prev >> 1) & 1, p.status, 41));
+          ok = named_and(kSoftBar, kGroupThreads, mbar_wait(&pempty[prev & 1], (prev >> 1) & 1, p.status, 41));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
-          for (int db = 0; db < kDkv / 128; ++db) {
+          for (int q2 = 0; q2 < 2 * kPairs; ++q2) {  // 4 d-blocks x 2 halves of 32 heads
             float v[32];
-            const uint32_t ta = tmem + t_lane + kColO + db * kHq + hcol;
+            const uint32_t ta = tmem + t_lane + kColO + (q2 >> 1) * kHq + (q2 & 1) * 32;
             tmem_ld32(ta, v);
             tc_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= alpha[hcol + i];
+            for (int i = 0; i < 32; ++i) v[i] *= alpha_s[(q2 & 1) * 32 + i];
             tmem_st32(ta, v);
           }
           tc_wait_st();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) lpart[i] *= alpha[hcol + i];
+          named_sync(kSoftBar, kGroupThreads);
         }
-        // probabilities, rounded to the kv dtype (the sums use the rounded values)
-        uint32_t packed[16];
+        lA *= aA;
+        lB *= aB;
+        // p = 2^(x c - m), rounded to the kv dtype; the sums use the rounded values
+        const float nA = (mA == -INFINITY) ? 0.f : -mA;
+        const float nB = (mB == -INFINITY) ? 0.f : -mB;
+        uint32_t pkA[8], pkB[8];
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          float4 m4 = *reinterpret_cast<const float4*>(&m_run[hcol + i]);
-          // a head with no visible row yet has m = -inf and only -inf logits: use 0 instead
-          m4.x = m4.x == -INFINITY ? 0.f : m4.x;
-          m4.y = m4.y == -INFINITY ? 0.f : m4.y;
-          m4.z = m4.z == -INFINITY ? 0.f : m4.z;
-          m4.w = m4.w == -INFINITY ? 0.f : m4.w;
+        for (int r = 0; r < 8; ++r) {
           float r0, r1, r2, r3;
-          packed[(i >> 1) + 0] = pack2<kBf16>(ex2_approx(x[i] - m4.x), ex2_approx(x[i + 1] - m4.y), r0, r1);
-          packed[(i >> 1) + 1] = pack2<kBf16>(ex2_approx(x[i + 2] - m4.z), ex2_approx(x[i + 3] - m4.w), r2, r3);
-          lpart[i] += r0;
-          lpart[i + 1] += r1;
-          lpart[i + 2] += r2;
-          lpart[i + 3] += r3;
+          pkA[r] = pack2<kBf16>(ex2_approx(fmaf(x[4 * r], c, nA)), ex2_approx(fmaf(x[4 * r + 1], c, nA)), r0, r1);
+          pkB[r] = pack2<kBf16>(ex2_approx(fmaf(x[4 * r + 2], c, nB)), ex2_approx(fmaf(x[4 * r + 3], c, nB)), r2, r3);
+          lA += r0 + r1;
+          lB += r2 + r3;
         }
         const int pb = gc & 1;
-        ok = named_and(kSoftBar, kSoftThreads, mbar_wait(&pempty[pb], ((gc >> 1) & 1) ^ 1, p.status, 42));
+        ok = named_and(kSoftBar, kGroupThreads, mbar_wait(&pempty[pb], ((gc >> 1) & 1) ^ 1, p.status, 42));
         if (!ok) break;
         {
-          const int r = quad * 32 + lane;
-          uint8_t* line = sp + pb * kPBytes + r * 128;
+          // P[h][j], K-major with the 128-byte swizzle: 16-byte chunk r of line h at (r ^ (h & 7))
+          uint8_t* lineA = sp + pb * kPBytes + hA * 128 + 4 * e;
+          uint8_t* lineB = sp + pb * kPBytes + hB * 128 + 4 * e;
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int chunk = (hh * 4 + q4) ^ (r & 7);
-            *reinterpret_cast<uint4*>(line + chunk * 16) =
-                make_uint4(packed[q4 * 4 + 0], packed[q4 * 4 + 1], packed[q4 * 4 + 2], packed[q4 * 4 + 3]);
+          for (int r = 0; r < 8; ++r) {
+            *reinterpret_cast<uint32_t*>(lineA + ((r ^ (hA & 7)) << 4)) = pkA[r];
+            *reinterpret_cast<uint32_t*>(lineB + ((r ^ (hB & 7)) << 4)) = pkB[r];
           }
         }
         fence_proxy_async();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&pfull[pb]);
-      }
-      if (!ok) break;
-      // ------------------------------------------------------------ token epilogue
-      ok = named_and(kSoftBar, kSoftThreads, mbar_wait(ofull, tok_i & 1, p.status, 43));
-      if (!ok) break;
-      tc_fence_after();
-      red[quad * kHq + hcol + lane] = warp_columns_reduce<false>(lpart);
-      named_sync(kSoftBar, kSoftThreads);
-      if (owner) {
-        const int h = hcol + lane;
-        const float l = (red[h] + red[kHq + h]) + (red[2 * kHq + h] + red[3 * kHq + h]);
-        alpha[h] = l > 0.f ? 1.f / l : 0.f;
-        if (p.lse) p.lse[(int64_t)t * kHq + h] = l > 0.f ? (m_run[h] + log2f(l)) * 0.69314718055994531f : -INFINITY;
-      }
-      named_sync(kSoftBar, kSoftThreads);
-      // out[t, h, d]: lane = d within the 32-row quadrant of a 128-wide d-block.  Lanes pair up
-      // (d, d+1) so that each store writes two values: the even lane stores the even heads, the
-      // odd lane the odd heads.
-      uint32_t* orow = reinterpret_cast<uint32_t*>(p.out + (int64_t)t * kHq * kDkv);
-      const bool odd = lane & 1;
-#pragma unroll 1
-      for (int db = 0; db < kDkv / 128; ++db) {
-        float v[32];
-        tmem_ld32(tmem + t_lane + kColO + db * kHq + hcol, v);
-        tc_wait_ld();
-        const int d_even = db * 128 + quad * 32 + (lane & ~1);
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float a0 = v[i] * alpha[hcol + i];          // head hcol+i, this lane's d
-          const float a1 = v[i + 1] * alpha[hcol + i + 1];  // head hcol+i+1
-          // even lane needs the odd lane's value of head i; odd lane needs the even lane's of i+1
-          const float give = odd ? a0 : a1;
-          const float got = __shfl_xor_sync(0xffffffffu, give, 1);
-          const int h = hcol + i + (odd ? 1 : 0);
-          const uint32_t pair = odd ? (uint32_t)to16<kBf16>(got) | ((uint32_t)to16<kBf16>(a1) << 16)
-                                    : (uint32_t)to16<kBf16>(a0) | ((uint32_t)to16<kBf16>(got) << 16);
-          orow[((int64_t)h * kDkv + d_even) >> 1] = pair;
+        if (ci == nch - 1) {
+          lA += __shfl_xor_sync(0xffffffffu, lA, 1);
+          lB += __shfl_xor_sync(0xffffffffu, lB, 1);
+          lA += __shfl_xor_sync(0xffffffffu, lA, 2);
+          lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+          // the slot of this token's parity was last read by the output of token tok_i - 2
+          ok = named_and(kSoftBar, kGroupThreads,
+                         mbar_wait(&lfree[tok_i & 1], ((tok_i >> 1) & 1) ^ 1, p.status, 45));
+          if (!ok) break;
+          if (e == 0) {
+            float* row = lm + (tok_i & 1) * 3 * kHq;
+            row[hA] = lA;
+            row[kHq + hA] = mA;
+            row[2 * kHq + hA] = lA > 0.f ? 1.f / lA : 0.f;
+            row[hB] = lB;
+            row[kHq + hB] = mB;
+            row[2 * kHq + hB] = lB > 0.f ? 1.f / lB : 0.f;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&lready[tok_i & 1]);
         }
       }
-      tc_fence_before();
+    }
+  } else if (warp < 12) {
+    // ----------------------------------------------------------------------- output
+    // O^T lanes 32q + lane (dims) of each 128-dim block; every d-block is released to the next
+    // token's products as soon as it is in registers
+    const int quad = warp - 8;
+    const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
+    uint32_t tok_i = 0;
+    bool ok = true;
+    const bool odd = lane & 1;
+    for (int t = blockIdx.x; t < p.T && ok; t += gridDim.x, ++tok_i) {
+      const int par = tok_i & 1;
+      ok = named_and(kEpiBar, kGroupThreads, mbar_wait(&lready[par], (tok_i >> 1) & 1, p.status, 43));
+      if (!ok) break;
+      const float* lrow = lm + par * 3 * kHq;
+      if (quad == 0) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int hh = lane + 32 * k;
+          const float l = lrow[hh];
+          if (p.lse) p.lse[(int64_t)t * kHq + hh] = l > 0.f ? (lrow[kHq + hh] + log2f(l)) * 0.69314718055994531f : -INFINITY;
+        }
+      }
+      uint32_t* orow = reinterpret_cast<uint32_t*>(p.out + (int64_t)t * kHq * kDkv);
+#pragma unroll 1
+      for (int db = 0; db < kPairs; ++db) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&ofull[db], tok_i & 1, p.status, 44));
+        if (!ok) break;
+        tc_fence_after();
+        float v[64];
+        {
+          float va[32], vb[32];
+          tmem_ld32(tmem + t_lane + kColO + db * kHq, va);
+          tmem_ld32(tmem + t_lane + kColO + db * kHq + 32, vb);
+          tc_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            v[i] = va[i];
+            v[i + 32] = vb[i];
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&oempty[db]);
+        const int d_even = db * 128 + quad * 32 + (lane & ~1);
+#pragma unroll
+        for (int h0 = 0; h0 < kHq; h0 += 2) {
+          const float a0 = v[h0] * lrow[2 * kHq + h0];
+          const float a1 = v[h0 + 1] * lrow[2 * kHq + h0 + 1];
+          const float give = odd ? a0 : a1;
+          const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+          const int hw = h0 + (odd ? 1 : 0);
+          const uint32_t pair = odd ? (uint32_t)to16<kBf16>(got) | ((uint32_t)to16<kBf16>(a1) << 16)
+                                    : (uint32_t)to16<kBf16>(a0) | ((uint32_t)to16<kBf16>(got) << 16);
+          orow[((int64_t)hw * kDkv + d_even) >> 1] = pair;
+        }
+      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(oempty);
+      if (lane == 0) mbar_arrive(&lfree[par]);
+    }
+  } else if (warp == kQWarp) {
+    // ------------------------------------------------------------------------- q loader
+    if (lane == 0) {
+      uint32_t tok_i = 0;
+      for (int t = blockIdx.x; t < p.T; t += gridDim.x, ++tok_i) {
+        const int tn = t + (int)gridDim.x;  // the next token's q (64 KB, contiguous) moves to L2 now
+        if (tn < p.T) prefetch_l2(p.q + (int64_t)tn * kHq * kDkv, kQBytes);
+        bool ok = true;
+        for (int pr = 0; pr < kPairs; ++pr) {
+          if (!mbar_wait(&qempty[pr], (tok_i & 1) ^ 1, p.status, 20)) { ok = false; break; }
+          mbar_arrive_expect_tx(&qfull[pr], 2 * kQBlockBytes);
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int kb = 2 * pr + h2;
+            tma_load_2d(sq + kb * kQBlockBytes, &tm_q, &qfull[pr], kb * 64, t * kHq);
+          }
+        }
+        if (!ok) break;
+      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kSWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -541,6 +628,7 @@ int launch_impl(const AttnArgs& a, cudaStream_t stream) {
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return DS4X_ERR_CUDA;
   Params p;
+  p.q = static_cast<const uint16_t*>(a.q_attn);
   p.kv = static_cast<const uint16_t*>(a.kv);
   p.zero_src = static_cast<const uint16_t*>(a.q_attn);
   p.indices = a.indices;
