@@ -11,7 +11,9 @@ Printed (one JSON line, rank 0): the whole-job throughput in query tokens/s time
 events on the launching stream, per-stage times, the dominant kernel against its roofline
 (peaks from MEASURED_PEAKS.json), the same metric end to end through the C ABI with pinned
 host buffers (copies inside the timed region), the oracle timed on the host cores as a
-reported baseline, SM clocks sampled during the timed region, and the launch count.
+reported baseline, SM clocks sampled during the timed region, and the launch count.  A
+"decode" object adds the 1M-context decode loop (256 single-token steps, 63 row appends) in
+decode tokens/s, issued from the host and replayed as one CUDA graph.
 
 With --impl reference the oracle (plain C, fp64) is timed instead, on a bounded sample of
 the same workload per step.  Under torchrun (--gpus N), every rank runs its own chunk (the
@@ -51,6 +53,7 @@ def parse():
     ap.add_argument("--impl", default="ds4x", choices=["ds4x", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the 1M-context decode measurement")
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
 
@@ -230,6 +233,111 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------- decode loop
+def measure_decode(ds4x, torch, dev, stream, seed: int, reps: int = 3, n_steps: int = 256):
+    """The 1M-context decode: n_steps single-token steps from position 1048575 over 262144
+    resident rows, a row appended every 4 positions (63 over 256 steps), each step
+    score -> top-512 -> sparse MQA.  One timed unit is a whole ds4x_decode call (appends
+    included), L2 flushed before it; reported as issued from the host and as one CUDA-graph
+    replay of the same call, plus a per-kernel split of one step."""
+    wl = synth.WORKLOADS["decode_1m"]
+    S0 = wl.S
+    inp = synth.make_inputs(wl, seed=seed, T=n_steps, S=S0)
+    kvt = torch.bfloat16 if wl.kv_dtype == "bf16" else torch.float16
+
+    def dev16(a, dt):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(dt)
+
+    q, w, qa = dev16(inp.q, torch.float16), dev16(inp.w, torch.float16), dev16(inp.q_attn, kvt)
+    k, kv = dev16(inp.k, torch.float16), dev16(inp.kv, kvt)          # capacity rows
+    k_new, kv_new = k[S0:].clone(), kv[S0:].clone()                   # the rows the loop appends
+    cap = k.shape[0]
+    pos = torch.empty((n_steps,), dtype=torch.int32, device=dev)
+    idx = torch.empty((n_steps, wl.k_top), dtype=torch.int32, device=dev)
+    out = torch.empty_like(qa)
+    lse = torch.empty((n_steps, wl.Hq), dtype=torch.float32, device=dev)
+    ws = torch.empty((ds4x.decode_workspace_bytes(cap, wl.k_top),), dtype=torch.uint8, device=dev)
+    flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+
+    def call():
+        r = ds4x.decode(q, w, qa, k, kv, S0, wl.pos0, wl.ratio, k_new=k_new, kv_new=kv_new, k_top=wl.k_top,
+                        scale=wl.scale, positions=pos, indices=idx, out=out, lse=lse, workspace=ws, stream=stream)
+        return r[4], ds4x.last_launch_count()
+
+    s_final, launches = call()
+    torch.cuda.synchronize()
+    assert ds4x.device_status() == ds4x.OK
+    times = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = float(np.median(times))
+    # the same call captured once into a CUDA graph and replayed
+    graph_ms = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                ds4x.decode(q, w, qa, k, kv, S0, wl.pos0, wl.ratio, k_new=k_new, kv_new=kv_new, k_top=wl.k_top,
+                            scale=wl.scale, positions=pos, indices=idx, out=out, lse=lse, workspace=ws,
+                            stream=side)
+        stream.wait_stream(side)
+        gt = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            gt.append(e0.elapsed_time(e1))
+        graph_ms = float(np.median(gt))
+        assert ds4x.device_status() == ds4x.OK
+    except RuntimeError as e:  # capture refused: report the host-issued number only
+        graph_ms = None
+        print(f"decode graph capture unavailable: {e}", file=sys.stderr)
+    # per-kernel split of the last step (T = 1 over S_final rows), each stage timed alone
+    S = s_final
+    sc = torch.empty((1, S), dtype=torch.float32, device=dev)
+    tws = torch.empty((max(16, ds4x.topk_workspace_bytes(1, S, wl.k_top)),), dtype=torch.uint8, device=dev)
+    i = n_steps - 1
+    p_last = pos[i:i + 1].clone()          # a 16-byte aligned copy of the step's position
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    split = []
+    for _ in range(reps):
+        flush.zero_()
+        ev[0].record(stream)
+        ds4x.indexer_score(q[i:i + 1], w[i:i + 1], k, p_last, wl.ratio, scores=sc, S=S, stream=stream)
+        ev[1].record(stream)
+        ds4x.topk(sc, p_last, S, wl.ratio, wl.k_top, indices=idx[i:i + 1], workspace=tws, stream=stream)
+        ev[2].record(stream)
+        ds4x.index_and_attend(q[i:i + 1], w[i:i + 1], k, p_last, qa[i:i + 1], kv, wl.ratio, wl.k_top, S=S,
+                              scale=wl.scale, indices=idx[i:i + 1], out=out[i:i + 1], lse=lse[i:i + 1],
+                              workspace=ws, stream=stream)
+        ev[3].record(stream)
+        torch.cuda.synchronize()
+        split.append([ev[j].elapsed_time(ev[j + 1]) * 1e3 for j in range(3)])
+    sp = np.median(np.array(split), axis=0)
+    return {
+        "workload": f"decode_1m: {n_steps} steps of 1 query token at positions {wl.pos0}..{wl.pos0 + n_steps - 1}, "
+                    f"ratio {wl.ratio}, {S0} resident rows + {s_final - S0} appended (capacity {cap}); "
+                    f"k[{cap},{wl.D}] fp16, kv[{cap},{wl.Dkv}] {wl.kv_dtype}; top-{wl.k_top}",
+        "value": n_steps / (ms / 1e3), "unit": "decode tokens/s", "us_per_step": 1e3 * ms / n_steps,
+        "graph_value": None if graph_ms is None else n_steps / (graph_ms / 1e3),
+        "graph_us_per_step": None if graph_ms is None else 1e3 * graph_ms / n_steps,
+        "steps": n_steps, "appended_rows": int(s_final - S0), "gpu_launches_per_call": int(launches),
+        "l2": "flushed before every timed call; within a call the steps re-read k from L2 as a decode does",
+        "one_step_us": {"score": float(sp[0]), "topk": float(sp[1]), "fused_step": float(sp[2])},
+    }
+
+
 # ------------------------------------------------------------------------------- GPU arm
 def main():
     args = parse()
@@ -396,6 +504,10 @@ def main():
         "attn_gather_gbs": alg["attn_gather_bytes"] / (st_mean[2] / 1e3) / 1e9,
     }
 
+    dec = None
+    if rank == 0 and not args.no_decode and wl.name != "decode_1m":
+        dec = measure_decode(ds4x, torch, dev, stream, args.seed)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         v, cores, desc = cpu_baseline(wl, inp)
@@ -412,7 +524,7 @@ def main():
             "roofline": roof, "stage_ms": stages, "stage_rates": others,
             "staged_ms_per_step": float(stage_ms.sum(axis=1).mean()),
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
-            "clocks": sampler.summary(),
+            "clocks": sampler.summary(), "decode": dec,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

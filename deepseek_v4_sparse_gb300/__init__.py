@@ -7,8 +7,9 @@ libds4x.so has not been built (``python -c "import __graft_entry__ as g; g.build
 every call raises.
 
 Entry points (same names as the C ABI, without the ``ds4x_`` prefix):
-  indexer_score, topk, sparse_attn, index_and_attend, workspace_bytes,
-  topk_workspace_bytes, device_status, selftest_bounded_wait, last_launch_count
+  indexer_score, topk, sparse_attn, index_and_attend, workspace_bytes, decode,
+  decode_workspace_bytes, topk_workspace_bytes, topk_static_scratch, device_status,
+  selftest_bounded_wait, last_launch_count
 """
 from __future__ import annotations
 
@@ -27,7 +28,7 @@ EXPORTS = (
     "ds4x_indexer_score", "ds4x_topk", "ds4x_topk_workspace_bytes", "ds4x_sparse_attn",
     "ds4x_index_and_attend", "ds4x_workspace_bytes", "ds4x_status_string",
     "ds4x_last_launch_count", "ds4x_device_status", "ds4x_selftest_bounded_wait",
-    "ds4x_topk_static_scratch",
+    "ds4x_topk_static_scratch", "ds4x_decode", "ds4x_decode_workspace_bytes",
 )
 
 _lock = threading.Lock()
@@ -59,12 +60,16 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                               i32, i32, i32, f32, P, P, P, P, sz, P]
         lib.ds4x_workspace_bytes.argtypes = [i32, i32, i32]
         lib.ds4x_workspace_bytes.restype = sz
+        lib.ds4x_decode.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                    i32, i32, f32, P, P, P, P, P, sz, ctypes.POINTER(i32), P]
+        lib.ds4x_decode_workspace_bytes.argtypes = [i32, i32]
+        lib.ds4x_decode_workspace_bytes.restype = sz
         lib.ds4x_status_string.argtypes = [ctypes.c_int]
         lib.ds4x_status_string.restype = ctypes.c_char_p
         lib.ds4x_last_launch_count.argtypes = []
         lib.ds4x_device_status.argtypes = [P, ctypes.c_int]
         lib.ds4x_selftest_bounded_wait.argtypes = [i64, P]
-        for f in ("ds4x_indexer_score", "ds4x_topk", "ds4x_sparse_attn", "ds4x_index_and_attend",
+        for f in ("ds4x_indexer_score", "ds4x_topk", "ds4x_sparse_attn", "ds4x_index_and_attend", "ds4x_decode",
                   "ds4x_last_launch_count", "ds4x_device_status", "ds4x_selftest_bounded_wait"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
@@ -221,6 +226,45 @@ def index_and_attend(q, w, k, positions, q_attn, kv, ratio: int, k_top: int = 51
                                       _ptr(out), _ptr(lse), _ptr(workspace), wbytes, _stream(stream))
     _check("ds4x_index_and_attend", rc)
     return indices, out, lse
+
+
+def decode_workspace_bytes(capacity: int, k_top: int = 512) -> int:
+    return int(load().ds4x_decode_workspace_bytes(capacity, k_top))
+
+
+def decode(q, w, q_attn, k, kv, S0: int, pos0: int, ratio: int, k_new=None, kv_new=None, k_top: int = 512,
+           scale: float | None = None, positions=None, indices=None, out=None, lse=None, workspace=None,
+           want_lse: bool = True, stream=None):
+    """n_steps = q.shape[0] decode steps at positions pos0, pos0+1, ...; rows of k_new / kv_new are
+    appended to k / kv (capacity = k.shape[0]) as the positions complete them.
+    Returns (indices, out, lse, positions, S_final)."""
+    torch = _torch()
+    dt = _kv_dtype(kv)
+    n_steps, H, D = q.shape
+    _, Hq, Dkv = q_attn.shape
+    capacity = k.shape[0]
+    if kv.shape[0] != capacity:
+        raise ValueError("k and kv must have the same capacity")
+    n_new = 0 if k_new is None else k_new.shape[0]
+    scale = 1.0 / math.sqrt(Dkv) if scale is None else scale
+    dev = q.device
+    if positions is None:
+        positions = torch.empty((n_steps,), dtype=torch.int32, device=dev)
+    if indices is None:
+        indices = torch.empty((n_steps, k_top), dtype=torch.int32, device=dev)
+    if out is None:
+        out = torch.empty_like(q_attn)
+    if lse is None and want_lse:
+        lse = torch.empty((n_steps, Hq), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty((max(decode_workspace_bytes(capacity, k_top), 16),), dtype=torch.uint8, device=dev)
+    s_final = ctypes.c_int32(0)
+    rc = load().ds4x_decode(_ptr(q), _ptr(w), _ptr(q_attn), _ptr(k), _ptr(kv), dt, capacity, S0, _ptr(k_new),
+                            _ptr(kv_new), n_new, pos0, n_steps, H, D, ratio, k_top, Hq, Dkv, scale, _ptr(positions),
+                            _ptr(indices), _ptr(out), _ptr(lse), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), ctypes.byref(s_final), _stream(stream))
+    _check("ds4x_decode", rc)
+    return indices, out, lse, positions, int(s_final.value)
 
 
 def device_status(stream=None, clear: bool = True) -> int:

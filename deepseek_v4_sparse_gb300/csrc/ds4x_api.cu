@@ -30,12 +30,18 @@ int current_device() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
+void call_begin() { t_launches = 0; }
+int call_end(int rc) {
+  if (rc == DS4X_OK) t_last_launches = t_launches;
+  return rc;
+}
+
+namespace {
 struct CallScope {  // launch accounting for ds4x_last_launch_count()
-  CallScope() { t_launches = 0; }
-  int done(int rc) {
-    if (rc == DS4X_OK) t_last_launches = t_launches;
-    return rc;
-  }
+  CallScope() { call_begin(); }
+  int done(int rc) { return call_end(rc); }
 };
 }  // namespace
 
@@ -59,6 +65,45 @@ int* device_status_ptr() {
 }
 
 void count_launch(int n) { t_launches += n; }
+
+namespace {
+size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
+}  // namespace
+
+// Workspace of the fused path: [scores T x S fp32 | top-k scratch | split-attention scratch].
+size_t fused_workspace_bytes(int T, int S, int k_top) {
+  if (T <= 0 || S <= 0 || k_top <= 0) return 0;
+  return round256((size_t)T * (size_t)S * sizeof(float)) + round256(topk_workspace_bytes(T, S, k_top)) +
+         attn_partial_bytes(T, k_top);
+}
+
+int run_index_and_attend(const void* q, const void* w, const void* k, const int32_t* positions, const void* q_attn,
+                         const void* kv, int bf16, int T, int H, int D, int S, int ratio, int k_top, float scale,
+                         int32_t* indices, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                         cudaStream_t st) {
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t score_bytes = round256((size_t)T * (size_t)S * sizeof(float));
+  const size_t topk_bytes = S > 0 ? round256(topk_workspace_bytes(T, S, k_top)) : 0;
+  int rc = DS4X_OK;
+  if (S > 0) {
+    // scores only for tokens that the shortcut does not cover; masked rows are never read
+    ScoreArgs sa{q, w, k, positions, reinterpret_cast<float*>(ws), (int64_t)S, T, H, D, S, ratio, k_top, 0};
+    rc = launch_score(sa, st);
+  }
+  if (rc == DS4X_OK) {
+    TopkArgs ta{reinterpret_cast<float*>(ws), (int64_t)(S > 0 ? S : 1), positions, T, S, ratio, k_top, indices,
+                nullptr, S > 0 ? ws + score_bytes : nullptr, S > 0 ? workspace_bytes - score_bytes : 0};
+    rc = launch_topk(ta, st);
+  }
+  if (rc == DS4X_OK) {
+    const size_t used = score_bytes + topk_bytes;
+    const bool room = S > 0 && workspace_bytes > used;
+    AttnArgs aa{q_attn, kv, bf16, indices, T, 64, 512, S, k_top, scale, out, lse,
+                room ? ws + used : nullptr, room ? workspace_bytes - used : 0};
+    rc = launch_sparse_attn(aa, st);
+  }
+  return rc;
+}
 
 namespace {
 // One thread waits on a barrier that nothing completes; the bounded wait gives up.
@@ -98,11 +143,7 @@ size_t ds4x_topk_workspace_bytes(int32_t T, int32_t S, int32_t k_top) {
   return topk_workspace_bytes(T, S, k_top);
 }
 
-size_t ds4x_workspace_bytes(int32_t T, int32_t S, int32_t k_top) {
-  if (T <= 0 || S <= 0 || k_top <= 0) return 0;
-  const size_t scores = ((size_t)T * (size_t)S * sizeof(float) + 255) & ~size_t(255);
-  return scores + topk_workspace_bytes(T, S, k_top);
-}
+size_t ds4x_workspace_bytes(int32_t T, int32_t S, int32_t k_top) { return fused_workspace_bytes(T, S, k_top); }
 
 int ds4x_indexer_score(const void* q, const void* w, const void* k, const int32_t* positions, int32_t T,
                        int32_t H, int32_t D, int32_t S, int32_t ratio, float* scores, int64_t ld_scores,
@@ -145,7 +186,7 @@ int ds4x_sparse_attn(const void* q_attn, const void* kv, ds4x_dtype dtype, const
       (lse && !aligned16(lse)))
     return DS4X_ERR_INVALID;
   if (!attn_shape_supported(Hq, Dkv)) return DS4X_ERR_UNSUPPORTED;
-  AttnArgs a{q_attn, kv, dtype == DS4X_BF16 ? 1 : 0, indices, T, Hq, Dkv, S, k_top, scale, out, lse};
+  AttnArgs a{q_attn, kv, dtype == DS4X_BF16 ? 1 : 0, indices, T, Hq, Dkv, S, k_top, scale, out, lse, nullptr, 0};
   return scope.done(launch_sparse_attn(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -168,26 +209,9 @@ int ds4x_index_and_attend(const void* q, const void* w, const void* k, const int
   if (!score_shape_supported(H, D) || !attn_shape_supported(Hq, Dkv)) return DS4X_ERR_UNSUPPORTED;
   const size_t need = ds4x_workspace_bytes(T, S, k_top);
   if (S > 0 && (workspace == nullptr || workspace_bytes < need)) return DS4X_ERR_WORKSPACE;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  float* scores = static_cast<float*>(workspace);
-  const size_t score_bytes = ((size_t)T * (size_t)S * sizeof(float) + 255) & ~size_t(255);
-  int rc = DS4X_OK;
-  if (S > 0) {
-    // scores only for tokens that the shortcut does not cover; masked rows are never read
-    ScoreArgs sa{q, w, k, positions, scores, (int64_t)S, T, H, D, S, ratio, k_top, 0};
-    rc = launch_score(sa, st);
-  }
-  if (rc == DS4X_OK) {
-    TopkArgs ta{scores, (int64_t)(S > 0 ? S : 1), positions, T, S, ratio, k_top, indices, nullptr,
-                S > 0 ? static_cast<uint8_t*>(workspace) + score_bytes : nullptr,
-                S > 0 ? workspace_bytes - score_bytes : 0};
-    rc = launch_topk(ta, st);
-  }
-  if (rc == DS4X_OK) {
-    AttnArgs aa{q_attn, kv, kv_dtype == DS4X_BF16 ? 1 : 0, indices, T, Hq, Dkv, S, k_top, scale, out, lse};
-    rc = launch_sparse_attn(aa, st);
-  }
-  return scope.done(rc);
+  return scope.done(run_index_and_attend(q, w, k, positions, q_attn, kv, kv_dtype == DS4X_BF16 ? 1 : 0, T, H, D, S,
+                                         ratio, k_top, scale, indices, out, lse, workspace, workspace_bytes,
+                                         static_cast<cudaStream_t>(stream)));
 }
 
 int ds4x_device_status(void* stream, int clear) {

@@ -12,6 +12,10 @@ namespace ds4x {
 int device_sm_count();
 // Launches issued by the current call (reset by the ABI layer at entry).
 void count_launch(int n = 1);
+// Launch accounting of one C-ABI call: call_begin() at entry, call_end(rc) on return (records the
+// count for ds4x_last_launch_count when rc == DS4X_OK and passes rc through).
+void call_begin();
+int call_end(int rc);
 // Device address of the library's status word on the current device (bounded waits that give
 // up record DS4X_ERR_TIMEOUT there).
 int* device_status_ptr();
@@ -52,8 +56,20 @@ struct AttnArgs {
   float scale;
   void* out;
   float* lse;
+  void* partial;         // scratch for the split mode (NULL: every token on one CTA)
+  size_t partial_bytes;  // used only when >= attn_partial_bytes(T, k_top)
 };
 int launch_sparse_attn(const AttnArgs& a, cudaStream_t stream);
 bool attn_shape_supported(int Hq, int Dkv);
+// Scratch the split mode wants for T tokens on the current device (0: no split at this T).
+size_t attn_partial_bytes(int T, int k_top);
+
+// The fused path (score -> top-k -> attention, Hq = 64, Dkv = 512) on validated arguments, and
+// the workspace it needs: [scores T x S fp32 | top-k scratch | split-attention scratch].
+size_t fused_workspace_bytes(int T, int S, int k_top);
+int run_index_and_attend(const void* q, const void* w, const void* k, const int32_t* positions, const void* q_attn,
+                         const void* kv, int bf16, int T, int H, int D, int S, int ratio, int k_top, float scale,
+                         int32_t* indices, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                         cudaStream_t st);
 
 }  // namespace ds4x

@@ -70,7 +70,10 @@ struct Params {
   uint16_t* out;
   float* lse;
   int* status;
+  float* part_o;   // split mode: per item, sum_j 2^(x_j - m) kv_j  [items, 64, 512] fp32 (unnormalized)
+  float* part_ml;  // split mode: per item, m [64] then l [64] (m in log2 units of the scaled logits)
   int T, S, k_top, nchunks;
+  int nsplit, cps, items;  // a token's chunks are spread over nsplit items of cps chunks each
   float scale_log2;
 };
 
@@ -208,6 +211,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nch = p.nchunks;
+  // work item it: token it / nsplit, chunks [c0, c1) of it (all of them when nsplit = 1)
+  auto item_of = [&](int it, int& t, int& c0, int& c1) {
+    t = it / p.nsplit;
+    c0 = (it - t * p.nsplit) * p.cps;
+    c1 = min(nch, c0 + p.cps);
+  };
+  // the chunk after (t, c) in this CTA's sequence: the next chunk of the item, else the first
+  // chunk of the CTA's next item (token p.T when there is none)
+  auto next_chunk = [&](int it, int t, int c, int c1, int& nt, int& nc) {
+    if (c + 1 < c1) {
+      nt = t;
+      nc = c + 1;
+    } else {
+      const int nit = it + (int)gridDim.x;
+      int d1;
+      item_of(nit, nt, nc, d1);
+      if (nit >= p.items) nt = p.T;
+    }
+  };
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPairs; ++i) {
       mbar_init(&qfull[i], 1);
@@ -254,12 +276,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         idx[i] = (t < p.T && j < p.k_top) ? __ldg(p.indices + (int64_t)t * p.k_top + j) : -1;
       }
     };
-    uint32_t gc = 0, tok_i = 0;
+    uint32_t gc = 0;
     bool ok = true;
     int32_t idx[4];
-    load_idx(blockIdx.x, 0, idx);
-    for (int t = blockIdx.x; t < p.T && ok; t += gridDim.x, ++tok_i) {
-      for (int c = 0; c < nch && ok; ++c, ++gc) {
+    {
+      int t0, a0, a1;
+      item_of(blockIdx.x, t0, a0, a1);
+      load_idx(blockIdx.x < p.items ? t0 : p.T, a0, idx);
+    }
+    for (int it = blockIdx.x; it < p.items && ok; it += gridDim.x) {
+      int t, c0, c1;
+      item_of(it, t, c0, c1);
+      for (int c = c0; c < c1 && ok; ++c, ++gc) {
         const char* src[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -268,8 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                        : nullptr;
         // the next chunk's indices are on their way while this chunk is issued
         {
-          const int nt = (c + 1 < nch) ? t : t + (int)gridDim.x;
-          load_idx(nt, (c + 1 < nch) ? c + 1 : 0, idx);
+          int nt, nc;
+          next_chunk(it, t, c, c1, nt, nc);
+          load_idx(nt, nc, idx);
         }
         const int b = gc & 1;
         uint8_t* buf = skv + b * kBufBytes;
@@ -295,12 +324,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     const uint32_t q_addr = smem_u32(sq);
     const uint32_t kv_addr = smem_u32(skv);
-    for (int t = blockIdx.x; t < p.T && ok; t += gridDim.x, ++tok_i) {
-      for (int c = 0; c < nch; ++c, ++gc) {
+    for (int it = blockIdx.x; it < p.items && ok; it += gridDim.x, ++tok_i) {
+      int t, c0, c1;
+      item_of(it, t, c0, c1);
+      for (int c = c0; c < c1; ++c, ++gc) {
         const int sb = gc & 1, b = gc & 1;
         if (!mbar_wait(&sempty[sb], ((gc >> 1) & 1) ^ 1, p.status, 31)) { ok = false; break; }
         for (int pr = 0; pr < kPairs; ++pr) {
-          if (c == 0 && !mbar_wait(&qfull[pr], tok_i & 1, p.status, 30)) { ok = false; break; }
+          if (c == c0 && !mbar_wait(&qfull[pr], tok_i & 1, p.status, 30)) { ok = false; break; }
           if (!mbar_wait(&kvfull[b * kPairs + pr], (gc >> 1) & 1, p.status, 32)) { ok = false; break; }
           fence_proxy_async();  // gathered rows -> visible to the tensor core
           tc_fence_after();
@@ -314,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_mma_f16_elect(tmem + sb * kHq, a, bd, kIdescS, (kb | kk) != 0);
             }
           }
-          if (c == nch - 1) tc_commit_elect(&qempty[pr]);  // the next token's q may replace this pair
+          if (c == c1 - 1) tc_commit_elect(&qempty[pr]);  // the next item's q may replace this pair
         }
         if (!ok) break;
         tc_commit_elect(&sfull[sb]);
@@ -326,15 +357,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     const uint32_t kv_addr = smem_u32(skv);
     const uint32_t p_addr = smem_u32(sp);
-    for (int t = blockIdx.x; t < p.T && ok; t += gridDim.x, ++tok_i) {
-      for (int c = 0; c < nch; ++c, ++gc) {
+    for (int it = blockIdx.x; it < p.items && ok; it += gridDim.x, ++tok_i) {
+      int t, c0, c1;
+      item_of(it, t, c0, c1);
+      for (int c = c0; c < c1; ++c, ++gc) {
         const int pb = gc & 1, b = gc & 1;
         if (!mbar_wait(&pfull[pb], (gc >> 1) & 1, p.status, 33)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int db = 0; db < kPairs; ++db) {
-          // a token's first product overwrites O^T: the previous token's output must have read it
-          if (c == 0) {
+          // an item's first product overwrites O^T: the previous item's output must have read it
+          if (c == c0) {
             if (!mbar_wait(&oempty[db], (tok_i & 1) ^ 1, p.status, 34)) { ok = false; break; }
             tc_fence_after();
           }
@@ -342,10 +375,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int ks = 0; ks < kRows / 16; ++ks) {
             const uint64_t a = desc_sw128(kv_addr + b * kBufBytes + (2 * db) * kSlotBytes + ks * 2048, kSlotBytes, 1024);
             const uint64_t bd = desc_sw128(p_addr + pb * kPBytes + ks * 32, 16, 1024);
-            tc_mma_f16_elect(tmem + kColO + db * kHq, a, bd, kIdescO, (c > 0 || ks > 0));
+            tc_mma_f16_elect(tmem + kColO + db * kHq, a, bd, kIdescO, (c > c0 || ks > 0));
           }
           tc_commit_elect(&kvempty[b * kPairs + db]);  // this 128-dim slice of the chunk is free
-          if (c == nch - 1) tc_commit_elect(&ofull[db]);
+          if (c == c1 - 1) tc_commit_elect(&ofull[db]);
         }
         if (!ok) break;
         tc_commit_elect(&pempty[pb]);
@@ -370,15 +403,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       i1 = (t < p.T && ci < nch && j1 < p.k_top) ? __ldg(p.indices + (int64_t)t * p.k_top + j1) : -1;
     };
     int32_t ni0, ni1;
-    load_valid(blockIdx.x, 0, ni0, ni1);
-    for (int t = blockIdx.x; t < p.T && ok; t += gridDim.x, ++tok_i) {
+    {
+      int t0, a0, a1;
+      item_of(blockIdx.x, t0, a0, a1);
+      load_valid(blockIdx.x < p.items ? t0 : p.T, a0, ni0, ni1);
+    }
+    for (int it = blockIdx.x; it < p.items && ok; it += gridDim.x, ++tok_i) {
+      int t, c0, c1;
+      item_of(it, t, c0, c1);
       float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;  // running max (scaled, log2) and sum
-      for (int ci = 0; ci < nch; ++ci, ++gc) {
+      for (int ci = c0; ci < c1; ++ci, ++gc) {
         const uint32_t v0 = __ballot_sync(0xffffffffu, ni0 >= 0 && ni0 < p.S) >> (2 * e);
         const uint32_t v1 = __ballot_sync(0xffffffffu, ni1 >= 0 && ni1 < p.S) >> (2 * e);
         {
-          const int nt = (ci + 1 < nch) ? t : t + (int)gridDim.x;
-          load_valid(nt, (ci + 1 < nch) ? ci + 1 : 0, ni0, ni1);
+          int nt, nc;
+          next_chunk(it, t, ci, c1, nt, nc);
+          load_valid(nt, nc, ni0, ni1);
         }
         const int sb = gc & 1;
         ok = named_and(kSoftBar, kGroupThreads, mbar_wait(&sfull[sb], (gc >> 1) & 1, p.status, 40));
@@ -475,12 +515,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&pfull[pb]);
-        if (ci == nch - 1) {
+        if (ci == c1 - 1) {
           lA += __shfl_xor_sync(0xffffffffu, lA, 1);
           lB += __shfl_xor_sync(0xffffffffu, lB, 1);
           lA += __shfl_xor_sync(0xffffffffu, lA, 2);
           lB += __shfl_xor_sync(0xffffffffu, lB, 2);
-          // the slot of this token's parity was last read by the output of token tok_i - 2
+          // the slot of this item's parity was last read by the output of item tok_i - 2
           ok = named_and(kSoftBar, kGroupThreads,
                          mbar_wait(&lfree[tok_i & 1], ((tok_i >> 1) & 1) ^ 1, p.status, 45));
           if (!ok) break;
@@ -492,6 +532,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             row[hB] = lB;
             row[kHq + hB] = mB;
             row[2 * kHq + hB] = lB > 0.f ? 1.f / lB : 0.f;
+            if (p.nsplit > 1) {
+              float* ml = p.part_ml + (int64_t)it * 2 * kHq;
+              ml[hA] = mA;
+              ml[hB] = mB;
+              ml[kHq + hA] = lA;
+              ml[kHq + hB] = lB;
+            }
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&lready[tok_i & 1]);
@@ -507,12 +554,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t tok_i = 0;
     bool ok = true;
     const bool odd = lane & 1;
-    for (int t = blockIdx.x; t < p.T && ok; t += gridDim.x, ++tok_i) {
+    for (int it = blockIdx.x; it < p.items && ok; it += gridDim.x, ++tok_i) {
+      const int t = it / p.nsplit;
       const int par = tok_i & 1;
       ok = named_and(kEpiBar, kGroupThreads, mbar_wait(&lready[par], (tok_i >> 1) & 1, p.status, 43));
       if (!ok) break;
       const float* lrow = lm + par * 3 * kHq;
-      if (quad == 0) {
+      if (quad == 0 && p.nsplit == 1) {
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           const int hh = lane + 32 * k;
@@ -541,6 +589,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&oempty[db]);
+        if (p.nsplit > 1) {  // split item: unnormalized fp32 sums, merged by the combine kernel
+          float* po = p.part_o + (int64_t)it * kHq * kDkv + db * 128 + quad * 32 + lane;
+#pragma unroll
+          for (int h = 0; h < kHq; ++h) po[h * kDkv] = v[h];
+          continue;
+        }
         const int d_even = db * 128 + quad * 32 + (lane & ~1);
 #pragma unroll
         for (int h0 = 0; h0 < kHq; h0 += 2) {
@@ -561,9 +615,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------------- q loader
     if (lane == 0) {
       uint32_t tok_i = 0;
-      for (int t = blockIdx.x; t < p.T; t += gridDim.x, ++tok_i) {
-        const int tn = t + (int)gridDim.x;  // the next token's q (64 KB, contiguous) moves to L2 now
-        if (tn < p.T) prefetch_l2(p.q + (int64_t)tn * kHq * kDkv, kQBytes);
+      for (int it = blockIdx.x; it < p.items; it += gridDim.x, ++tok_i) {
+        const int t = it / p.nsplit;
+        const int nit = it + (int)gridDim.x;  // the next item's q (64 KB, contiguous) moves to L2 now
+        if (nit < p.items) prefetch_l2(p.q + (int64_t)(nit / p.nsplit) * kHq * kDkv, kQBytes);
         bool ok = true;
         for (int pr = 0; pr < kPairs; ++pr) {
           if (!mbar_wait(&qempty[pr], (tok_i & 1) ^ 1, p.status, 20)) { ok = false; break; }
@@ -585,6 +640,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// Merge of a token's split items (one block per (token, head), 4 dims a thread): item i holds
+// O_i = sum_j 2^(x_j - m_i) kv_j and l_i = sum_j 2^(x_j - m_i) over its rows, so
+//   out = sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i,  M = max_i m_i,  lse = ln 2 (M + log2 L).
+template <bool kBf16>
+__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_o,
+                                                      const float* __restrict__ part_ml, int nsplit,
+                                                      uint16_t* __restrict__ out, float* __restrict__ lse) {
+  const int t = blockIdx.x / kHq, h = blockIdx.x - t * kHq;
+  const float* ml = part_ml + (int64_t)t * nsplit * 2 * kHq;
+  float mx = -INFINITY;
+  for (int i = 0; i < nsplit; ++i) mx = fmaxf(mx, ml[i * 2 * kHq + h]);
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = 0; i < nsplit; ++i) {
+    const float mi = ml[i * 2 * kHq + h];
+    const float wgt = (mi == -INFINITY) ? 0.f : exp2f(mi - mx);
+    L += wgt * ml[i * 2 * kHq + kHq + h];
+    const float4 o = *reinterpret_cast<const float4*>(part_o + (((int64_t)t * nsplit + i) * kHq + h) * kDkv +
+                                                      4 * threadIdx.x);
+    acc.x += wgt * o.x;
+    acc.y += wgt * o.y;
+    acc.z += wgt * o.z;
+    acc.w += wgt * o.w;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  float r0, r1;
+  const uint32_t lo = pack2<kBf16>(acc.x * inv, acc.y * inv, r0, r1);
+  const uint32_t hi = pack2<kBf16>(acc.z * inv, acc.w * inv, r0, r1);
+  *reinterpret_cast<uint2*>(out + ((int64_t)t * kHq + h) * kDkv + 4 * threadIdx.x) = make_uint2(lo, hi);
+  if (threadIdx.x == 0 && lse)
+    lse[(int64_t)t * kHq + h] = L > 0.f ? (mx + log2f(L)) * 0.69314718055994531f : -INFINITY;
+}
+
+// Split plan: when the tokens fill less than half of the SMs, a token's chunks are spread over
+// up to sms / T items (at least one chunk each) and merged by combine_kernel.
+void split_plan(int T, int k_top, int sms, int& nsplit, int& cps) {
+  const int nch = (k_top + kRows - 1) / kRows;
+  nsplit = 1;
+  cps = nch;
+  if (T <= 0 || 2 * T > sms || nch < 2) return;
+  int want = sms / T;
+  if (want > nch) want = nch;
+  cps = (nch + want - 1) / want;
+  nsplit = (nch + cps - 1) / cps;
+}
+
+size_t partial_bytes_for(int T, int nsplit) {
+  if (nsplit <= 1) return 0;
+  return (size_t)T * nsplit * ((size_t)kHq * kDkv * 4 + 2 * kHq * 4);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -641,15 +747,44 @@ int launch_impl(const AttnArgs& a, cudaStream_t stream) {
   p.nchunks = (a.k_top + kRows - 1) / kRows;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   const int sms = device_sm_count();
-  const int grid = a.T < sms ? a.T : sms;
+  p.nsplit = 1;
+  p.cps = p.nchunks;
+  p.part_o = nullptr;
+  p.part_ml = nullptr;
+  if (a.partial) {
+    int ns, cps;
+    split_plan(a.T, a.k_top, sms, ns, cps);
+    const size_t need = partial_bytes_for(a.T, ns);
+    if (ns > 1 && a.partial_bytes >= need) {
+      p.nsplit = ns;
+      p.cps = cps;
+      p.part_o = static_cast<float*>(a.partial);
+      p.part_ml = p.part_o + (size_t)a.T * ns * kHq * kDkv;
+    }
+  }
+  p.items = a.T * p.nsplit;
+  const int grid = p.items < sms ? p.items : sms;
   sparse_mqa_kernel<kBf16><<<grid, kThreads, kSmem, stream>>>(tq, p);
   count_launch();
-  return cudaGetLastError() == cudaSuccess ? DS4X_OK : DS4X_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return DS4X_ERR_CUDA;
+  if (p.nsplit > 1) {
+    combine_kernel<kBf16><<<a.T * kHq, kDkv / 4, 0, stream>>>(p.part_o, p.part_ml, p.nsplit,
+                                                              static_cast<uint16_t*>(a.out), a.lse);
+    count_launch();
+    if (cudaGetLastError() != cudaSuccess) return DS4X_ERR_CUDA;
+  }
+  return DS4X_OK;
 }
 
 }  // namespace
 
 bool attn_shape_supported(int Hq, int Dkv) { return Hq == kHq && Dkv == kDkv; }
+
+size_t attn_partial_bytes(int T, int k_top) {
+  int ns, cps;
+  split_plan(T, k_top, device_sm_count(), ns, cps);
+  return partial_bytes_for(T, ns);
+}
 
 int launch_sparse_attn(const AttnArgs& a, cudaStream_t stream) {
   if (a.T == 0) return DS4X_OK;

@@ -155,6 +155,11 @@ int ds4x_sparse_attn(const void* q_attn, const void* kv, ds4x_dtype dtype,
  *   Equal to ds4x_indexer_score + ds4x_topk + ds4x_sparse_attn with the same arguments;
  *   the scores live only in `workspace` (at least ds4x_workspace_bytes(T, S, k_top)).
  *   q, w, k fp16 as in ds4x_indexer_score; q_attn, kv, out of kv_dtype.
+ *   When the tokens fill less than half of the GPU's SMs (2T <= SM count, e.g. decode), the
+ *   attention of each token is split over several CTAs by chunks of its selected rows and the
+ *   parts are merged by their softmax statistics; out and lse then differ from the unsplit
+ *   result only by fp32 rounding order.  The workspace holds
+ *   [scores T x S fp32 | top-k scratch | split-attention scratch] (256-byte aligned parts).
  * ------------------------------------------------------------------------- */
 int ds4x_index_and_attend(const void* q, const void* w, const void* k, const int32_t* positions,
                           const void* q_attn, const void* kv, ds4x_dtype kv_dtype,
@@ -164,6 +169,37 @@ int ds4x_index_and_attend(const void* q, const void* w, const void* k, const int
                           void* workspace, size_t workspace_bytes, void* stream);
 
 size_t ds4x_workspace_bytes(int32_t T, int32_t S, int32_t k_top);
+
+/* ---------------------------------------------------------------------------
+ * ds4x_decode — the decode loop: n_steps query tokens at consecutive positions
+ * pos0, pos0+1, ..., one fused step (ds4x_index_and_attend with T = 1) each, with the
+ * compressed rows appended as the positions complete them ([K]: decode at long context;
+ * [S]: one pooled row per `ratio` positions).
+ *
+ *   Before step i (position p = pos0 + i) the loop appends, while S < floor((p+1)/ratio),
+ *   the next unused staged rows k_new[a], kv_new[a] (a = 0, 1, ...) at row S of k and kv
+ *   and increments S (stopping when the n_new staged rows or the capacity run out; the step
+ *   then sees min(S, floor((p+1)/ratio)) rows).  The step writes
+ *     positions[i] = p, indices[i, :], out[i, :, :], lse[i, :]  (lse may be NULL)
+ *   exactly as ds4x_index_and_attend would for that one token with the current S.
+ *
+ *   q [n_steps, H, D] fp16, w [n_steps, H] fp16, q_attn [n_steps, Hq, Dkv] kv_dtype
+ *   k [capacity, D] fp16 and kv [capacity, Dkv] kv_dtype: rows 0..S0-1 valid on entry,
+ *     rows S0.. are overwritten by the appends (read and written by the call)
+ *   k_new [n_new, D], kv_new [n_new, Dkv]: staged rows in append order (NULL when n_new = 0)
+ *   positions [n_steps] int32 (written), indices [n_steps, k_top] int32, out like q_attn
+ *   workspace: at least ds4x_decode_workspace_bytes(capacity, k_top) bytes
+ *   S_final (host pointer, may be NULL): receives S after the last step.
+ *   Requires pos0 >= 0, H % 8 == 0 and k_top % 4 == 0 (per-step rows stay 16-byte aligned).
+ *   The loop runs on the host and only issues kernel launches on `stream` (no synchronization,
+ *   no allocation), so a call may be captured into a CUDA graph after a first call on the device.
+ * ------------------------------------------------------------------------- */
+int ds4x_decode(const void* q, const void* w, const void* q_attn, void* k, void* kv, ds4x_dtype kv_dtype,
+                int32_t capacity, int32_t S0, const void* k_new, const void* kv_new, int32_t n_new,
+                int32_t pos0, int32_t n_steps, int32_t H, int32_t D, int32_t ratio, int32_t k_top,
+                int32_t Hq, int32_t Dkv, float scale, int32_t* positions, int32_t* indices, void* out,
+                float* lse, void* workspace, size_t workspace_bytes, int32_t* S_final, void* stream);
+size_t ds4x_decode_workspace_bytes(int32_t capacity, int32_t k_top);
 
 /* Human-readable name of a ds4x_status value (static storage, never NULL). */
 const char* ds4x_status_string(int status);

@@ -44,6 +44,8 @@ def _bind(lib):
     lib.ds4x_ref_sparse_attn.argtypes = [P, P, ctypes.c_int, P, i32, i32, i32, i32, i32, f32, P, P]
     lib.ds4x_ref_index_and_attend.argtypes = [P, P, P, P, P, P, ctypes.c_int, i32, i32, i32, i32,
                                               i32, i32, i32, i32, f32, P, P, P]
+    lib.ds4x_ref_decode.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, P, i32, i32, i32, i32, i32, i32,
+                                    i32, i32, i32, f32, P, P, P, P, P]
     lib.ds4x_ref_n_visible.argtypes = [i64, i64, i64]
     lib.ds4x_ref_n_visible.restype = i64
     lib.ds4x_ref_decode16.argtypes = [ctypes.c_uint16, ctypes.c_int]
@@ -51,7 +53,7 @@ def _bind(lib):
     lib.ds4x_ref_encode16.argtypes = [ctypes.c_double, ctypes.c_int]
     lib.ds4x_ref_encode16.restype = ctypes.c_uint16
     for f in ("ds4x_ref_indexer_score", "ds4x_ref_topk_ex", "ds4x_ref_sparse_attn",
-              "ds4x_ref_index_and_attend"):
+              "ds4x_ref_index_and_attend", "ds4x_ref_decode"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -138,6 +140,29 @@ class Oracle:
         return idx, out, lse
 
 
+    def decode(self, q, w, q_attn, k, kv, kv_dtype, S0, pos0, ratio, k_new, kv_new, k_top, scale):
+        """The decode loop on copies of k / kv (capacity = their row count).
+        Returns (indices, out bits, lse, positions, S per step, k after, kv after)."""
+        q, w, q_attn = _c(q, np.uint16), _c(w, np.uint16), _c(q_attn, np.uint16)
+        k, kv = np.array(k, dtype=np.uint16, copy=True), np.array(kv, dtype=np.uint16, copy=True)
+        n_new = 0 if k_new is None else k_new.shape[0]
+        k_new = None if k_new is None else _c(k_new, np.uint16)
+        kv_new = None if kv_new is None else _c(kv_new, np.uint16)
+        n_steps, H, D = q.shape
+        _, Hq, Dkv = q_attn.shape
+        idx = np.empty((n_steps, k_top), dtype=np.int32)
+        out = np.empty((n_steps, Hq, Dkv), dtype=np.uint16)
+        lse = np.empty((n_steps, Hq), dtype=np.float32)
+        pos = np.empty((n_steps,), dtype=np.int32)
+        s_steps = np.empty((n_steps,), dtype=np.int32)
+        rc = self.lib.ds4x_ref_decode(_ptr(q), _ptr(w), _ptr(q_attn), _ptr(k), _ptr(kv), DTYPES[kv_dtype],
+                                      k.shape[0], S0, _ptr(k_new), _ptr(kv_new), n_new, pos0, n_steps, H, D,
+                                      ratio, k_top, Hq, Dkv, scale, _ptr(pos), _ptr(idx), _ptr(out), _ptr(lse),
+                                      _ptr(s_steps))
+        assert rc == 0, rc
+        return idx, out, lse, pos, s_steps, k, kv
+
+
 def default() -> Oracle:
     """The oracle built from ds4x_oracle.c (compiled on first use)."""
     global _lib
@@ -173,3 +198,7 @@ def sparse_attn(*a, **kw):
 
 def index_and_attend(*a, **kw):
     return default().index_and_attend(*a, **kw)
+
+
+def decode(*a, **kw):
+    return default().decode(*a, **kw)

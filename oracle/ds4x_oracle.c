@@ -19,6 +19,9 @@
  *    sequential indices are built directly.
  *  - A CPU path kept only to verify accuracy: the ds4.c overview (id.news.hada.io,
  *    sections "Gambaran proyek dan filosofi desain" and "Backend").
+ *  - The decode loop: one pooled row per `ratio` positions ("How I turned one oversized
+ *    DeepSeek optimization into three merged oMLX PRs", section "The three changes that
+ *    merged"), decode at long context ("How I made DeepSeek 12x faster on a Mac Studio").
  *  - The formula (which the pages leave unstated) is this library's definition:
  *    score[t,s] = sum_h w[t,h] * ReLU(q[t,h,:] . k[s,:]), row s visible iff
  *    (s+1)*ratio <= p+1, ties to the lower row index, indices ascending, attention with
@@ -27,8 +30,10 @@
  * Parity pins (tests/test_oracle.py): brute force in numpy on tiny inputs, an int64
  * recomputation of 4*score on integer inputs, a hand-worked example
  * (tests/golden/indexer_worked_example.txt), the dominance / mask / shortcut
- * invariants of the selection, and the closed-form attention cases (zero query ->
- * mean of the rows, one row -> that row, two rows -> logistic weights).
+ * invariants of the selection, the closed-form attention cases (zero query ->
+ * mean of the rows, one row -> that row, two rows -> logistic weights), and for the
+ * decode loop the closed-form row count per step, the appended bytes and a numpy
+ * brute-force of every step on tiny inputs.
  */
 #include <math.h>
 #include <stdint.h>
@@ -324,4 +329,39 @@ int ds4x_ref_index_and_attend(const uint16_t* q, const uint16_t* w, const uint16
   }
   free(kd);
   return ds4x_ref_sparse_attn(q_attn, kv, kv_dtype, indices, T, Hq, Dkv, S, k_top, scale, out, lse);
+}
+
+/* ---- the decode loop ------------------------------------------------------------------ */
+
+/* n_steps single-token steps at positions p = pos0 + i.  Before step i, while S is below the
+ * number of rows p may see (floor((p+1)/ratio)) and a staged row and capacity are left, the
+ * next staged row (k_new[a], kv_new[a]) is copied to row S of k and kv and S grows by one.
+ * Step i is then ds4x_ref_index_and_attend for that one token with the current S; S_steps[i]
+ * records that S.  k and kv are host arrays of `capacity` rows, updated in place. */
+int ds4x_ref_decode(const uint16_t* q, const uint16_t* w, const uint16_t* q_attn, uint16_t* k,
+                    uint16_t* kv, int kv_dtype, int32_t capacity, int32_t S0,
+                    const uint16_t* k_new, const uint16_t* kv_new, int32_t n_new, int32_t pos0,
+                    int32_t n_steps, int32_t H, int32_t D, int32_t ratio, int32_t k_top,
+                    int32_t Hq, int32_t Dkv, float scale, int32_t* positions, int32_t* indices,
+                    uint16_t* out, float* lse, int32_t* S_steps) {
+  if (n_steps < 0 || capacity < 1 || S0 < 0 || S0 > capacity || n_new < 0 || ratio < 1 || pos0 < 0)
+    return -1;
+  int32_t S = S0, a = 0;
+  for (int32_t i = 0; i < n_steps; ++i) {
+    const int64_t p = (int64_t)pos0 + i;
+    positions[i] = (int32_t)p;
+    while (S < capacity && a < n_new && (int64_t)S < (p + 1) / ratio) {
+      memcpy(k + (int64_t)S * D, k_new + (int64_t)a * D, sizeof(uint16_t) * (size_t)D);
+      memcpy(kv + (int64_t)S * Dkv, kv_new + (int64_t)a * Dkv, sizeof(uint16_t) * (size_t)Dkv);
+      ++S;
+      ++a;
+    }
+    S_steps[i] = S;
+    int rc = ds4x_ref_index_and_attend(q + (int64_t)i * H * D, w + (int64_t)i * H, k, positions + i,
+                                       q_attn + (int64_t)i * Hq * Dkv, kv, kv_dtype, 1, H, D, S, ratio,
+                                       k_top, Hq, Dkv, scale, indices + (int64_t)i * k_top,
+                                       out + (int64_t)i * Hq * Dkv, lse + (int64_t)i * Hq);
+    if (rc != 0) return rc;
+  }
+  return 0;
 }

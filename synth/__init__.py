@@ -22,6 +22,7 @@ Workloads follow the shapes of the pages' prefill chunks (2048 query tokens at 8
 from __future__ import annotations
 
 import math
+import os
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -175,10 +176,32 @@ class Inputs:
     kv: np.ndarray         # [rows, Dkv] uint16 (kv dtype bits)
 
 
-def _values(seed, wl: Workload, name: str, n: int, int_range, normal_scale=1.0):
+_PARALLEL_MIN = 1 << 24
+
+
+def _normal_bits_piece(job):
+    seed, name, n, offset, dtype = job
+    return to_bits(normal(seed, name, n, offset), dtype)
+
+
+def normal_bits(seed: int, name: str, n: int, dtype: str) -> np.ndarray:
+    """to_bits(normal(seed, name, n), dtype), drawn in pieces on a thread pool when n is large
+    (numpy's array operations release the GIL); the counter-based stream makes the pieces
+    independent, so the bits equal those of the single-piece draw."""
+    workers = min(16, os.cpu_count() or 1)
+    if n < _PARALLEL_MIN or workers < 2:
+        return to_bits(normal(seed, name, n), dtype)
+    import concurrent.futures as cf
+    piece = ((n + 4 * workers - 1) // (4 * workers) + 1) & ~1     # even: whole Box-Muller pairs
+    jobs = [(seed, name, min(piece, n - a), a, dtype) for a in range(0, n, piece)]
+    with cf.ThreadPoolExecutor(workers) as ex:
+        return np.concatenate(list(ex.map(_normal_bits_piece, jobs)))
+
+
+def _bits(seed, wl: Workload, name: str, n: int, int_range, dtype: str) -> np.ndarray:
     if wl.kind == "int":
-        return uniform_int(seed, f"{wl.name}/{name}", n, *int_range).astype(np.float64)
-    return normal(seed, f"{wl.name}/{name}", n) * normal_scale
+        return to_bits(uniform_int(seed, f"{wl.name}/{name}", n, *int_range).astype(np.float64), dtype)
+    return normal_bits(seed, f"{wl.name}/{name}", n, dtype)
 
 
 def make_inputs(wl: Workload, seed: int = 0, T: int | None = None, S: int | None = None,
@@ -190,16 +213,16 @@ def make_inputs(wl: Workload, seed: int = 0, T: int | None = None, S: int | None
     pos0 = wl.pos0 if pos0 is None else pos0
     rows = (S + wl.extra_rows) if rows is None else rows
     H, D, Hq, Dkv = wl.H, wl.D, wl.Hq, wl.Dkv
-    q = to_f16_bits(_values(seed, wl, "q", T * H * D, (-3, 3))).reshape(T, H, D)
-    k = to_f16_bits(_values(seed, wl, "k", rows * D, (-3, 3))).reshape(rows, D)
+    q = _bits(seed, wl, "q", T * H * D, (-3, 3), "f16").reshape(T, H, D)
+    k = _bits(seed, wl, "k", rows * D, (-3, 3), "f16").reshape(rows, D)
     if wl.kind == "int":
         sel = uniform_int(seed, f"{wl.name}/w", T * H, 0, 2)
         w = to_f16_bits(np.array([0.25, 0.5, 1.0])[sel]).reshape(T, H)
     else:
         w = to_f16_bits(uniform01(seed, f"{wl.name}/w", T * H) / 8.0).reshape(T, H)
     kvd = wl.kv_dtype
-    q_attn = to_bits(_values(seed, wl, "q_attn", T * Hq * Dkv, (-2, 2)), kvd).reshape(T, Hq, Dkv)
-    kv = to_bits(_values(seed, wl, "kv", rows * Dkv, (-2, 2)), kvd).reshape(rows, Dkv)
+    q_attn = _bits(seed, wl, "q_attn", T * Hq * Dkv, (-2, 2), kvd).reshape(T, Hq, Dkv)
+    kv = _bits(seed, wl, "kv", rows * Dkv, (-2, 2), kvd).reshape(rows, Dkv)
     positions = (pos0 + np.arange(T, dtype=np.int64)).astype(np.int32)
     return Inputs(wl, q, w, k, positions, q_attn, kv)
 
@@ -210,8 +233,8 @@ def custom_inputs(seed: int, tag: str, T: int, H: int, D: int, rows: int, Hq: in
     "pow2" = {1/4,1/2,1}."""
     wl = Workload(tag, T=T, H=H, D=D, S=rows, ratio=1, pos0=0, kind=kind, kv_dtype=kv_dtype,
                   Hq=Hq, Dkv=Dkv)
-    q = to_f16_bits(_values(seed, wl, "q", T * H * D, (-3, 3))).reshape(T, H, D)
-    k = to_f16_bits(_values(seed, wl, "k", rows * D, (-3, 3))).reshape(rows, D)
+    q = _bits(seed, wl, "q", T * H * D, (-3, 3), "f16").reshape(T, H, D)
+    k = _bits(seed, wl, "k", rows * D, (-3, 3), "f16").reshape(rows, D)
     if w_kind == "pow2":
         sel = uniform_int(seed, f"{tag}/w", T * H, 0, 2)
         w = to_f16_bits(np.array([0.25, 0.5, 1.0])[sel]).reshape(T, H)
@@ -219,6 +242,6 @@ def custom_inputs(seed: int, tag: str, T: int, H: int, D: int, rows: int, Hq: in
         w = to_f16_bits(normal(seed, f"{tag}/w", T * H)).reshape(T, H)
     else:
         w = to_f16_bits(uniform01(seed, f"{tag}/w", T * H) / 8.0).reshape(T, H)
-    q_attn = to_bits(_values(seed, wl, "q_attn", T * Hq * Dkv, (-2, 2)), kv_dtype).reshape(T, Hq, Dkv)
-    kv = to_bits(_values(seed, wl, "kv", rows * Dkv, (-2, 2)), kv_dtype).reshape(rows, Dkv)
+    q_attn = _bits(seed, wl, "q_attn", T * Hq * Dkv, (-2, 2), kv_dtype).reshape(T, Hq, Dkv)
+    kv = _bits(seed, wl, "kv", rows * Dkv, (-2, 2), kv_dtype).reshape(rows, Dkv)
     return Inputs(wl, q, w, k, np.asarray(positions, dtype=np.int32), q_attn, kv)

@@ -14,7 +14,9 @@ Independent facts used:
   * brute-force ranking with Python's sorted() on tiny inputs;
   * the selection invariants (dominance, mask, count, ascending order, shortcut);
   * closed-form attention cases (zero query, single row, two rows) and a textbook
-    float64 numpy softmax-attention.
+    float64 numpy softmax-attention;
+  * for the decode loop: the closed-form row count of every step, the appended bytes, and a
+    numpy brute-force (definition score, sorted() ranking, textbook attention) of each step.
 """
 from __future__ import annotations
 
@@ -353,10 +355,79 @@ def check_index_and_attend_composes(o):
     assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
 
 
+def decode_rows_closed_form(S0, capacity, n_new, pos0, ratio, n_steps):
+    """Rows present at each decode step: the visible count floor((p+1)/ratio), never below S0,
+    capped by the staged rows and the capacity."""
+    return [min(S0 + n_new, capacity, max(S0, (pos0 + i + 1) // ratio)) for i in range(n_steps)]
+
+
+def _tiny_decode_case(seed=7):
+    rng = np.random.default_rng(seed)
+    capacity, S0, n_new, H, D, Hq, Dkv = 40, 30, 3, 4, 16, 4, 32
+    k = _f16(rng.standard_normal((capacity, D)))
+    kv = synth.to_bf16_bits(rng.standard_normal((capacity, Dkv)))
+    k[S0:] = 0
+    kv[S0:] = 0
+    k_new = _f16(rng.standard_normal((n_new, D)))
+    kv_new = synth.to_bf16_bits(rng.standard_normal((n_new, Dkv)))
+    n_steps = 10
+    q = _f16(rng.standard_normal((n_steps, H, D)))
+    w = _f16(rng.uniform(0.0, 1.0, (n_steps, H)) / 8)
+    qa = synth.to_bf16_bits(rng.standard_normal((n_steps, Hq, Dkv)))
+    return dict(k=k, kv=kv, k_new=k_new, kv_new=kv_new, q=q, w=w, qa=qa, S0=S0, pos0=59, ratio=2,
+                k_top=8, n_steps=n_steps, capacity=capacity, n_new=n_new)
+
+
+def check_decode_schedule(o):
+    c = _tiny_decode_case()
+    idx, out, lse, pos, s_steps, k_after, kv_after = o.decode(
+        c["q"], c["w"], c["qa"], c["k"], c["kv"], "bf16", c["S0"], c["pos0"], c["ratio"], c["k_new"],
+        c["kv_new"], c["k_top"], 0.25)
+    assert list(pos) == [c["pos0"] + i for i in range(c["n_steps"])]
+    want = decode_rows_closed_form(c["S0"], c["capacity"], c["n_new"], c["pos0"], c["ratio"], c["n_steps"])
+    assert list(s_steps) == want, (list(s_steps), want)
+    # appended rows carry the staged bytes, in order; rows before S0 and after are untouched
+    S = int(s_steps[-1])
+    assert np.array_equal(k_after[c["S0"]:S], c["k_new"][:S - c["S0"]])
+    assert np.array_equal(kv_after[c["S0"]:S], c["kv_new"][:S - c["S0"]])
+    assert np.array_equal(k_after[:c["S0"]], c["k"][:c["S0"]]) and not k_after[S:].any()
+    # the 1M-context decode: 63 rows appended over 256 steps from position 1048575
+    assert decode_rows_closed_form(262144, 262208, 64, 1048575, 4, 256)[-1] - 262144 == 63
+
+
+def check_decode_steps_brute_force(o):
+    c = _tiny_decode_case()
+    scale = 0.25
+    idx, out, lse, pos, s_steps, k_after, _ = o.decode(
+        c["q"], c["w"], c["qa"], c["k"], c["kv"], "bf16", c["S0"], c["pos0"], c["ratio"], c["k_new"],
+        c["kv_new"], c["k_top"], scale)
+    rows_k = np.concatenate([c["k"][:c["S0"]], c["k_new"]])
+    rows_kv = np.concatenate([c["kv"][:c["S0"]], c["kv_new"]])
+    kf, kvf = _f16_val(rows_k), _bits_val(rows_kv, "bf16")
+    for i in range(c["n_steps"]):
+        p = c["pos0"] + i
+        S = min(c["S0"] + c["n_new"], max(c["S0"], (p + 1) // c["ratio"]))
+        n = min(S, (p + 1) // c["ratio"])
+        qf, wf = _f16_val(c["q"][i]), _f16_val(c["w"][i])
+        dots = qf @ kf[:n].T                                  # [H, n]
+        score = (wf[:, None] * np.maximum(dots, 0.0)).sum(axis=0).astype(np.float32)
+        ranked = sorted(range(n), key=lambda s_: (-float(score[s_]), s_))[:c["k_top"]]
+        sel = sorted(ranked) + [-1] * (c["k_top"] - min(n, c["k_top"]))
+        assert list(idx[i]) == sel, (i, list(idx[i]), sel)
+        V = kvf[sorted(ranked)]
+        logits = scale * _bits_val(c["qa"][i], "bf16") @ V.T
+        m = logits.max(axis=1, keepdims=True)
+        pr = np.exp(logits - m)
+        ref = (pr / pr.sum(axis=1, keepdims=True)) @ V
+        assert np.allclose(_bits_val(out[i], "bf16"), ref, rtol=2 ** -8, atol=1e-6)
+        assert np.allclose(lse[i], m[:, 0] + np.log(pr.sum(axis=1)), rtol=1e-6, atol=1e-6)
+
+
 ALL_CHECKS = [
     check_f16_decode_exhaustive, check_bf16_decode_exhaustive, check_encode_rne,
     check_visibility, check_golden_example, check_scores_int64_closed_form,
     check_scores_float_vs_numpy, check_topk_brute_force, check_topk_invariants,
     check_shortcut, check_attn_zero_query_is_mean, check_attn_single_row,
     check_attn_two_rows_logistic, check_attn_vs_textbook, check_index_and_attend_composes,
+    check_decode_schedule, check_decode_steps_brute_force,
 ]

@@ -89,6 +89,31 @@ def test_empty_calls_are_noops(lib):
     assert lib.ds4x_sparse_attn(_p(A), _p(A), 1, _p(A), 0, 64, 512, 10, 512, 0.1, _p(A), None, None) == ds4x.OK
 
 
+def _decode(lib, capacity=100, S0=90, n_new=4, pos0=359, n_steps=8, H=64, D=128, ratio=4, k_top=512, dtype=1,
+            ws=0, q=0x10000, S_final=None):
+    A = 0x10000
+    return lib.ds4x_decode(_p(q), _p(A), _p(A), _p(A), _p(A), dtype, capacity, S0, _p(A), _p(A), n_new, pos0,
+                           n_steps, H, D, ratio, k_top, 64, 512, 0.1, _p(A), _p(A), _p(A), None, _p(A), ws,
+                           S_final, None)
+
+
+def test_decode_arguments_rejected_without_launch(lib):
+    assert _decode(lib, capacity=80) == ds4x.ERR_INVALID          # S0 > capacity
+    assert _decode(lib, n_steps=-1) == ds4x.ERR_INVALID
+    assert _decode(lib, ratio=0) == ds4x.ERR_INVALID
+    assert _decode(lib, pos0=-1) == ds4x.ERR_INVALID
+    assert _decode(lib, pos0=2**31 - 4) == ds4x.ERR_INVALID       # positions would overflow int32
+    assert _decode(lib, dtype=5) == ds4x.ERR_INVALID
+    assert _decode(lib, H=48) == ds4x.ERR_UNSUPPORTED
+    assert _decode(lib, k_top=2048) == ds4x.ERR_UNSUPPORTED
+    assert _decode(lib, k_top=510) == ds4x.ERR_UNSUPPORTED        # index rows would lose 16-byte alignment
+    assert _decode(lib, q=0x10002) == ds4x.ERR_INVALID            # misaligned
+    assert _decode(lib, ws=16) == ds4x.ERR_WORKSPACE
+    s = ctypes.c_int32(-7)
+    assert _decode(lib, n_steps=0, S_final=ctypes.byref(s)) == ds4x.OK   # nothing to do, nothing launched
+    assert s.value == 90
+
+
 def test_workspace_sizes(lib):
     # the fused entry keeps T x S fp32 scores (rounded up to 256 bytes)
     assert ds4x.workspace_bytes(2048, 2048, 512) >= 2048 * 2048 * 4
@@ -96,3 +121,6 @@ def test_workspace_sizes(lib):
     # one decode token over a long row is split and needs candidate scratch
     assert ds4x.topk_workspace_bytes(1, 262208, 512) > 0
     assert ds4x.topk_workspace_bytes(2048, 16384, 512) == 0
+    # the decode loop sizes its workspace for one token at full capacity
+    assert ds4x.decode_workspace_bytes(262208, 512) >= ds4x.workspace_bytes(1, 262208, 512) >= 262208 * 4
+    assert ds4x.decode_workspace_bytes(0, 512) == 0

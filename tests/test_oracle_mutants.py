@@ -36,6 +36,9 @@ MUTANTS = {
                           "else v = ldexp((double)(f + 1024), e - 24);"),
     "shortcut_wrong_count": ("for (int64_t i = 0; i < n; ++i) out[i] = (int32_t)i;",
                              "for (int64_t i = 0; i < n; ++i) out[i] = (int32_t)(i + 1);"),
+    "decode_append_one_early": ("(int64_t)S < (p + 1) / ratio) {", "(int64_t)S <= (p + 1) / ratio) {"),
+    "decode_position_shifted": ("const int64_t p = (int64_t)pos0 + i;", "const int64_t p = (int64_t)pos0 + i + 1;"),
+    "decode_first_staged_row_only": ("kv_new + (int64_t)a * Dkv,", "kv_new,"),
     "w_index_transposed": ("ref_decode_n(w + (int64_t)t * H, H, REF_F16, wd);\n      int64_t n",
                            "ref_decode_n(w + (int64_t)t, H, REF_F16, wd);\n      int64_t n"),
 }
