@@ -61,6 +61,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kSoftBar = 1, kEpiBar = 2, kGroupThreads = 128;
+constexpr int kMaxSplit = (DS4X_MAX_KTOP + kRows - 1) / kRows;  // items a token can be split into
 
 struct Params {
   const uint16_t* q;         // q_attn [T, 64, 512]; read by TMA (and prefetched to L2 a token ahead)
@@ -651,20 +652,34 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
                                                       uint16_t* __restrict__ out, float* __restrict__ lse) {
   const int t = blockIdx.x / kHq, h = blockIdx.x - t * kHq;
   const float* ml = part_ml + (int64_t)t * nsplit * 2 * kHq;
+  // every part's statistics and partial row are loaded before any is used (nsplit <= kMaxSplit)
+  float m[kMaxSplit], l[kMaxSplit];
+  float4 o[kMaxSplit];
+#pragma unroll
+  for (int i = 0; i < kMaxSplit; ++i) {
+    m[i] = -INFINITY;
+    l[i] = 0.f;
+    o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i < nsplit) {
+      m[i] = ml[i * 2 * kHq + h];
+      l[i] = ml[i * 2 * kHq + kHq + h];
+      o[i] = *reinterpret_cast<const float4*>(part_o + (((int64_t)t * nsplit + i) * kHq + h) * kDkv +
+                                              4 * threadIdx.x);
+    }
+  }
   float mx = -INFINITY;
-  for (int i = 0; i < nsplit; ++i) mx = fmaxf(mx, ml[i * 2 * kHq + h]);
+#pragma unroll
+  for (int i = 0; i < kMaxSplit; ++i) mx = fmaxf(mx, m[i]);
   float L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i = 0; i < nsplit; ++i) {
-    const float mi = ml[i * 2 * kHq + h];
-    const float wgt = (mi == -INFINITY) ? 0.f : exp2f(mi - mx);
-    L += wgt * ml[i * 2 * kHq + kHq + h];
-    const float4 o = *reinterpret_cast<const float4*>(part_o + (((int64_t)t * nsplit + i) * kHq + h) * kDkv +
-                                                      4 * threadIdx.x);
-    acc.x += wgt * o.x;
-    acc.y += wgt * o.y;
-    acc.z += wgt * o.z;
-    acc.w += wgt * o.w;
+#pragma unroll
+  for (int i = 0; i < kMaxSplit; ++i) {
+    const float wgt = (m[i] == -INFINITY) ? 0.f : exp2f(m[i] - mx);
+    L += wgt * l[i];
+    acc.x += wgt * o[i].x;
+    acc.y += wgt * o[i].y;
+    acc.z += wgt * o[i].z;
+    acc.w += wgt * o[i].w;
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   float r0, r1;

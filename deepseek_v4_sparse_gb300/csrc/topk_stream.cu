@@ -23,9 +23,11 @@
 //      bit where the buffer's max and min differ) and compact the buffer in place;
 //   3. at the end select once more, mark the winners in a bitmap over the row and emit them in
 //      ascending order with a block scan of the bitmap's popcounts.
-// A decode-sized row (one token, 262k rows) is split over many CTAs (same routine, each
-// emitting its local top-k as (key, row) pairs into the workspace) and merged by a second
-// kernel that runs the routine over the candidates.
+// Rows up to 32768 long are staged in shared memory and resolved with a histogram of the keys
+// (one pass for min / max, one for the histogram, one to mark the bins above the boundary bin
+// and collect the boundary bin, whose rows are then ranked exactly).
+// A decode-sized row (few tokens, e.g. one token over 262k rows) is spread over many CTAs with
+// the same histogram scheme run across the grid in three launches (see "long rows").
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -41,7 +43,6 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCap = 2048;                 // buffered survivors (>= k_top + kChunk)
 constexpr int kChunk = kThreads * 4;       // elements streamed per step
-constexpr int kSplitRows = 4096;           // rows per CTA when a row is split
 constexpr uint32_t kNoRow = 0xFFFFFFFFu;   // padding of partial candidate lists
 
 __device__ __forceinline__ uint32_t ordered_key(float x) {
@@ -56,7 +57,7 @@ __device__ __forceinline__ uint64_t composite(uint32_t key, uint32_t row) {
 constexpr int kBins = 2048;                // histogram of the fast path
 constexpr int kStageMax = 32768;           // rows up to this long are staged in shared memory
 
-struct Shared {
+struct alignas(16) Shared {
   uint32_t key[kCap];
   uint32_t row[kCap];
   uint32_t hist[256];
@@ -512,9 +513,8 @@ struct KParams {
   int T, S, ratio, k_top;
   int32_t* indices;
   int32_t* counts;
-  uint32_t* cand_key;  // [T, nsplit, k_top] (split mode)
-  uint32_t* cand_row;
-  int nsplit;
+  uint8_t* long_ws;     // long-row mode: one LongLayout block per token
+  int nslice;           // long-row mode: CTAs per token
   int* status;
 };
 
@@ -545,82 +545,351 @@ __global__ void __launch_bounds__(kThreads) topk_row_kernel(const KParams p) {
   emit_sorted(sh, bitmap, thr, n, p.k_top, out, cnt_out);
 }
 
-// Split mode, pass 1: CTA (t, part) keeps the k_top best of rows [part*kSplitRows, ...).
-__global__ void __launch_bounds__(kThreads) topk_part_kernel(const KParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
-  const int t = blockIdx.y, part = blockIdx.x;
-  const int n = n_visible(p.positions, t, p.ratio, p.S);
-  if (n <= p.k_top) return;  // the merge kernel takes the shortcut
-  const int lo = part * kSplitRows;
-  const int hi = min(n, lo + kSplitRows);
-  uint32_t* ck = p.cand_key + ((int64_t)t * p.nsplit + part) * p.k_top;
-  uint32_t* cr = p.cand_row + ((int64_t)t * p.nsplit + part) * p.k_top;
-  int have = 0;
-  if (lo < hi) {
-    RowSource src{p.scores + (int64_t)t * p.ld};
-    const uint64_t thr = stream_select(sh, src, lo, hi, p.k_top);
-    if (sh.count > p.k_top) compact(sh, thr);
-    have = sh.count;
-    for (int j = threadIdx.x; j < have; j += kThreads) {
-      ck[j] = sh.key[j];
-      cr[j] = sh.row[j];
-    }
+// ---------------------------------------------------------------------------- long rows
+// A token's row is spread over P = ceil(S / kSliceRows) CTAs, one slice each, in three launches
+// that run the histogram scheme of the staged path across the grid:
+//   long_minmax_kernel  min and max of the slice's ordered keys into the token's slot table;
+//                       zeroes the token's histogram, bitmap and counters
+//   long_hist_kernel    the row's min / max from the slots, then a kGBins-bin monotone histogram
+//                       of the slice (shared memory, then global atomics); the token's last CTA
+//                       (atomic ticket, no waiting) finds the boundary bin b* holding the k_top-th
+//                       largest key and the number of rows above it
+//   long_mark_kernel    rows in bins above b* are set in the token's bitmap (a warp owns a word:
+//                       plain stores), rows in b* are collected; the token's last CTA ranks the
+//                       collected rows by the composite order, adds the k_top - above best to the
+//                       bitmap and emits it in ascending row order (when more than kCandCap rows
+//                       share b*, it runs the streaming routine over the whole row instead).
+constexpr int kSliceRows = 2048;   // a multiple of 32: every bitmap word lies in one slice
+constexpr int kSlicePer = kSliceRows / kThreads;  // rows of a slice per thread, all loaded at once
+constexpr int kGBins = 4096;
+constexpr int kCandCap = 8192;
+
+struct LongCtl {
+  uint32_t kmin, mult, bstar, above;
+  uint32_t ncand, done2, done3, pad;
+};
+
+struct LongLayout {  // byte offsets inside one token's block of the workspace
+  size_t ctl, slots, hist, bitmap, ckey, crow, total;
+};
+
+__host__ __device__ inline size_t align_up(size_t n, size_t a) { return (n + a - 1) / a * a; }
+
+__host__ __device__ inline LongLayout long_layout(int S) {
+  const size_t P = (size_t)(S + kSliceRows - 1) / kSliceRows;
+  const size_t W = (size_t)(S + 31) / 32;
+  LongLayout L;
+  size_t o = 0;
+  L.ctl = o;
+  o += sizeof(LongCtl);
+  L.slots = o;
+  o = align_up(o + P * 2 * sizeof(uint32_t), 16);
+  L.hist = o;
+  o += (size_t)kGBins * sizeof(uint32_t);
+  L.bitmap = o;
+  o = align_up(o + W * sizeof(uint32_t), 16);
+  L.ckey = o;
+  o += (size_t)kCandCap * sizeof(uint32_t);
+  L.crow = o;
+  o += (size_t)kCandCap * sizeof(uint32_t);
+  L.total = align_up(o, 256);
+  return L;
+}
+
+// bin of an ordered key over [kmin, kmax]: direct when the range has at most kGBins values
+// (mult == 0), else umulhi(key - kmin, floor(kGBins 2^32 / range)); non-decreasing in the key
+__device__ __forceinline__ uint32_t long_bin(uint32_t key, uint32_t kmin, uint32_t mult) {
+  return mult == 0 ? key - kmin : __umulhi(key - kmin, mult);
+}
+
+// Block-wide reduction helpers on a few words of static shared memory.
+__device__ __forceinline__ uint32_t block_min_u32(uint32_t v, uint32_t* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  uint32_t r = red[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) r = min(r, red[w]);
+  return r;
+}
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  uint32_t r = red[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) r = max(r, red[w]);
+  return r;
+}
+
+// the thread's rows lo + i * kThreads + threadIdx.x of the slice as ordered keys (all loads issued
+// before any is used); rows at or past hi are flagged invalid
+__device__ __forceinline__ void load_slice(const float* row, int lo, int hi, uint32_t (&k)[kSlicePer],
+                                           bool (&v)[kSlicePer]) {
+  float x[kSlicePer];
+#pragma unroll
+  for (int i = 0; i < kSlicePer; ++i) {
+    const int j = lo + i * kThreads + threadIdx.x;
+    v[i] = j < hi;
+    x[i] = v[i] ? __ldcs(row + j) : 0.f;
   }
-  for (int j = have + threadIdx.x; j < p.k_top; j += kThreads) {
-    ck[j] = 0;
-    cr[j] = kNoRow;
+#pragma unroll
+  for (int i = 0; i < kSlicePer; ++i) k[i] = ordered_key(x[i]);
+}
+
+__global__ void __launch_bounds__(kThreads) long_minmax_kernel(const KParams p) {
+  __shared__ uint32_t red[kWarps];
+  const int t = blockIdx.y, part = blockIdx.x, P = gridDim.x;
+  const LongLayout L = long_layout(p.S);
+  uint8_t* blk = p.long_ws + (size_t)t * L.total;
+  uint32_t* hist = reinterpret_cast<uint32_t*>(blk + L.hist);
+  uint32_t* bm = reinterpret_cast<uint32_t*>(blk + L.bitmap);
+  const int W = (p.S + 31) / 32;
+  for (int i = part * kThreads + threadIdx.x; i < kGBins; i += P * kThreads) hist[i] = 0;
+  for (int i = part * kThreads + threadIdx.x; i < W; i += P * kThreads) bm[i] = 0;
+  if (part == 0 && threadIdx.x < (int)(sizeof(LongCtl) / 4)) reinterpret_cast<uint32_t*>(blk + L.ctl)[threadIdx.x] = 0;
+  const int n = n_visible(p.positions, t, p.ratio, p.S);
+  if (n <= p.k_top) return;
+  const int lo = part * kSliceRows, hi = min(n, lo + kSliceRows);
+  const float* row = p.scores + (int64_t)t * p.ld;
+  uint32_t mn = 0xFFFFFFFFu, mx = 0;
+  uint32_t k[kSlicePer];
+  bool v[kSlicePer];
+  load_slice(row, lo, hi, k, v);
+#pragma unroll
+  for (int i = 0; i < kSlicePer; ++i)
+    if (v[i]) {
+      mn = min(mn, k[i]);
+      mx = max(mx, k[i]);
+    }
+  mn = block_min_u32(mn, red);
+  mx = block_max_u32(mx, red);
+  if (threadIdx.x == 0) {  // an empty slice leaves the neutral pair (~0, 0)
+    uint32_t* slot = reinterpret_cast<uint32_t*>(blk + L.slots) + 2 * part;
+    slot[0] = mn;
+    slot[1] = mx;
   }
 }
 
-// Split mode, pass 2: one CTA per token over its nsplit * k_top candidates.
-__global__ void __launch_bounds__(kThreads) topk_merge_kernel(const KParams p) {
+__global__ void __launch_bounds__(kThreads) long_hist_kernel(const KParams p) {
+  __shared__ uint32_t sh_hist[kGBins];
+  __shared__ uint32_t red[kWarps];
+  __shared__ int sh_last;
+  const int t = blockIdx.y, part = blockIdx.x, P = gridDim.x;
+  const int n = n_visible(p.positions, t, p.ratio, p.S);
+  if (n <= p.k_top) return;
+  const LongLayout L = long_layout(p.S);
+  uint8_t* blk = p.long_ws + (size_t)t * L.total;
+  LongCtl* ctl = reinterpret_cast<LongCtl*>(blk + L.ctl);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(blk + L.hist);
+  const uint32_t* slots = reinterpret_cast<const uint32_t*>(blk + L.slots);
+  uint32_t mn = 0xFFFFFFFFu, mx = 0;
+  for (int i = threadIdx.x; i < P; i += kThreads) {
+    mn = min(mn, __ldcg(slots + 2 * i));
+    mx = max(mx, __ldcg(slots + 2 * i + 1));
+  }
+  const int lo = part * kSliceRows, hi = min(n, lo + kSliceRows);
+  const float* row = p.scores + (int64_t)t * p.ld;
+  uint32_t k[kSlicePer];
+  bool v[kSlicePer];
+  load_slice(row, lo, hi, k, v);  // in flight while the slots are reduced
+  const uint32_t kmin = block_min_u32(mn, red);
+  const uint32_t kmax = block_max_u32(mx, red);
+  const uint64_t range = (uint64_t)kmax - kmin + 1;
+  const uint32_t mult = range <= (uint64_t)kGBins ? 0u : (uint32_t)(((uint64_t)kGBins << 32) / range);
+  for (int i = threadIdx.x; i < kGBins; i += kThreads) sh_hist[i] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < kSlicePer; ++i)
+    if (v[i]) atomicAdd(&sh_hist[long_bin(k[i], kmin, mult)], 1u);
+  __syncthreads();
+  for (int i = threadIdx.x; i < kGBins; i += kThreads)
+    if (sh_hist[i]) atomicAdd(&hist[i], sh_hist[i]);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) sh_last = atomicAdd(&ctl->done2, 1u) == (uint32_t)(P - 1);
+  __syncthreads();
+  if (!sh_last) return;
+  __threadfence();
+  // the token's last CTA: suffix counts from the top bin down; thread i owns the 16 bins
+  // [kGBins - 16 (i+1), kGBins - 16 i)
+  constexpr int kPer = kGBins / kThreads;
+  uint32_t c[kPer], own = 0;
+  const int top = kGBins - kPer * threadIdx.x;  // bins top-1 .. top-kPer
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    c[i] = __ldcg(hist + top - 1 - i);
+    own += c[i];
+  }
+  // inclusive prefix over threads (thread 0 = highest bins)
+  uint32_t incl = own;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) red[warp] = incl;
+  __syncthreads();
+  uint32_t before_w = 0;
+  for (int w = 0; w < warp; ++w) before_w += red[w];
+  incl += before_w;
+  const uint32_t need = (uint32_t)p.k_top;
+  uint32_t run = incl - own;  // rows in bins above this thread's range
+  if (run < need && incl >= need) {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      if (run + c[i] >= need) {
+        ctl->kmin = kmin;
+        ctl->mult = mult;
+        ctl->bstar = (uint32_t)(top - 1 - i);
+        ctl->above = run;
+        break;
+      }
+      run += c[i];
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) long_mark_kernel(const KParams p) {
   extern __shared__ uint8_t smem_raw[];
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
-  uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem_raw + sizeof(Shared));
-  const int t = blockIdx.x;
+  uint32_t* sbm = reinterpret_cast<uint32_t*>(smem_raw + sizeof(Shared));
+  __shared__ int sh_last;
+  const int t = blockIdx.y, part = blockIdx.x, P = gridDim.x;
   const int n = n_visible(p.positions, t, p.ratio, p.S);
   int32_t* out = p.indices + (int64_t)t * p.k_top;
   int32_t* cnt_out = p.counts ? p.counts + t : nullptr;
   if (n <= p.k_top) {
-    emit_shortcut(n, p.k_top, out, cnt_out);
+    if (part == 0) emit_shortcut(n, p.k_top, out, cnt_out);
     return;
   }
-  const int m = p.nsplit * p.k_top;
-  CandSource src{p.cand_key + (int64_t)t * m, p.cand_row + (int64_t)t * m};
-  const uint64_t thr = stream_select(sh, src, 0, m, p.k_top);
-  emit_sorted(sh, bitmap, thr, n, p.k_top, out, cnt_out);
+  const LongLayout L = long_layout(p.S);
+  uint8_t* blk = p.long_ws + (size_t)t * L.total;
+  LongCtl* ctl = reinterpret_cast<LongCtl*>(blk + L.ctl);
+  uint32_t* bm = reinterpret_cast<uint32_t*>(blk + L.bitmap);
+  uint32_t* ckey = reinterpret_cast<uint32_t*>(blk + L.ckey);
+  uint32_t* crow = reinterpret_cast<uint32_t*>(blk + L.crow);
+  const int lo = part * kSliceRows, hi = min(n, lo + kSliceRows);
+  const float* row = p.scores + (int64_t)t * p.ld;
+  uint32_t ks[kSlicePer];
+  bool vs[kSlicePer];
+  load_slice(row, lo, hi, ks, vs);
+  const uint32_t kmin = __ldcg(&ctl->kmin), mult = __ldcg(&ctl->mult), bstar = __ldcg(&ctl->bstar);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int i = 0; i < kSlicePer; ++i) {
+    const int base = lo + i * kThreads + warp * 32;  // row of lane 0: a multiple of 32
+    if (base >= hi) break;
+    const int j = base + lane;
+    const bool valid = vs[i];
+    const uint32_t key = ks[i];
+    const uint32_t b = valid ? long_bin(key, kmin, mult) : 0u;
+    const uint32_t word = __ballot_sync(0xffffffffu, valid && b > bstar);
+    if (lane == 0) bm[base >> 5] = word;  // this warp owns the word (base is a multiple of 32)
+    const bool inb = valid && b == bstar;
+    const uint32_t bal = __ballot_sync(0xffffffffu, inb);
+    if (bal) {
+      uint32_t slot0 = 0;
+      if (lane == 0) slot0 = atomicAdd(&ctl->ncand, (uint32_t)__popc(bal));
+      slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+      if (inb) {
+        const uint32_t slot = slot0 + __popc(bal & ((1u << lane) - 1u));
+        if (slot < (uint32_t)kCandCap) {
+          ckey[slot] = key;
+          crow[slot] = (uint32_t)j;
+        }
+      }
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) sh_last = atomicAdd(&ctl->done3, 1u) == (uint32_t)(P - 1);
+  __syncthreads();
+  if (!sh_last) return;
+  __threadfence();
+  const int m = (int)__ldcg(&ctl->ncand);
+  if (m > kCandCap) {  // too many rows share the boundary bin: rank the whole row
+    const uint64_t thr = stream_select(sh, RowSource{row}, 0, n, p.k_top);
+    emit_sorted(sh, sbm, thr, n, p.k_top, out, cnt_out);
+    return;
+  }
+  const int need = p.k_top - (int)__ldcg(&ctl->above);
+  const int nw = (n + 31) >> 5;
+  {  // the token's bitmap into shared memory: 16-byte loads, eight in flight per thread
+    const int nq = (nw + 3) >> 2;  // the bitmap's allocation is a multiple of 16 bytes
+    const uint4* src = reinterpret_cast<const uint4*>(bm);
+    uint4* dst = reinterpret_cast<uint4*>(sbm);
+    for (int q0 = 0; q0 < nq; q0 += 8 * kThreads) {
+      uint4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int q = q0 + i * kThreads + threadIdx.x;
+        if (q < nq) v[i] = __ldcg(src + q);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int q = q0 + i * kThreads + threadIdx.x;
+        if (q < nq) dst[q] = v[i];
+      }
+    }
+  }
+  const uint64_t thr = stream_select(sh, CandSource{ckey, crow}, 0, m, need);
+  if (sh.count > need) compact(sh, thr);
+  for (int j = threadIdx.x; j < sh.count; j += kThreads) {
+    const uint32_t r = sh.row[j];
+    atomicOr(&sbm[r >> 5], 1u << (r & 31));
+  }
+  __syncthreads();
+  emit_bitmap(sh, sbm, n, p.k_top, out, cnt_out);
 }
 
-// dynamic shared memory of the row and merge kernels: the work struct, the bitmap of the row
-// and (row kernel, rows that are staged) 16 bytes of alignment slack plus the staged row
-size_t bitmap_smem(int S) { return sizeof(Shared) + (size_t)((S + 31) / 32 + 1) * sizeof(uint32_t); }
+// dynamic shared memory of the row and long-row mark kernels: the work struct, the bitmap of the
+// row and (row kernel, rows that are staged) 16 bytes of alignment slack plus the staged row
+// (the bitmap holds whole 16-byte groups: the long-row kernel copies it in with 16-byte stores)
+size_t bitmap_smem(int S) {
+  static_assert(sizeof(Shared) % 16 == 0, "the bitmap after Shared must be 16-byte aligned");
+  return sizeof(Shared) + (((size_t)(S + 31) / 32 + 1 + 3) & ~size_t(3)) * sizeof(uint32_t);
+}
 size_t row_kernel_smem(int S) {
   if (S > kStageMax) return bitmap_smem(S);
   return bitmap_smem(S) + 16 + ((size_t)(S + 3) & ~size_t(3)) * sizeof(float);
 }
 
-cudaError_t set_smem_attrs(size_t row_smem, size_t merge_smem) {
+cudaError_t set_smem_attrs(size_t row_smem, size_t mark_smem) {
   cudaError_t e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)row_smem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)merge_smem);
+    e = cudaFuncSetAttribute(long_mark_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mark_smem);
   return e;
 }
 
-int split_parts(int T, int S) {
-  // few tokens with long rows cannot fill the GPU with one CTA per token
+// CTAs per token in long-row mode (1: one CTA per token).  Few tokens with long rows cannot
+// fill the GPU with one CTA per token.
+int long_slices(int T, int S) {
   const int sms = device_sm_count();
-  if (S <= 2 * kSplitRows || T >= sms) return 1;
-  const int parts = (S + kSplitRows - 1) / kSplitRows;
-  return parts;
+  if (S <= 4 * kSliceRows || T >= sms) return 1;
+  return (S + kSliceRows - 1) / kSliceRows;
+}
+
+// the three long-row launches (workspace already checked)
+void launch_long(KParams& p, cudaStream_t st, size_t mark_smem) {
+  const dim3 grid(p.nslice, p.T);
+  long_minmax_kernel<<<grid, kThreads, 0, st>>>(p);
+  long_hist_kernel<<<grid, kThreads, 0, st>>>(p);
+  long_mark_kernel<<<grid, kThreads, mark_smem, st>>>(p);
+  count_launch(3);
 }
 
 }  // namespace
 
 size_t topk_workspace_bytes(int T, int S, int k_top) {
-  const int parts = split_parts(T, S);
-  if (parts <= 1) return 0;
-  return (size_t)T * parts * k_top * 2 * sizeof(uint32_t);
+  (void)k_top;
+  if (long_slices(T, S) <= 1) return 0;
+  return (size_t)T * long_layout(S).total;
 }
 
 int launch_topk(const TopkArgs& a, cudaStream_t stream) {
@@ -639,21 +908,17 @@ int launch_topk(const TopkArgs& a, cudaStream_t stream) {
   p.k_top = a.k_top;
   p.indices = a.indices;
   p.counts = a.counts;
-  p.nsplit = split_parts(a.T, a.S);
-  p.cand_key = nullptr;
-  p.cand_row = nullptr;
+  p.nslice = long_slices(a.T, a.S);
+  p.long_ws = nullptr;
   p.status = device_status_ptr();
-  if (p.nsplit <= 1) {
+  if (p.nslice <= 1) {
     topk_row_kernel<<<a.T, kThreads, smem, stream>>>(p);
     count_launch();
   } else {
     const size_t need = topk_workspace_bytes(a.T, a.S, a.k_top);
     if (a.workspace == nullptr || a.workspace_bytes < need) return DS4X_ERR_WORKSPACE;
-    p.cand_key = static_cast<uint32_t*>(a.workspace);
-    p.cand_row = p.cand_key + (size_t)a.T * p.nsplit * a.k_top;
-    topk_part_kernel<<<dim3(p.nsplit, a.T), kThreads, sizeof(Shared), stream>>>(p);
-    topk_merge_kernel<<<a.T, kThreads, msmem, stream>>>(p);
-    count_launch(2);
+    p.long_ws = static_cast<uint8_t*>(a.workspace);
+    launch_long(p, stream, msmem);
   }
   return cudaGetLastError() == cudaSuccess ? DS4X_OK : DS4X_ERR_CUDA;
 }
@@ -725,19 +990,16 @@ extern "C" int ds4x_topk_static_scratch(const float* scores, int64_t ld_scores, 
   p.k_top = k_top;
   p.indices = indices;
   p.counts = counts;
-  p.nsplit = split_parts(T, S);
-  p.cand_key = nullptr;
-  p.cand_row = nullptr;
+  p.nslice = long_slices(T, S);
+  p.long_ws = nullptr;
   p.status = device_status_ptr();
-  if (p.nsplit <= 1) {
+  if (p.nslice <= 1) {
     topk_row_kernel<<<T, kThreads, smem, st>>>(p);
   } else {
-    // every slot of the candidate lists is written by the split pass (rows or padding), so
-    // nothing left by an earlier call is ever read
-    p.cand_key = static_cast<uint32_t*>(scratch);
-    p.cand_row = p.cand_key + (size_t)T * p.nsplit * k_top;
-    topk_part_kernel<<<dim3(p.nsplit, T), kThreads, sizeof(Shared), st>>>(p);
-    topk_merge_kernel<<<T, kThreads, msmem, st>>>(p);
+    // the first launch zeroes every counter, histogram and bitmap the later ones read, so
+    // nothing left in the array by an earlier call is ever read
+    p.long_ws = static_cast<uint8_t*>(scratch);
+    launch_long(p, st, msmem);
   }
   return cudaGetLastError() == cudaSuccess ? DS4X_OK : DS4X_ERR_CUDA;
 }

@@ -186,6 +186,31 @@ def test_split_topk_decode_row():
     assert np.array_equal(cnt.cpu().numpy(), ref_cnt)
 
 
+@pytest.mark.parametrize("case", ["boundary_overflow", "all_equal", "few_tokens"])
+def test_long_row_topk_exact(case):
+    # long rows over many CTAs: a boundary bin with more rows than the candidate buffer (the last
+    # CTA ranks the whole row), a row of equal scores (lowest rows win), several tokens at once
+    rng = np.random.default_rng(12)
+    S, T = 262144, 1
+    if case == "boundary_overflow":
+        scores = np.floor(rng.standard_normal((1, S)) / 1.5).astype(np.float32)   # ~17k rows tie at 1.0
+    elif case == "all_equal":
+        scores = np.full((1, S), 3.25, dtype=np.float32)
+    else:
+        T = 7
+        scores = rng.standard_normal((T, S)).astype(np.float32)
+        scores[3, 5000:9000] = scores[3].max()                                    # a tied block on top
+    pos = (4 * S - 1 - np.arange(T) * 40000).astype(np.int32)                      # different n per token
+    idx, cnt = ds4x.topk(torch.from_numpy(scores).cuda(), torch.from_numpy(pos).cuda(), S, 4, 512)
+    torch.cuda.synchronize()
+    assert ds4x.device_status() == ds4x.OK
+    ref_idx, ref_cnt = oracle.topk(scores, pos, S, 4, 512)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    assert np.array_equal(cnt.cpu().numpy(), ref_cnt)
+    if case == "all_equal":
+        assert np.array_equal(ref_idx[0], np.arange(512))
+
+
 # --------------------------------------- full-size workloads in the benchmark's launch shape
 @pytest.mark.parametrize("name", ["prefill_8k", "prefill_64k"])
 def test_full_size_sampled(name):
