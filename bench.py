@@ -54,6 +54,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the 1M-context decode measurement")
+    ap.add_argument("--decode-steps", type=int, default=256, help="decode steps per timed call (decode_1m)")
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
 
@@ -234,7 +235,7 @@ def run_reference(args, wl):
 
 
 # ---------------------------------------------------------------------------- decode loop
-def measure_decode(ds4x, torch, dev, stream, seed: int, reps: int = 3, n_steps: int = 256):
+def measure_decode(ds4x, torch, dev, stream, seed: int, reps: int = 3, n_steps: int = 256, warm: int = 1):
     """The 1M-context decode: n_steps single-token steps from position 1048575 over 262144
     resident rows, a row appended every 4 positions (63 over 256 steps), each step
     score -> top-512 -> sparse MQA.  One timed unit is a whole ds4x_decode call (appends
@@ -264,7 +265,8 @@ def measure_decode(ds4x, torch, dev, stream, seed: int, reps: int = 3, n_steps: 
                         scale=wl.scale, positions=pos, indices=idx, out=out, lse=lse, workspace=ws, stream=stream)
         return r[4], ds4x.last_launch_count()
 
-    s_final, launches = call()
+    for _ in range(max(1, warm)):
+        s_final, launches = call()
     torch.cuda.synchronize()
     assert ds4x.device_status() == ds4x.OK
     times = []
@@ -338,6 +340,37 @@ def measure_decode(ds4x, torch, dev, stream, seed: int, reps: int = 3, n_steps: 
     }
 
 
+def decode_main(args, ds4x, torch, dev, rank, world):
+    """--workload decode_1m: the decode loop is the step (one call = decode_steps tokens)."""
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(dev.index or 0)
+    with sampler:
+        dec = measure_decode(ds4x, torch, dev, stream, args.seed + rank, reps=max(1, args.steps),
+                             n_steps=args.decode_steps, warm=max(3, args.warmup))
+    peaks = load_peaks()
+    # a decode step is bound by memory: every step reads all of k ([rows, 128] fp16) for the scores,
+    # writes and reads one fp32 score per row, and gathers 512 kv rows; rows = the average S
+    wl = synth.WORKLOADS["decode_1m"]
+    rows = wl.S + dec["appended_rows"] / 2.0
+    step_bytes = 2.0 * wl.D * rows + 2 * 4.0 * rows + 2.0 * wl.Dkv * wl.k_top
+    roof = {"kernel": "decode step (score, top-k, attention launches)", "bound": "hbm",
+            "achieved": step_bytes / (dec["us_per_step"] * 1e-6) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "algorithmic": step_bytes, "traffic": None}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["peak_source"] = f"{peaks['source']} (burst)"
+    if rank == 0:
+        step_ms = 1e3 * dec["steps"] / dec["value"]
+        line = {
+            "metric": METRIC, "value": world * dec["value"], "unit": "decode tokens/s", "n_gpus": world,
+            "steps": max(1, args.steps), "warmup": max(3, args.warmup), "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16+bf16 (fp32 accumulate)",
+            "data": "synthetic", "config": {"workload": dec["workload"], "l2": dec["l2"]},
+            "roofline": roof, "decode": dec, "cpu_baseline": None, "e2e": None,
+            "gpu_launches": dec["gpu_launches_per_call"] * max(1, args.steps), "clocks": sampler.summary(),
+        }
+        print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------------------- GPU arm
 def main():
     args = parse()
@@ -361,6 +394,9 @@ def main():
     if world > 1:
         dist.barrier()
     ds4x.load()
+
+    if wl.name == "decode_1m":
+        return decode_main(args, ds4x, torch, dev, rank, world)
 
     # every rank processes its own chunk: same shapes, its own seed
     inp = synth.make_inputs(wl, seed=args.seed + rank)
