@@ -15,11 +15,14 @@
 #include <stdint.h>
 
 #include "ds4x_internal.h"
+#include "ds4x_ptx.cuh"
 
 namespace ds4x {
 namespace {
 
 __global__ void fill_positions_kernel(int32_t* positions, int32_t pos0, int n) {
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) positions[i] = pos0 + i;
 }
@@ -28,6 +31,8 @@ __global__ void fill_positions_kernel(int32_t* positions, int32_t pos0, int n) {
 // pointers already point at the first destination and source rows.
 __global__ void append_rows_kernel(uint4* __restrict__ k, const uint4* __restrict__ k_new, int k16,
                                    uint4* __restrict__ kv, const uint4* __restrict__ kv_new, int kv16, int n) {
+  pdl_wait();
+  pdl_trigger();
   const int per_row = k16 + kv16;
   const int total = n * per_row;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
@@ -82,9 +87,10 @@ int ds4x_decode(const void* q, const void* w, const void* q_attn, void* k, void*
   if (workspace_bytes < ds4x_decode_workspace_bytes(capacity, k_top)) return DS4X_ERR_WORKSPACE;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  fill_positions_kernel<<<(n_steps + 255) / 256, 256, 0, st>>>(positions, pos0, n_steps);
+  if (launch_pdl(fill_positions_kernel, dim3((n_steps + 255) / 256), dim3(256), 0, st, positions, pos0, n_steps) !=
+      cudaSuccess)
+    return DS4X_ERR_CUDA;
   count_launch();
-  if (cudaGetLastError() != cudaSuccess) return DS4X_ERR_CUDA;
   const int k16 = D * 2 / 16, kv16 = Dkv * 2 / 16;
   const int bf16 = kv_dtype == DS4X_BF16 ? 1 : 0;
   int S = S0, appended = 0;
@@ -95,12 +101,13 @@ int ds4x_decode(const void* q, const void* w, const void* q_attn, void* k, void*
       int n = (int)((need - S) < (int64_t)(n_new - appended) ? (need - S) : (n_new - appended));
       if (n > capacity - S) n = capacity - S;
       const int total = n * (k16 + kv16);
-      append_rows_kernel<<<(total + 255) / 256 < 64 ? (total + 255) / 256 : 64, 256, 0, st>>>(
-          static_cast<uint4*>(k) + (int64_t)S * k16, static_cast<const uint4*>(k_new) + (int64_t)appended * k16, k16,
-          static_cast<uint4*>(kv) + (int64_t)S * kv16, static_cast<const uint4*>(kv_new) + (int64_t)appended * kv16,
-          kv16, n);
+      const int blocks = (total + 255) / 256 < 64 ? (total + 255) / 256 : 64;
+      if (launch_pdl(append_rows_kernel, dim3(blocks), dim3(256), 0, st, static_cast<uint4*>(k) + (int64_t)S * k16,
+                     static_cast<const uint4*>(k_new) + (int64_t)appended * k16, k16,
+                     static_cast<uint4*>(kv) + (int64_t)S * kv16,
+                     static_cast<const uint4*>(kv_new) + (int64_t)appended * kv16, kv16, n) != cudaSuccess)
+        return DS4X_ERR_CUDA;
       count_launch();
-      if (cudaGetLastError() != cudaSuccess) return DS4X_ERR_CUDA;
       S += n;
       appended += n;
     }

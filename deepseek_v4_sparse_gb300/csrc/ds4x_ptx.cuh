@@ -83,6 +83,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
 }
 
 // ----------------------------------------------------------------------------------- TMA
+// Programmatic dependent launch.  A kernel launched with launch_pdl may start while the kernel
+// before it on the stream is still running: pdl_wait() blocks until that kernel has completed and
+// its memory is visible (it returns at once for a kernel launched normally); pdl_trigger() lets the
+// next kernel be launched.  Every kernel of this library waits before it touches global memory
+// written by earlier work and triggers only after its wait, so at most two kernels overlap and the
+// earlier of them has nothing pending before it.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

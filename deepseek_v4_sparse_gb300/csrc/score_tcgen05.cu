@@ -151,6 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // everything above touched only this CTA's own resources
+  pdl_trigger();
 
   const long long beg = (long long)blockIdx.x * p.total_items / gridDim.x;
   const long long end = (long long)(blockIdx.x + 1) * p.total_items / gridDim.x;
@@ -394,9 +396,9 @@ int launch_impl(const ScoreArgs& a, cudaStream_t stream) {
   p.status = device_status_ptr();
   const int sms = device_sm_count();
   const int grid = (int)(p.total_items < sms ? p.total_items : sms);
-  score_kernel<H, D><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, p);
+  const cudaError_t e = launch_pdl(score_kernel<H, D>, dim3(grid), dim3(kThreads), (size_t)C::SMEM, stream, tq, tk, p);
   count_launch();
-  return cudaGetLastError() == cudaSuccess ? DS4X_OK : DS4X_ERR_CUDA;
+  return e == cudaSuccess ? DS4X_OK : DS4X_ERR_CUDA;
 }
 
 }  // namespace

@@ -258,6 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // everything above touched only this CTA's own resources
+  pdl_trigger();
 
   if (warp < 4) {
     // ------------------------------------------------------------------------ gather
@@ -650,6 +652,8 @@ template <bool kBf16>
 __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_o,
                                                       const float* __restrict__ part_ml, int nsplit,
                                                       uint16_t* __restrict__ out, float* __restrict__ lse) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x / kHq, h = blockIdx.x - t * kHq;
   const float* ml = part_ml + (int64_t)t * nsplit * 2 * kHq;
   // every part's statistics and partial row are loaded before any is used (nsplit <= kMaxSplit)
@@ -779,14 +783,14 @@ int launch_impl(const AttnArgs& a, cudaStream_t stream) {
   }
   p.items = a.T * p.nsplit;
   const int grid = p.items < sms ? p.items : sms;
-  sparse_mqa_kernel<kBf16><<<grid, kThreads, kSmem, stream>>>(tq, p);
+  if (launch_pdl(sparse_mqa_kernel<kBf16>, dim3(grid), dim3(kThreads), (size_t)kSmem, stream, tq, p) != cudaSuccess)
+    return DS4X_ERR_CUDA;
   count_launch();
-  if (cudaGetLastError() != cudaSuccess) return DS4X_ERR_CUDA;
   if (p.nsplit > 1) {
-    combine_kernel<kBf16><<<a.T * kHq, kDkv / 4, 0, stream>>>(p.part_o, p.part_ml, p.nsplit,
-                                                              static_cast<uint16_t*>(a.out), a.lse);
+    if (launch_pdl(combine_kernel<kBf16>, dim3(a.T * kHq), dim3(kDkv / 4), 0, stream, p.part_o, p.part_ml, p.nsplit,
+                   static_cast<uint16_t*>(a.out), a.lse) != cudaSuccess)
+      return DS4X_ERR_CUDA;
     count_launch();
-    if (cudaGetLastError() != cudaSuccess) return DS4X_ERR_CUDA;
   }
   return DS4X_OK;
 }

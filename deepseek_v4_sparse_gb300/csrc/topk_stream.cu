@@ -520,6 +520,8 @@ struct KParams {
 
 // One CTA per token: the whole row.
 __global__ void __launch_bounds__(kThreads) topk_row_kernel(const KParams p) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem_raw + sizeof(Shared));
@@ -642,6 +644,8 @@ __device__ __forceinline__ void load_slice(const float* row, int lo, int hi, uin
 }
 
 __global__ void __launch_bounds__(kThreads) long_minmax_kernel(const KParams p) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ uint32_t red[kWarps];
   const int t = blockIdx.y, part = blockIdx.x, P = gridDim.x;
   const LongLayout L = long_layout(p.S);
@@ -676,6 +680,8 @@ __global__ void __launch_bounds__(kThreads) long_minmax_kernel(const KParams p) 
 }
 
 __global__ void __launch_bounds__(kThreads) long_hist_kernel(const KParams p) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ uint32_t sh_hist[kGBins];
   __shared__ uint32_t red[kWarps];
   __shared__ int sh_last;
@@ -756,6 +762,8 @@ __global__ void __launch_bounds__(kThreads) long_hist_kernel(const KParams p) {
 }
 
 __global__ void __launch_bounds__(kThreads) long_mark_kernel(const KParams p) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
   uint32_t* sbm = reinterpret_cast<uint32_t*>(smem_raw + sizeof(Shared));
@@ -876,12 +884,13 @@ int long_slices(int T, int S) {
 }
 
 // the three long-row launches (workspace already checked)
-void launch_long(KParams& p, cudaStream_t st, size_t mark_smem) {
+cudaError_t launch_long(KParams& p, cudaStream_t st, size_t mark_smem) {
   const dim3 grid(p.nslice, p.T);
-  long_minmax_kernel<<<grid, kThreads, 0, st>>>(p);
-  long_hist_kernel<<<grid, kThreads, 0, st>>>(p);
-  long_mark_kernel<<<grid, kThreads, mark_smem, st>>>(p);
+  cudaError_t e = launch_pdl(long_minmax_kernel, grid, dim3(kThreads), 0, st, p);
+  if (e == cudaSuccess) e = launch_pdl(long_hist_kernel, grid, dim3(kThreads), 0, st, p);
+  if (e == cudaSuccess) e = launch_pdl(long_mark_kernel, grid, dim3(kThreads), mark_smem, st, p);
   count_launch(3);
+  return e;
 }
 
 }  // namespace
@@ -912,13 +921,13 @@ int launch_topk(const TopkArgs& a, cudaStream_t stream) {
   p.long_ws = nullptr;
   p.status = device_status_ptr();
   if (p.nslice <= 1) {
-    topk_row_kernel<<<a.T, kThreads, smem, stream>>>(p);
+    if (launch_pdl(topk_row_kernel, dim3(a.T), dim3(kThreads), smem, stream, p) != cudaSuccess) return DS4X_ERR_CUDA;
     count_launch();
   } else {
     const size_t need = topk_workspace_bytes(a.T, a.S, a.k_top);
     if (a.workspace == nullptr || a.workspace_bytes < need) return DS4X_ERR_WORKSPACE;
     p.long_ws = static_cast<uint8_t*>(a.workspace);
-    launch_long(p, stream, msmem);
+    if (launch_long(p, stream, msmem) != cudaSuccess) return DS4X_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? DS4X_OK : DS4X_ERR_CUDA;
 }
@@ -993,13 +1002,14 @@ extern "C" int ds4x_topk_static_scratch(const float* scores, int64_t ld_scores, 
   p.nslice = long_slices(T, S);
   p.long_ws = nullptr;
   p.status = device_status_ptr();
+  cudaError_t e;
   if (p.nslice <= 1) {
-    topk_row_kernel<<<T, kThreads, smem, st>>>(p);
+    e = launch_pdl(topk_row_kernel, dim3(T), dim3(kThreads), smem, st, p);
   } else {
     // the first launch zeroes every counter, histogram and bitmap the later ones read, so
     // nothing left in the array by an earlier call is ever read
     p.long_ws = static_cast<uint8_t*>(scratch);
-    launch_long(p, st, msmem);
+    e = launch_long(p, st, msmem);
   }
-  return cudaGetLastError() == cudaSuccess ? DS4X_OK : DS4X_ERR_CUDA;
+  return e == cudaSuccess ? DS4X_OK : DS4X_ERR_CUDA;
 }
