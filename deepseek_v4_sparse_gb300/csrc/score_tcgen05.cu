@@ -163,8 +163,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int cur_g = -1, rows = 0;
       bool started = false;
       uint32_t q_it = 0, k_it = 0;
+      int g = (int)(beg / p.n_stiles), st = (int)(beg % p.n_stiles) - 1;
       for (long long it = beg; it < end; ++it) {
-        const int g = (int)(it / p.n_stiles), st = (int)(it % p.n_stiles);
+        if (++st == p.n_stiles) {
+          st = 0;
+          ++g;
+        }
         if (g != cur_g) {
           cur_g = g;
           rows = group_rows<C::TPT>(p, g);
@@ -199,8 +203,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int cur_g = -1, rows = 0, qb = -1;
       bool started = false;
       uint32_t q_it = 0, k_it = 0, a_it = 0;
+      int g = (int)(beg / p.n_stiles), st = (int)(beg % p.n_stiles) - 1;
       for (long long it = beg; it < end; ++it) {
-        const int g = (int)(it / p.n_stiles), st = (int)(it % p.n_stiles);
+        if (++st == p.n_stiles) {
+          st = 0;
+          ++g;
+        }
         if (g != cur_g) {
           cur_g = g;
           rows = group_rows<C::TPT>(p, g);
@@ -266,8 +274,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t a_it = 0;
     int nvis[C::HALF];
     if (beg < end) prefetch((int)(beg / p.n_stiles));
+    int g = (int)(beg / p.n_stiles), st = (int)(beg % p.n_stiles) - 1;
     for (long long it = beg; it < end; ++it) {
-      const int g = (int)(it / p.n_stiles), st = (int)(it % p.n_stiles);
+      if (++st == p.n_stiles) {
+        st = 0;
+        ++g;
+      }
       if (g != cur_g) {
         cur_g = g;
         rows = group_rows<C::TPT>(p, g);
