@@ -514,6 +514,7 @@ struct KParams {
   int32_t* indices;
   int32_t* counts;
   uint8_t* long_ws;     // long-row mode: one LongLayout block per token
+  uint32_t* gbar;       // one-launch long-row mode: a barrier counter per token (zeroed before the launch)
   int nslice;           // long-row mode: CTAs per token
   int* status;
 };
@@ -563,16 +564,16 @@ __global__ void __launch_bounds__(kThreads) topk_row_kernel(const KParams p) {
 //                       share b*, it runs the streaming routine over the whole row instead).
 constexpr int kSliceRows = 2048;   // a multiple of 32: every bitmap word lies in one slice
 constexpr int kSlicePer = kSliceRows / kThreads;  // rows of a slice per thread, all loaded at once
-constexpr int kGBins = 4096;
+constexpr int kGBins = 1024;
 constexpr int kCandCap = 8192;
 
 struct LongCtl {
   uint32_t kmin, mult, bstar, above;
-  uint32_t ncand, done2, done3, pad;
+  uint32_t ncand, done2, done3, whole;  // whole: one-launch mode, slice 0 emitted the whole row
 };
 
 struct LongLayout {  // byte offsets inside one token's block of the workspace
-  size_t ctl, slots, hist, bitmap, ckey, crow, total;
+  size_t ctl, slots, scnt, hist, bitmap, ckey, crow, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t n, size_t a) { return (n + a - 1) / a * a; }
@@ -586,6 +587,8 @@ __host__ __device__ inline LongLayout long_layout(int S) {
   o += sizeof(LongCtl);
   L.slots = o;
   o = align_up(o + P * 2 * sizeof(uint32_t), 16);
+  L.scnt = o;  // rows each slice selects (one-launch mode)
+  o = align_up(o + P * sizeof(uint32_t), 16);
   L.hist = o;
   o += (size_t)kGBins * sizeof(uint32_t);
   L.bitmap = o;
@@ -856,6 +859,243 @@ __global__ void __launch_bounds__(kThreads) long_mark_kernel(const KParams p) {
   emit_bitmap(sh, sbm, n, p.k_top, out, cnt_out);
 }
 
+// ----------------------------------------------------------------- long rows, one launch
+// When a token's slices can all be resident at once (a cooperative launch), the scheme above
+// runs in one kernel: a per-token grid barrier (an atomic counter polled with a time limit)
+// separates the phases, each slice keeps its keys in registers throughout, and the emission is
+// parallel: after slice 0 has ranked the boundary bin, every slice writes its selected rows at
+// the offset given by the counts of the slices before it.
+
+// Arrive on the token's counter and wait until it reaches `target` (= slices x phase).
+__device__ bool token_barrier(uint32_t* counter, uint32_t target, int* status, int site) {
+  __shared__ int sh_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(counter, 1u);
+    int ok = 1;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+      uint32_t v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+      if (v >= target) break;
+      if (global_timer_ns() - t0 > DS4X_WAIT_TIMEOUT_NS) {
+        report_timeout(status, site);
+        ok = 0;
+        break;
+      }
+      __nanosleep(64);
+    }
+    sh_ok = ok;
+  }
+  __syncthreads();
+  return sh_ok != 0;
+}
+
+__global__ void __launch_bounds__(kThreads) long_coop_kernel(const KParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
+  uint32_t* sbm = reinterpret_cast<uint32_t*>(smem_raw + sizeof(Shared));  // whole-row fallback only
+  __shared__ uint32_t sh_hist[kGBins];
+  __shared__ uint32_t red[kWarps];
+  __shared__ uint32_t sh_b[3];
+  const int t = blockIdx.y, part = blockIdx.x, P = gridDim.x;
+  const int n = n_visible(p.positions, t, p.ratio, p.S);
+  int32_t* out = p.indices + (int64_t)t * p.k_top;
+  int32_t* cnt_out = p.counts ? p.counts + t : nullptr;
+  if (n <= p.k_top) {  // every slice of the token leaves here, before any barrier
+    if (part == 0) emit_shortcut(n, p.k_top, out, cnt_out);
+    return;
+  }
+  const LongLayout L = long_layout(p.S);
+  uint8_t* blk = p.long_ws + (size_t)t * L.total;
+  LongCtl* ctl = reinterpret_cast<LongCtl*>(blk + L.ctl);
+  uint32_t* slots = reinterpret_cast<uint32_t*>(blk + L.slots);
+  uint32_t* scnt = reinterpret_cast<uint32_t*>(blk + L.scnt);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(blk + L.hist);
+  uint32_t* bm = reinterpret_cast<uint32_t*>(blk + L.bitmap);
+  uint32_t* ckey = reinterpret_cast<uint32_t*>(blk + L.ckey);
+  uint32_t* crow = reinterpret_cast<uint32_t*>(blk + L.crow);
+  uint32_t* counter = p.gbar + t;
+  const int W = (p.S + 31) / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  // phase 1: zero this slice's share of the scratch; the slice's keys; their min and max
+  for (int i = part * kThreads + threadIdx.x; i < kGBins; i += P * kThreads) hist[i] = 0;
+  for (int i = part * kThreads + threadIdx.x; i < W; i += P * kThreads) bm[i] = 0;
+  if (part == 0 && threadIdx.x < (int)(sizeof(LongCtl) / 4)) reinterpret_cast<uint32_t*>(ctl)[threadIdx.x] = 0;
+  const int lo = part * kSliceRows, hi = min(n, lo + kSliceRows);
+  const float* row = p.scores + (int64_t)t * p.ld;
+  uint32_t k[kSlicePer];
+  bool v[kSlicePer];
+  load_slice(row, lo, hi, k, v);
+  uint32_t mn = 0xFFFFFFFFu, mx = 0;
+#pragma unroll
+  for (int i = 0; i < kSlicePer; ++i)
+    if (v[i]) {
+      mn = min(mn, k[i]);
+      mx = max(mx, k[i]);
+    }
+  mn = block_min_u32(mn, red);
+  mx = block_max_u32(mx, red);
+  if (threadIdx.x == 0) {
+    slots[2 * part] = mn;
+    slots[2 * part + 1] = mx;
+  }
+  if (!token_barrier(counter, (uint32_t)P, p.status, 60)) return;
+
+  // phase 2: the row's key range from the slots; histogram of the slice into the token's
+  mn = 0xFFFFFFFFu;
+  mx = 0;
+  for (int i = threadIdx.x; i < P; i += kThreads) {
+    mn = min(mn, __ldcg(slots + 2 * i));
+    mx = max(mx, __ldcg(slots + 2 * i + 1));
+  }
+  const uint32_t kmin = block_min_u32(mn, red);
+  const uint32_t kmax = block_max_u32(mx, red);
+  const uint64_t range = (uint64_t)kmax - kmin + 1;
+  const uint32_t mult = range <= (uint64_t)kGBins ? 0u : (uint32_t)(((uint64_t)kGBins << 32) / range);
+  for (int i = threadIdx.x; i < kGBins; i += kThreads) sh_hist[i] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < kSlicePer; ++i)
+    if (v[i]) atomicAdd(&sh_hist[long_bin(k[i], kmin, mult)], 1u);
+  __syncthreads();
+  for (int i = threadIdx.x; i < kGBins; i += kThreads)
+    if (sh_hist[i]) atomicAdd(&hist[i], sh_hist[i]);
+  if (!token_barrier(counter, 2u * P, p.status, 61)) return;
+
+  // phase 3: every slice finds the boundary bin b* from the token's histogram, writes its words
+  // of the bitmap (rows in bins above b*) and collects its rows in b*
+  {
+    constexpr int kPer = kGBins / kThreads;
+    uint32_t c[kPer], own = 0;
+    const int top = kGBins - kPer * threadIdx.x;  // this thread's bins: top-1 .. top-kPer
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      c[i] = __ldcg(hist + top - 1 - i);
+      own += c[i];
+    }
+    uint32_t total;
+    const uint32_t incl = block_scan(own, sh, &total);  // rows in this thread's bins and above
+    uint32_t run = incl - own;
+    const uint32_t need = (uint32_t)p.k_top;
+    if (run < need && incl >= need) {
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        if (run + c[i] >= need) {
+          sh_b[0] = (uint32_t)(top - 1 - i);
+          sh_b[1] = run;
+          break;
+        }
+        run += c[i];
+      }
+    }
+    __syncthreads();
+  }
+  const uint32_t bstar = sh_b[0], above = sh_b[1];
+  uint32_t marked = 0;
+#pragma unroll
+  for (int i = 0; i < kSlicePer; ++i) {
+    const int base = lo + i * kThreads + warp * 32;  // row of lane 0: a multiple of 32
+    if (base >= hi) break;
+    const int j = base + lane;
+    const uint32_t b = v[i] ? long_bin(k[i], kmin, mult) : 0u;
+    const uint32_t word = __ballot_sync(0xffffffffu, v[i] && b > bstar);
+    if (lane == 0) {
+      bm[base >> 5] = word;
+      marked += __popc(word);
+    }
+    const bool inb = v[i] && b == bstar;
+    const uint32_t bal = __ballot_sync(0xffffffffu, inb);
+    if (bal) {
+      uint32_t slot0 = 0;
+      if (lane == 0) slot0 = atomicAdd(&ctl->ncand, (uint32_t)__popc(bal));
+      slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+      if (inb) {
+        const uint32_t slot = slot0 + __popc(bal & ((1u << lane) - 1u));
+        if (slot < (uint32_t)kCandCap) {
+          ckey[slot] = k[i];
+          crow[slot] = (uint32_t)j;
+        }
+      }
+    }
+  }
+  if (lane == 0) red[warp] = marked;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t sum = 0;
+    for (int w = 0; w < kWarps; ++w) sum += red[w];
+    scnt[part] = sum;
+  }
+  if (!token_barrier(counter, 3u * P, p.status, 62)) return;
+
+  // phase 4: slice 0 ranks the boundary bin's rows and adds the missing ones (or, when more than
+  // kCandCap rows share the bin, ranks and emits the whole row itself)
+  if (part == 0) {
+    const int m = (int)__ldcg(&ctl->ncand);
+    if (m > kCandCap) {
+      const uint64_t thr = stream_select(sh, RowSource{row}, 0, n, p.k_top);
+      emit_sorted(sh, sbm, thr, n, p.k_top, out, cnt_out);
+      if (threadIdx.x == 0) ctl->whole = 1;
+    } else if (m <= kThreads) {
+      // few candidates: candidate j is in iff fewer than `need` candidates beat it
+      const int need = p.k_top - (int)above;
+      for (int j = threadIdx.x; j < m; j += kThreads) {
+        sh.key[j] = __ldcg(ckey + j);
+        sh.row[j] = __ldcg(crow + j);
+      }
+      __syncthreads();
+      if ((int)threadIdx.x < m) {
+        const uint64_t mine = composite(sh.key[threadIdx.x], sh.row[threadIdx.x]);
+        int rank = 0;
+        for (int j = 0; j < m; ++j) rank += composite(sh.key[j], sh.row[j]) > mine;
+        if (rank < need) {
+          const uint32_t r = sh.row[threadIdx.x];
+          atomicOr(&bm[r >> 5], 1u << (r & 31));
+          atomicAdd(&scnt[r / kSliceRows], 1u);
+        }
+      }
+      if (cnt_out && threadIdx.x == 0) *cnt_out = p.k_top;
+    } else {
+      const int need = p.k_top - (int)above;
+      const uint64_t thr = stream_select(sh, CandSource{ckey, crow}, 0, m, need);
+      if (sh.count > need) compact(sh, thr);
+      for (int j = threadIdx.x; j < sh.count; j += kThreads) {
+        const uint32_t r = sh.row[j];
+        atomicOr(&bm[r >> 5], 1u << (r & 31));
+        atomicAdd(&scnt[r / kSliceRows], 1u);
+      }
+      if (cnt_out && threadIdx.x == 0) *cnt_out = p.k_top;
+    }
+  }
+  if (!token_barrier(counter, 4u * P, p.status, 63)) return;
+  if (__ldcg(&ctl->whole)) return;
+
+  // phase 5: this slice's selected rows, in ascending order, after those of the slices before it
+  uint32_t before = 0;
+  for (int i = threadIdx.x; i < part; i += kThreads) before += __ldcg(scnt + i);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+  __syncthreads();
+  if (lane == 0) red[warp] = before;
+  __syncthreads();
+  uint32_t offset = 0;
+  for (int w = 0; w < kWarps; ++w) offset += red[w];
+  constexpr int kSliceWords = kSliceRows / 32;
+  const int w0 = lo >> 5;
+  const uint32_t word = (threadIdx.x < kSliceWords && lo + 32 * threadIdx.x < hi) ? __ldcg(bm + w0 + threadIdx.x) : 0u;
+  uint32_t total;
+  const uint32_t incl = block_scan((uint32_t)__popc(word), sh, &total);
+  uint32_t pos = offset + incl - (uint32_t)__popc(word);
+  uint32_t bits = word;
+  while (bits) {
+    const int b = __ffs(bits) - 1;
+    bits &= bits - 1;
+    out[pos++] = (w0 + (int)threadIdx.x) * 32 + b;
+  }
+}
+
 // dynamic shared memory of the row and long-row mark kernels: the work struct, the bitmap of the
 // row and (row kernel, rows that are staged) 16 bytes of alignment slack plus the staged row
 // (the bitmap holds whole 16-byte groups: the long-row kernel copies it in with 16-byte stores)
@@ -868,10 +1108,76 @@ size_t row_kernel_smem(int S) {
   return bitmap_smem(S) + 16 + ((size_t)(S + 3) & ~size_t(3)) * sizeof(float);
 }
 
+// Per-device host state: the largest dynamic shared memory granted to each kernel so far (the
+// attribute is raised only when a call needs more) and the last occupancy answer.
+struct DeviceTopkState {
+  size_t row_smem = 0, mark_smem = 0;
+  size_t occ_smem = 0;
+  int occ_blocks = -1;
+};
+std::mutex g_topk_state_mutex;
+DeviceTopkState g_topk_state[64];
+
+int current_device_index() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return 0;
+  return d;
+}
+
 cudaError_t set_smem_attrs(size_t row_smem, size_t mark_smem) {
-  cudaError_t e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)row_smem);
-  if (e == cudaSuccess)
+  std::lock_guard<std::mutex> lock(g_topk_state_mutex);
+  DeviceTopkState& st = g_topk_state[current_device_index()];
+  cudaError_t e = cudaSuccess;
+  if (row_smem > st.row_smem) {
+    e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)row_smem);
+    if (e == cudaSuccess) st.row_smem = row_smem;
+  }
+  if (e == cudaSuccess && mark_smem > st.mark_smem) {
     e = cudaFuncSetAttribute(long_mark_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mark_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(long_coop_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mark_smem);
+    if (e == cudaSuccess) st.mark_smem = mark_smem;
+  }
+  return e;
+}
+
+// The long-row workspace: [a barrier counter per token | one LongLayout block per token].
+size_t long_counters_bytes(int T) { return align_up((size_t)T * sizeof(uint32_t), 256); }
+
+// One launch when all of the tokens' slices can be resident at once.
+bool long_coop_fits(int T, int P, size_t smem) {
+  int nb = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_topk_state_mutex);
+    DeviceTopkState& st = g_topk_state[current_device_index()];
+    if (st.occ_blocks < 0 || st.occ_smem != smem) {
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, long_coop_kernel, kThreads, smem) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+      }
+      st.occ_smem = smem;
+      st.occ_blocks = nb;
+    }
+    nb = st.occ_blocks;
+  }
+  return (long long)nb * device_sm_count() >= (long long)T * P;
+}
+
+cudaError_t launch_long_coop(KParams& p, cudaStream_t st, size_t smem) {
+  cudaError_t e = cudaMemsetAsync(p.gbar, 0, (size_t)p.T * sizeof(uint32_t), st);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.nslice, p.T);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, long_coop_kernel, p);
+  count_launch();
   return e;
 }
 
@@ -898,7 +1204,7 @@ cudaError_t launch_long(KParams& p, cudaStream_t st, size_t mark_smem) {
 size_t topk_workspace_bytes(int T, int S, int k_top) {
   (void)k_top;
   if (long_slices(T, S) <= 1) return 0;
-  return (size_t)T * long_layout(S).total;
+  return long_counters_bytes(T) + (size_t)T * long_layout(S).total;
 }
 
 int launch_topk(const TopkArgs& a, cudaStream_t stream) {
@@ -919,6 +1225,7 @@ int launch_topk(const TopkArgs& a, cudaStream_t stream) {
   p.counts = a.counts;
   p.nslice = long_slices(a.T, a.S);
   p.long_ws = nullptr;
+  p.gbar = nullptr;
   p.status = device_status_ptr();
   if (p.nslice <= 1) {
     if (launch_pdl(topk_row_kernel, dim3(a.T), dim3(kThreads), smem, stream, p) != cudaSuccess) return DS4X_ERR_CUDA;
@@ -926,8 +1233,11 @@ int launch_topk(const TopkArgs& a, cudaStream_t stream) {
   } else {
     const size_t need = topk_workspace_bytes(a.T, a.S, a.k_top);
     if (a.workspace == nullptr || a.workspace_bytes < need) return DS4X_ERR_WORKSPACE;
-    p.long_ws = static_cast<uint8_t*>(a.workspace);
-    if (launch_long(p, stream, msmem) != cudaSuccess) return DS4X_ERR_CUDA;
+    p.gbar = static_cast<uint32_t*>(a.workspace);
+    p.long_ws = static_cast<uint8_t*>(a.workspace) + long_counters_bytes(a.T);
+    const cudaError_t e = long_coop_fits(a.T, p.nslice, msmem) ? launch_long_coop(p, stream, msmem)
+                                                             : launch_long(p, stream, msmem);
+    if (e != cudaSuccess) return DS4X_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? DS4X_OK : DS4X_ERR_CUDA;
 }
@@ -1001,6 +1311,7 @@ extern "C" int ds4x_topk_static_scratch(const float* scores, int64_t ld_scores, 
   p.counts = counts;
   p.nslice = long_slices(T, S);
   p.long_ws = nullptr;
+  p.gbar = nullptr;
   p.status = device_status_ptr();
   cudaError_t e;
   if (p.nslice <= 1) {
@@ -1008,8 +1319,9 @@ extern "C" int ds4x_topk_static_scratch(const float* scores, int64_t ld_scores, 
   } else {
     // the first launch zeroes every counter, histogram and bitmap the later ones read, so
     // nothing left in the array by an earlier call is ever read
-    p.long_ws = static_cast<uint8_t*>(scratch);
-    e = launch_long(p, st, msmem);
+    p.gbar = static_cast<uint32_t*>(scratch);
+    p.long_ws = static_cast<uint8_t*>(scratch) + long_counters_bytes(T);
+    e = long_coop_fits(T, p.nslice, msmem) ? launch_long_coop(p, st, msmem) : launch_long(p, st, msmem);
   }
   return e == cudaSuccess ? DS4X_OK : DS4X_ERR_CUDA;
 }
