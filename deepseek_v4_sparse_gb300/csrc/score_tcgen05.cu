@@ -9,18 +9,24 @@
 // tiles feeding tcgen05.mma, with a q tile resident across a run of k tiles and the
 // accumulator in TMEM.  The full T x H x S product never leaves the SM.
 //
-// Mapping (one UMMA per 16-wide K step, M=128, N=256, fp16 in, fp32 accumulate):
+// Mapping (one UMMA per 16-wide K step, M=128, N=TN, fp16 in, fp32 accumulate):
 //   A = k tile    [128 rows s] x [D]       (M axis = compressed rows = TMEM lanes)
-//   B = q tile    [256 = TPT tokens x H heads] x [D]    (N axis = TMEM columns)
-//   D = TMEM      [128 lanes] x [256 columns] fp32, double-buffered (2 x 256 = 512 columns)
+//   B = q tile    [TN = TPT tokens x H heads] x [D]    (N axis = TMEM columns)
+//   D = TMEM      [128 lanes] x [TN columns] fp32, NACC buffers
 // so each epilogue thread owns one row s and reduces the H head columns of a token in its
 // own registers: relu, multiply by w[t,h] (from shared memory, broadcast), sum, mask, store.
+//
+// Two tile widths.  Wide (TN = 256, four tokens of 64 heads): prefill, where a k tile feeds
+// as many tokens as one UMMA can take.  Narrow (TN = max(64, H)): when all tokens fit in one
+// narrow tile (a decode step), so that no tensor-pipe time and no shared memory goes to
+// padding tokens: the q tile shrinks from 64 KB to 16 KB and the k pipeline deepens from 5 to
+// 11 stages, which is what a pass over a long k needs to keep enough bytes in flight.
 //
 // Warp roles (384 threads, one CTA per SM, persistent over a contiguous range of tiles):
 //   warp 0      TMA producer (one lane): q tile per token group, k tile per (group, s-tile)
 //   warp 1      MMA issuer (one lane) + TMEM allocation
-//   warps 4..11 epilogue: warp%4 selects the 32-lane TMEM quadrant, (warp-4)/4 the half of
-//               the tile's tokens
+//   warps 4..11 epilogue: warp%4 selects the 32-lane TMEM quadrant; (warp-4)/4 selects the
+//               half of each wide tile's tokens, or, for narrow tiles, every other tile
 // The k pipeline stage is one 128-row x 64-column block (16 KB) so that D=128 tiles stream
 // as two stages; q is double-buffered so that a new token group loads while the previous
 // group's MMAs drain.
@@ -35,23 +41,34 @@ namespace ds4x {
 namespace {
 
 constexpr int kTileS = 128;   // compressed rows per tile (UMMA M)
-constexpr int kTileN = 256;   // token x head columns per tile (UMMA N)
+constexpr int kTileWide = 256;  // token x head columns of a wide tile (UMMA N)
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (4 + kEpiWarps);
 constexpr int kBlockBytes = kTileS * 128;  // one k stage: 128 rows x 64 fp16
-constexpr uint32_t kTmemCols = 512;
+constexpr int kSmemBudget = 227 * 1024;
 
-template <int H, int D>
+constexpr int narrow_tile(int H) { return H > 64 ? H : 64; }
+
+template <int H, int D, int TN>
 struct Cfg {
-  static constexpr int TPT = kTileN / H;          // tokens per tile
-  static constexpr int HALF = TPT / 2;            // tokens per epilogue warp
-  static constexpr int KB = D / 64;               // 64-wide blocks along D
-  static constexpr int Q_BYTES = kTileN * D * 2;  // one q tile
-  static constexpr int QB_BYTES = kTileN * 128;   // one 64-wide block of the q tile
-  static constexpr int NK = (D == 128) ? 5 : 8;   // k stages (one 64-wide block each)
-  static constexpr int SMEM = 2 * Q_BYTES + NK * kBlockBytes + kEpiWarps * 128 * 4 + 512 + 1024;
-  static_assert(TPT >= 2 && TPT * H == kTileN, "H must divide 128");
+  static constexpr int TPT = TN / H;               // tokens per tile
+  static constexpr bool ALT = TN <= 128;           // epilogue groups take alternate tiles
+  static constexpr int TOKW = ALT ? TPT : TPT / 2; // tokens one epilogue warp reduces per tile
+  static constexpr int NACC = TN >= 256 ? 2 : 4;   // TMEM accumulator buffers
+  static constexpr uint32_t TMEM_COLS = NACC * TN; // 512, 256 or 512: a power of two
+  static constexpr int KB = D / 64;                // 64-wide blocks along D
+  static constexpr int Q_BYTES = TN * D * 2;       // one q tile
+  static constexpr int QB_BYTES = TN * 128;        // one 64-wide block of the q tile
+  static constexpr int FIXED = 2 * Q_BYTES + kEpiWarps * 128 * 4 + 512 + 1024;
+  static constexpr int NK_FIT = (kSmemBudget - FIXED) / kBlockBytes;
+  static constexpr int NK = NK_FIT < 12 ? NK_FIT : 12;  // k stages (one 64-wide block each)
+  static constexpr int SMEM = FIXED + NK * kBlockBytes;
+  static_assert(TPT >= 1 && TPT * H == TN, "H must divide the tile width");
+  static_assert(ALT || TPT % 2 == 0, "a wide tile splits its tokens over two epilogue groups");
+  static_assert(TOKW * H <= 128 && (TOKW * H) % 32 == 0, "per-warp w stage is 128 floats");
   static_assert(D % 64 == 0, "D must be a multiple of 64");
+  static_assert(NK >= 4 && SMEM <= kSmemBudget, "shared memory");
+  static_assert(TMEM_COLS <= 512, "TMEM");
 };
 
 struct Params {
@@ -106,12 +123,12 @@ __device__ __forceinline__ int group_rows(const Params& p, int g) {
   return m;
 }
 
-template <int H, int D>
+template <int H, int D, int TN>
 __global__ void __launch_bounds__(kThreads, 1)
     score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const Params p) {
-  using C = Cfg<H, D>;
-  constexpr uint32_t kIdesc = idesc_f16(kTileS, kTileN, 0, 0, 0);
+  using C = Cfg<H, D, TN>;
+  constexpr uint32_t kIdesc = idesc_f16(kTileS, TN, 0, 0, 0);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sq = smem;                                   // 2 x Q_BYTES
@@ -123,8 +140,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* qfull = kempty + C::NK;
   uint64_t* qempty = qfull + 2;
   uint64_t* afull = qempty + 2;
-  uint64_t* aempty = afull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aempty + 2);
+  uint64_t* aempty = afull + C::NACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aempty + C::NACC);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -137,8 +154,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&qfull[i], 1);
       mbar_init(&qempty[i], 1);
+    }
+    for (int i = 0; i < C::NACC; ++i) {
       mbar_init(&afull[i], 1);
-      mbar_init(&aempty[i], kEpiWarps);
+      mbar_init(&aempty[i], C::ALT ? kEpiWarps / 2 : kEpiWarps);  // the warps that read the buffer
     }
     fence_mbarrier_init();
   }
@@ -146,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -181,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&qfull[b], C::Q_BYTES);
 #pragma unroll
           for (int kb = 0; kb < C::KB; ++kb)
-            tma_load_2d(sq + b * C::Q_BYTES + kb * C::QB_BYTES, &tm_q, &qfull[b], kb * 64, g * kTileN);
+            tma_load_2d(sq + b * C::Q_BYTES + kb * C::QB_BYTES, &tm_q, &qfull[b], kb * 64, g * TN);
           ++q_it;
           started = true;
         }
@@ -223,10 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           started = true;
           tc_fence_after();
         }
-        const int ab = a_it & 1;
-        if (!mbar_wait(&aempty[ab], ((a_it >> 1) & 1) ^ 1, p.status, 4)) break;
+        const int ab = a_it % C::NACC;
+        if (!mbar_wait(&aempty[ab], ((a_it / C::NACC) & 1) ^ 1, p.status, 4)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + ab * kTileN;
+        const uint32_t d_tmem = tmem_base + ab * TN;
         const uint32_t q_addr = smem_u32(sq + qb * C::Q_BYTES);
         bool ok = true;
 #pragma unroll
@@ -253,14 +272,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // --------------------------------------------------------------------- epilogue
     const int e = warp - 4;
     const int quad = warp & 3;   // TMEM lanes 32*quad .. 32*quad+31
-    const int half = e >> 2;     // which half of the tile's tokens
+    const int grp = e >> 2;      // epilogue group
+    // first token of a tile this warp reduces: all of them for narrow tiles (the groups take
+    // alternate tiles), its group's half for wide ones
+    const int tok0 = C::ALT ? 0 : grp * C::TOKW;
     float* my_w = sw + e * 128;  // this warp's w[t, h] for its tokens, fp32
-    constexpr int WPL = (C::HALF * H) / 32;  // w values per lane per group (always 4)
+    constexpr int WPL = (C::TOKW * H) / 32;  // w values per lane per group
     // the next group's w and visibility are loaded into registers one group ahead
     float w_next[WPL];
-    int nvis_next[C::HALF];
+    int nvis_next[C::TOKW];
     auto prefetch = [&](int g) {
-      const int t0 = g * C::TPT + half * C::HALF;
+      const int t0 = g * C::TPT + tok0;
 #pragma unroll
       for (int i = 0; i < WPL; ++i) {
         const int idx = lane + 32 * i;
@@ -268,11 +290,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         w_next[i] = t < p.T ? __half2float(p.w[(int64_t)t * H + (idx % H)]) : 0.f;
       }
 #pragma unroll
-      for (int j = 0; j < C::HALF; ++j) nvis_next[j] = (t0 + j < p.T) ? n_visible(p, t0 + j) : 0;
+      for (int j = 0; j < C::TOKW; ++j) nvis_next[j] = (t0 + j < p.T) ? n_visible(p, t0 + j) : 0;
     };
     int cur_g = -1, rows = 0;
     uint32_t a_it = 0;
-    int nvis[C::HALF];
+    int nvis[C::TOKW];
     if (beg < end) prefetch((int)(beg / p.n_stiles));
     int g = (int)(beg / p.n_stiles), st = (int)(beg % p.n_stiles) - 1;
     for (long long it = beg; it < end; ++it) {
@@ -287,28 +309,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < WPL; ++i) my_w[lane + 32 * i] = w_next[i];
 #pragma unroll
-        for (int j = 0; j < C::HALF; ++j) nvis[j] = nvis_next[j];
+        for (int j = 0; j < C::TOKW; ++j) nvis[j] = nvis_next[j];
         __syncwarp();
         const long long next_group_item = (long long)(g + 1) * p.n_stiles;
         if (next_group_item < end) prefetch(g + 1);
       }
       const int row = st * kTileS + quad * 32 + lane;
-      const int t0 = g * C::TPT + half * C::HALF;
+      const int t0 = g * C::TPT + tok0;
       if (st * kTileS >= rows) {
-        if (p.write_masked && row < p.S) {
+        if (p.write_masked && row < p.S && (!C::ALT || (st & 1) == grp)) {
 #pragma unroll
-          for (int j = 0; j < C::HALF; ++j)
+          for (int j = 0; j < C::TOKW; ++j)
             if (t0 + j < p.T) p.scores[(int64_t)(t0 + j) * p.ld + row] = -INFINITY;
         }
         continue;
       }
-      const int ab = a_it & 1;
-      if (!mbar_wait(&afull[ab], (a_it >> 1) & 1, p.status, 6)) break;
+      const uint32_t my_it = a_it++;
+      if (C::ALT && (int)(my_it & 1) != grp) continue;  // the other group's tile
+      const int ab = my_it % C::NACC;
+      if (!mbar_wait(&afull[ab], (my_it / C::NACC) & 1, p.status, 6)) break;
       tc_fence_after();
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + ab * kTileN;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + ab * TN;
 #pragma unroll
-      for (int j = 0; j < C::HALF; ++j) {
-        const uint32_t col = (half * C::HALF + j) * H;
+      for (int j = 0; j < C::TOKW; ++j) {
+        const uint32_t col = (tok0 + j) * H;
         // sum_h w[h] * max(0, acc[h]): ReLU in scalar, products in packed f32x2 pairs
         uint64_t a01 = 0, a23 = 0;  // two pair accumulators (bit pattern 0 = +0.0f, +0.0f)
         constexpr int CH = H >= 32 ? 32 : H;
@@ -334,7 +358,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&aempty[ab]);
-      ++a_it;
     }
   }
 
@@ -342,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
@@ -379,18 +402,18 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int H, int D>
+template <int H, int D, int TN>
 int launch_impl(const ScoreArgs& a, cudaStream_t stream) {
-  using C = Cfg<H, D>;
+  using C = Cfg<H, D, TN>;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(score_kernel<H, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+    if (cudaFuncSetAttribute(score_kernel<H, D, TN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
         cudaSuccess)
       return DS4X_ERR_CUDA;
     attr_set = true;
   }
   CUtensorMap tq, tk;
-  if (!make_map(&tq, a.q, (uint64_t)a.T * H, D, kTileN) || !make_map(&tk, a.k, (uint64_t)a.S, D, kTileS))
+  if (!make_map(&tq, a.q, (uint64_t)a.T * H, D, TN) || !make_map(&tk, a.k, (uint64_t)a.S, D, kTileS))
     return DS4X_ERR_CUDA;
   Params p;
   p.w = static_cast<const __half*>(a.w);
@@ -408,9 +431,17 @@ int launch_impl(const ScoreArgs& a, cudaStream_t stream) {
   p.status = device_status_ptr();
   const int sms = device_sm_count();
   const int grid = (int)(p.total_items < sms ? p.total_items : sms);
-  const cudaError_t e = launch_pdl(score_kernel<H, D>, dim3(grid), dim3(kThreads), (size_t)C::SMEM, stream, tq, tk, p);
+  const cudaError_t e = launch_pdl(score_kernel<H, D, TN>, dim3(grid), dim3(kThreads), (size_t)C::SMEM, stream, tq, tk, p);
   count_launch();
   return e == cudaSuccess ? DS4X_OK : DS4X_ERR_CUDA;
+}
+
+// Narrow tiles when every token fits in one (a decode step), wide ones otherwise.
+template <int H, int D>
+int launch_shape(const ScoreArgs& a, cudaStream_t stream) {
+  constexpr int TN = narrow_tile(H);
+  if ((int64_t)a.T * H <= TN) return launch_impl<H, D, TN>(a, stream);
+  return launch_impl<H, D, kTileWide>(a, stream);
 }
 
 }  // namespace
@@ -422,7 +453,7 @@ bool score_shape_supported(int H, int D) {
 int launch_score(const ScoreArgs& a, cudaStream_t stream) {
   if (a.T == 0 || a.S == 0) return DS4X_OK;
 #define DS4X_SCORE_CASE(HH, DD) \
-  if (a.H == HH && a.D == DD) return launch_impl<HH, DD>(a, stream);
+  if (a.H == HH && a.D == DD) return launch_shape<HH, DD>(a, stream);
   DS4X_SCORE_CASE(16, 64)
   DS4X_SCORE_CASE(16, 128)
   DS4X_SCORE_CASE(32, 64)

@@ -548,6 +548,231 @@ __global__ void __launch_bounds__(kThreads) topk_row_kernel(const KParams p) {
   emit_sorted(sh, bitmap, thr, n, p.k_top, out, cnt_out);
 }
 
+// ------------------------------------------------------------- register-resident rows
+// Rows of up to B * NPT scores (prefill chunks): one CTA per token, thread i holding the ordered
+// keys of rows [i*NPT, (i+1)*NPT) in registers, read once from global memory with nothing
+// staged.  Rounds of the monotone histogram narrow the undecided rows ("candidates"): rows in
+// bins above the boundary bin are taken, rows below it dropped, and the boundary bin's rows are
+// the next round's candidates, until the boundary bin is taken whole, holds few enough rows to
+// rank directly by the composite order, or all its rows share one key (then the lowest rows
+// win, the tie rule).  A round maps the candidates' key range [lo, hi] onto NB bins (identity
+// when the range is that small), so each round shrinks the range by that factor: at most four
+// rounds for 32-bit keys and 2048 bins, eight for 256.  The selected rows are written in ascending order by one
+// block scan.  The result is the same set as every other path's: the composite order is total.
+constexpr int kRegRank = 256;   // boundary bins of up to this many rows are ranked directly
+constexpr int kRegRounds = 12;  // more than a 32-bit key range can need with 256 bins or more
+
+template <int NB>
+struct RegShared {
+  uint32_t bins[NB];
+  uint32_t wmin[32], wmax[32], wsum[32];
+  uint64_t cand[kRegRank];
+  uint64_t cthr;
+  uint32_t ncand, bstar, above, cntb;
+};
+
+// Block min / max (one barrier; the caller keeps wmin / wmax unwritten until every thread has
+// passed a later barrier).
+template <int B, class Sh>
+__device__ __forceinline__ void reg_minmax(uint32_t mn, uint32_t mx, Sh& sh, uint32_t& omin, uint32_t& omax) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  if (lane == 0) {
+    sh.wmin[warp] = mn;
+    sh.wmax[warp] = mx;
+  }
+  __syncthreads();
+  // every warp reduces the per-warp values itself: one shared load a lane, then shuffles
+  mn = lane < B / 32 ? sh.wmin[lane] : 0xFFFFFFFFu;
+  mx = lane < B / 32 ? sh.wmax[lane] : 0u;
+#pragma unroll
+  for (int o = B / 64; o > 0; o >>= 1) {
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  omin = __shfl_sync(0xffffffffu, mn, 0);  // lanes past the warp count reduced only identities
+  omax = __shfl_sync(0xffffffffu, mx, 0);
+}
+
+// Inclusive block scan (one barrier; same rule for wsum).
+template <int B, class Sh>
+__device__ __forceinline__ uint32_t reg_scan(uint32_t v, Sh& sh, uint32_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
+  }
+  if (lane == 31) sh.wsum[warp] = v;
+  __syncthreads();
+  // every warp scans the per-warp totals itself: one shared load a lane, then shuffles
+  uint32_t x = lane < B / 32 ? sh.wsum[lane] : 0u;
+#pragma unroll
+  for (int o = 1; o < B / 32; o <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += u;
+  }
+  total = __shfl_sync(0xffffffffu, x, B / 32 - 1);
+  const uint32_t upto = __shfl_sync(0xffffffffu, x, warp);  // totals of warps 0..warp
+  return v + upto - __shfl_sync(0xffffffffu, v, 31);
+}
+
+template <int B, int NPT, int NB>
+__global__ void __launch_bounds__(B) topk_reg_kernel(const KParams p) {
+  static_assert(B % 32 == 0 && B <= 1024 && NB % B == 0 && NB >= 256 && NPT % 4 == 0 && NPT <= 32, "shape");
+  pdl_wait();
+  pdl_trigger();
+  __shared__ RegShared<NB> sh;
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const int n = n_visible(p.positions, t, p.ratio, p.S);
+  int32_t* out = p.indices + (int64_t)t * p.k_top;
+  int32_t* cnt_out = p.counts ? p.counts + t : nullptr;
+  if (n <= p.k_top) {
+    for (int i = tid; i < p.k_top; i += B) out[i] = i < n ? i : -1;
+    if (cnt_out && tid == 0) *cnt_out = n;
+    return;
+  }
+  const float* row = p.scores + (int64_t)t * p.ld;
+  const int r0 = tid * NPT;
+  uint32_t key[NPT];
+  uint32_t cand = 0;  // bit i: row r0 + i is undecided
+  if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0 && r0 + NPT <= n) {
+#pragma unroll
+    for (int v = 0; v < NPT / 4; ++v) {
+      const float4 x = __ldcs(reinterpret_cast<const float4*>(row + r0) + v);
+      key[4 * v] = ordered_key(x.x);
+      key[4 * v + 1] = ordered_key(x.y);
+      key[4 * v + 2] = ordered_key(x.z);
+      key[4 * v + 3] = ordered_key(x.w);
+    }
+    cand = NPT == 32 ? 0xFFFFFFFFu : ((1u << NPT) - 1u);
+  } else {
+#pragma unroll
+    for (int i = 0; i < NPT; ++i) {
+      const bool valid = r0 + i < n;
+      key[i] = valid ? ordered_key(__ldcs(row + r0 + i)) : 0u;
+      cand |= valid ? (1u << i) : 0u;
+    }
+  }
+  uint32_t sel = 0;
+  int need = p.k_top;
+  for (int i = tid; i < NB; i += B) sh.bins[i] = 0;
+  bool done = false;
+  for (int round = 0; round < kRegRounds && !done; ++round) {
+    uint32_t mn = 0xFFFFFFFFu, mx = 0;
+#pragma unroll
+    for (int i = 0; i < NPT; ++i)
+      if ((cand >> i) & 1u) {
+        mn = min(mn, key[i]);
+        mx = max(mx, key[i]);
+      }
+    uint32_t lo, hi;
+    reg_minmax<B>(mn, mx, sh, lo, hi);  // its barrier also orders the bins' zeroing
+    if (lo == hi) {
+      // one key left: the need lowest candidate rows win
+      const uint32_t c = __popc(cand);
+      uint32_t total;
+      uint32_t rank = reg_scan<B>(c, sh, total) - c;
+#pragma unroll
+      for (int i = 0; i < NPT; ++i)
+        if ((cand >> i) & 1u) {
+          if ((int)rank < need) sel |= 1u << i;
+          ++rank;
+        }
+      done = true;
+      break;
+    }
+    const uint64_t range = (uint64_t)(hi - lo) + 1u;
+    const bool ident = range <= (uint64_t)NB;
+    const uint32_t mult = ident ? 0u : (uint32_t)(((uint64_t)NB << 32) / range);
+#pragma unroll
+    for (int i = 0; i < NPT; ++i)
+      if ((cand >> i) & 1u) {
+        const uint32_t d = key[i] - lo;
+        atomicAdd(&sh.bins[ident ? d : __umulhi(d, mult)], 1u);
+      }
+    __syncthreads();
+    // boundary bin, counted from the top: thread tid owns bins [NB - BPT(tid+1), NB - BPT tid)
+    constexpr int BPT = NB / B;
+    const int b_hi = NB - BPT * tid;
+    uint32_t mine = 0;
+#pragma unroll
+    for (int q = 0; q < BPT; ++q) mine += sh.bins[b_hi - 1 - q];
+    uint32_t total;
+    uint32_t above = reg_scan<B>(mine, sh, total) - mine;
+#pragma unroll 4
+    for (int q = 0; q < BPT; ++q) {
+      const uint32_t c = sh.bins[b_hi - 1 - q];
+      if (above < (uint32_t)need && above + c >= (uint32_t)need) {
+        sh.bstar = (uint32_t)(b_hi - 1 - q);
+        sh.above = above;
+        sh.cntb = c;
+      }
+      above += c;
+    }
+    if (tid == 0) sh.ncand = 0;
+    __syncthreads();
+    const uint32_t bstar = sh.bstar;
+    const int cntb = (int)sh.cntb;
+    need -= (int)sh.above;
+    uint32_t inb = 0;
+#pragma unroll
+    for (int i = 0; i < NPT; ++i)
+      if ((cand >> i) & 1u) {
+        const uint32_t d = key[i] - lo;
+        const uint32_t b = ident ? d : __umulhi(d, mult);
+        if (b > bstar) sel |= 1u << i;
+        else if (b == bstar) inb |= 1u << i;
+      }
+    cand = inb;
+    if (cntb == need) {  // the boundary bin is taken whole
+      sel |= cand;
+      done = true;
+      break;
+    }
+    if (cntb <= kRegRank) {
+      // rank the boundary bin's rows directly: the need-th largest composite is the threshold
+#pragma unroll
+      for (int i = 0; i < NPT; ++i)
+        if ((cand >> i) & 1u) sh.cand[atomicAdd(&sh.ncand, 1u)] = composite(key[i], (uint32_t)(r0 + i));
+      __syncthreads();
+      for (int j = tid; j < cntb; j += B) {
+        const uint64_t cj = sh.cand[j];
+        int greater = 0;
+        for (int m = 0; m < cntb; ++m) greater += sh.cand[m] > cj ? 1 : 0;
+        if (greater == need - 1) sh.cthr = cj;
+      }
+      __syncthreads();
+      const uint64_t cthr = sh.cthr;
+#pragma unroll
+      for (int i = 0; i < NPT; ++i)
+        if (((cand >> i) & 1u) && composite(key[i], (uint32_t)(r0 + i)) >= cthr) sel |= 1u << i;
+      done = true;
+      break;
+    }
+    // next round on the boundary bin's rows
+    __syncthreads();  // every thread has read the bins and the broadcast values
+    for (int i = tid; i < NB; i += B) sh.bins[i] = 0;
+  }
+  if (!done) {  // cannot happen (each round shrinks the key range by NB); reported, not hidden
+    if (tid == 0) report_timeout(p.status, 60);
+    return;
+  }
+  __syncthreads();  // wsum is rewritten below
+  const uint32_t c = __popc(sel);
+  uint32_t total;
+  int pos = (int)(reg_scan<B>(c, sh, total) - c);
+#pragma unroll
+  for (int i = 0; i < NPT; ++i)
+    if ((sel >> i) & 1u) out[pos++] = r0 + i;
+  for (int i = (int)total + tid; i < p.k_top; i += B) out[i] = -1;
+  if (cnt_out && tid == 0) *cnt_out = (int)total;
+}
+
 // ---------------------------------------------------------------------------- long rows
 // A token's row is spread over P = ceil(S / kSliceRows) CTAs, one slice each, in three launches
 // that run the histogram scheme of the staged path across the grid:
@@ -1199,6 +1424,16 @@ cudaError_t launch_long(KParams& p, cudaStream_t st, size_t mark_smem) {
   return e;
 }
 
+// One CTA per token: rows of up to kRegMaxRows keep their keys in registers (threads x keys a
+// thread by row length), longer ones are staged in shared memory or streamed.
+constexpr int kRegMaxRows = 4096;
+cudaError_t launch_one_cta_per_token(const KParams& p, size_t row_smem, cudaStream_t st) {
+  const dim3 grid(p.T);
+  if (p.S <= 2048) return launch_pdl(topk_reg_kernel<128, 16, 256>, grid, dim3(128), 0, st, p);
+  if (p.S <= kRegMaxRows) return launch_pdl(topk_reg_kernel<256, 16, 2048>, grid, dim3(256), 0, st, p);
+  return launch_pdl(topk_row_kernel, grid, dim3(kThreads), row_smem, st, p);
+}
+
 }  // namespace
 
 size_t topk_workspace_bytes(int T, int S, int k_top) {
@@ -1228,7 +1463,7 @@ int launch_topk(const TopkArgs& a, cudaStream_t stream) {
   p.gbar = nullptr;
   p.status = device_status_ptr();
   if (p.nslice <= 1) {
-    if (launch_pdl(topk_row_kernel, dim3(a.T), dim3(kThreads), smem, stream, p) != cudaSuccess) return DS4X_ERR_CUDA;
+    if (launch_one_cta_per_token(p, smem, stream) != cudaSuccess) return DS4X_ERR_CUDA;
     count_launch();
   } else {
     const size_t need = topk_workspace_bytes(a.T, a.S, a.k_top);
@@ -1315,7 +1550,7 @@ extern "C" int ds4x_topk_static_scratch(const float* scores, int64_t ld_scores, 
   p.status = device_status_ptr();
   cudaError_t e;
   if (p.nslice <= 1) {
-    e = launch_pdl(topk_row_kernel, dim3(T), dim3(kThreads), smem, st, p);
+    e = launch_one_cta_per_token(p, smem, st);
   } else {
     // the first launch zeroes every counter, histogram and bitmap the later ones read, so
     // nothing left in the array by an earlier call is ever read

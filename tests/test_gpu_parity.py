@@ -119,6 +119,26 @@ def test_visibility_edges(ratio):
                extra=few_rows_bound(inp.kv, g["fidx"], ref_fout, "bf16", S))
 
 
+@pytest.mark.parametrize("H,D", [(16, 64), (16, 128), (32, 64), (32, 128), (64, 64), (64, 128), (128, 64),
+                                 (128, 128)])
+def test_score_shapes_both_tile_widths(H, D):
+    # every supported indexer shape, bit-exact on integer inputs, at token counts that take the
+    # narrow tile (all tokens in max(64, H) columns: one token for H >= 64, up to 4 for H = 16)
+    # and the wide one (four 64-head tokens per tile), with a ragged row count
+    S, ratio = 1000, 1
+    narrow_tokens = max(64, H) // H
+    for T in sorted({1, narrow_tokens, narrow_tokens + 1, 9}):
+        positions = [S - 1 - 37 * t for t in range(T)]          # n_vis from 1000 down
+        raw = _edge_inputs(f"shape_{H}_{D}_{T}", positions, S, kind="int", kv_dtype="f16", H=H, D=D,
+                           w_kind="pow2")
+        d = to_device(raw)
+        scores = ds4x.indexer_score(d["q"], d["w"], d["k"], d["positions"], ratio, S=S)
+        torch.cuda.synchronize()
+        assert ds4x.device_status() == ds4x.OK
+        ref = oracle.indexer_score(raw.q, raw.w, raw.k, raw.positions, ratio, S=S)
+        check_scores(scores.cpu().numpy(), ref, raw.positions, ratio, S, exact=True)
+
+
 def test_all_equal_scores_tie_break():
     # q = 0 -> every visible score is exactly 0 -> the k lowest rows win
     S, T = 900, 5
@@ -182,6 +202,31 @@ def test_split_topk_decode_row():
     idx, cnt = ds4x.topk(torch.from_numpy(scores).cuda(), torch.from_numpy(pos).cuda(), S, 4, 512)
     torch.cuda.synchronize()
     ref_idx, ref_cnt = oracle.topk(scores, pos, S, 4, 512)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    assert np.array_equal(cnt.cpu().numpy(), ref_cnt)
+
+
+@pytest.mark.parametrize("S", [2048, 4096, 8192, 16384])
+@pytest.mark.parametrize("pad", [0, 1])
+def test_topk_one_cta_rounds_exact(S, pad):
+    # one CTA per token with the keys in registers, at every row-length class: a dense cluster of
+    # repeated adjacent floats behind two far outliers (a boundary bin of more rows than are
+    # ranked directly: a second round, then a direct rank among ties), equal scores under 100
+    # larger ones (a pure tie at the boundary), N(0,1), a ragged visible count, a row of equal
+    # scores; pad = 1 makes the row pitch odd so that most rows start unaligned
+    rng = np.random.default_rng(S + pad)
+    ld = S + pad
+    sc = rng.standard_normal((5, ld)).astype(np.float32)
+    sc[0, :S] = (np.float32(3.0).view(np.int32) + rng.integers(0, 400, S)).astype(np.int32).view(np.float32)
+    sc[0, 5], sc[0, S - 7] = -1e30, 1e30
+    sc[1, :S] = 0.5
+    sc[1, rng.choice(S, 100, replace=False)] = 1.0 + rng.random(100).astype(np.float32)
+    sc[4, :] = -2.0
+    pos = np.array([4 * S - 1, 4 * S - 1, 4 * S - 1, 4 * (S - 37) - 1, 4 * S + 100], dtype=np.int32)
+    idx, cnt = ds4x.topk(torch.from_numpy(sc).cuda(), torch.from_numpy(pos).cuda(), S, 4, 512)
+    torch.cuda.synchronize()
+    assert ds4x.device_status() == ds4x.OK
+    ref_idx, ref_cnt = oracle.topk(sc, pos, S, 4, 512)
     assert np.array_equal(idx.cpu().numpy(), ref_idx)
     assert np.array_equal(cnt.cpu().numpy(), ref_cnt)
 
