@@ -19,14 +19,19 @@
 // Two tile widths.  Wide (TN = 256, four tokens of 64 heads): prefill, where a k tile feeds
 // as many tokens as one UMMA can take.  Narrow (TN = max(64, H)): when all tokens fit in one
 // narrow tile (a decode step), so that no tensor-pipe time and no shared memory goes to
-// padding tokens: the q tile shrinks from 64 KB to 16 KB and the k pipeline deepens from 5 to
-// 11 stages, which is what a pass over a long k needs to keep enough bytes in flight.
+// padding tokens: the q tile shrinks from 64 KB to 16 KB and the k pipeline deepens from 6 to
+// 12 stages, which is what a pass over a long k needs to keep enough bytes in flight.
 //
 // Warp roles (384 threads, one CTA per SM, persistent over a contiguous range of tiles):
-//   warp 0      TMA producer (one lane): q tile per token group, k tile per (group, s-tile)
+//   warp 0      TMA producer of k tiles (one lane), one per (group, s-tile)
 //   warp 1      MMA issuer (one lane) + TMEM allocation
-//   warps 4..11 epilogue: warp%4 selects the 32-lane TMEM quadrant; (warp-4)/4 selects the
-//               half of each wide tile's tokens, or, for narrow tiles, every other tile
+//   warp 2      TMA producer of q tiles (one lane), one per token group
+//   warps 4..   epilogue, groups of four: warp%4 selects the 32-lane TMEM quadrant; the groups
+//               split a tile's tokens or, when a tile holds fewer tokens than there are
+//               groups, take turns over the tiles
+// Eight epilogue warps (two groups): the single thread issuing the products shares a scheduler
+// with two of them, and measured faster than with four (more of its issue slots are taken) or
+// one (the reduction of a tile no longer hides behind its products).
 // The k pipeline stage is one 128-row x 64-column block (16 KB) so that D=128 tiles stream
 // as two stages; q is double-buffered so that a new token group loads while the previous
 // group's MMAs drain.
@@ -43,6 +48,8 @@ namespace {
 constexpr int kTileS = 128;   // compressed rows per tile (UMMA M)
 constexpr int kTileWide = 256;  // token x head columns of a wide tile (UMMA N)
 constexpr int kEpiWarps = 8;
+constexpr int kGroups = kEpiWarps / 4;  // epilogue groups of four warps (one per TMEM quadrant)
+constexpr int kWStage = 512 / kGroups;  // floats of w staged per epilogue group
 constexpr int kThreads = 32 * (4 + kEpiWarps);
 constexpr int kBlockBytes = kTileS * 128;  // one k stage: 128 rows x 64 fp16
 constexpr int kSmemBudget = 227 * 1024;
@@ -51,21 +58,23 @@ constexpr int narrow_tile(int H) { return H > 64 ? H : 64; }
 
 template <int H, int D, int TN>
 struct Cfg {
-  static constexpr int TPT = TN / H;               // tokens per tile
-  static constexpr bool ALT = TN <= 128;           // epilogue groups take alternate tiles
-  static constexpr int TOKW = ALT ? TPT : TPT / 2; // tokens one epilogue warp reduces per tile
-  static constexpr int NACC = TN >= 256 ? 2 : 4;   // TMEM accumulator buffers
-  static constexpr uint32_t TMEM_COLS = NACC * TN; // 512, 256 or 512: a power of two
+  static constexpr int TPT = TN / H;                  // tokens per tile
+  static constexpr int SPLIT = TPT >= kGroups ? kGroups : TPT;  // epilogue groups sharing a tile's tokens
+  static constexpr int ROT = kGroups / SPLIT;         // sets of groups taking turns over tiles
+  static constexpr int TOKW = TPT / SPLIT;            // tokens one epilogue warp reduces per tile
+  static constexpr int NACC = TN >= 256 ? 2 : 512 / TN > 8 ? 8 : 512 / TN;  // TMEM accumulators
+  static constexpr uint32_t TMEM_COLS = NACC * TN;    // 512
   static constexpr int KB = D / 64;                // 64-wide blocks along D
   static constexpr int Q_BYTES = TN * D * 2;       // one q tile
   static constexpr int QB_BYTES = TN * 128;        // one 64-wide block of the q tile
-  static constexpr int FIXED = 2 * Q_BYTES + kEpiWarps * 128 * 4 + 512 + 1024;
+  static constexpr int FIXED = 2 * Q_BYTES + kGroups * kWStage * 4 + 512;  // q, w of the epilogue groups, barriers
   static constexpr int NK_FIT = (kSmemBudget - FIXED) / kBlockBytes;
   static constexpr int NK = NK_FIT < 12 ? NK_FIT : 12;  // k stages (one 64-wide block each)
   static constexpr int SMEM = FIXED + NK * kBlockBytes;
   static_assert(TPT >= 1 && TPT * H == TN, "H must divide the tile width");
-  static_assert(ALT || TPT % 2 == 0, "a wide tile splits its tokens over two epilogue groups");
-  static_assert(TOKW * H <= 128 && (TOKW * H) % 32 == 0, "per-warp w stage is 128 floats");
+  static_assert(SPLIT * ROT == kGroups && TOKW * SPLIT == TPT, "epilogue split");
+  static_assert(TOKW * H <= kWStage, "w stage of an epilogue group");
+  static_assert(NACC >= ROT, "every set of epilogue groups needs a buffer of its own");
   static_assert(D % 64 == 0, "D must be a multiple of 64");
   static_assert(NK >= 4 && SMEM <= kSmemBudget, "shared memory");
   static_assert(TMEM_COLS <= 512, "TMEM");
@@ -85,17 +94,12 @@ struct Params {
 };
 
 __device__ __forceinline__ int n_visible(const Params& p, int t) {
-  int pos = __ldg(p.positions + t);
+  const int pos = __ldg(p.positions + t);
   if (pos < 0) return 0;
-  long long n = ((long long)pos + 1) / p.ratio;
-  return n < p.S ? (int)n : p.S;
+  const uint32_t n = (uint32_t)(pos + 1u) / (uint32_t)p.ratio;  // pos + 1 <= 2^31
+  return n < (uint32_t)p.S ? (int)n : p.S;
 }
 
-// Rows a token needs scored: all visible rows, or none when the shortcut covers it.
-__device__ __forceinline__ int rows_needed(const Params& p, int t) {
-  int n = n_visible(p, t);
-  return (p.skip_k_top > 0 && n <= p.skip_k_top) ? 0 : n;
-}
 
 // Packed fp32 pairs (sm_100 family): d = a * b + c element-wise, round to nearest.
 __device__ __forceinline__ uint64_t pack_f2(float lo, float hi) {
@@ -112,16 +116,34 @@ __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
   return d;
 }
 
+// Rows a token group needs scored (the most any of its tokens needs), with the group's
+// positions loaded one group ahead: load(g + 1) when group g starts, rows() when g + 1 starts,
+// so that no role waits on global loads at a group change.
 template <int TPT>
-__device__ __forceinline__ int group_rows(const Params& p, int g) {
-  int m = 0;
-#pragma unroll 1
-  for (int j = 0; j < TPT; ++j) {
-    int t = g * TPT + j;
-    if (t < p.T) m = max(m, rows_needed(p, t));
+struct GroupRowsAhead {
+  int pos[TPT];
+  __device__ __forceinline__ void load(const Params& p, int g) {
+#pragma unroll
+    for (int j = 0; j < TPT; ++j) {
+      const long long t = (long long)g * TPT + j;
+      pos[j] = t < p.T ? __ldg(p.positions + t) : -1;
+    }
   }
-  return m;
-}
+  __device__ __forceinline__ int rows(const Params& p) const {
+    int m = 0;
+#pragma unroll
+    for (int j = 0; j < TPT; ++j) {
+      int n = 0;
+      if (pos[j] >= 0) {  // pos + 1 <= 2^31: a 32-bit unsigned division, not a 64-bit routine
+        const uint32_t v = (uint32_t)(pos[j] + 1u) / (uint32_t)p.ratio;
+        n = v < (uint32_t)p.S ? (int)v : p.S;
+      }
+      if (p.skip_k_top > 0 && n <= p.skip_k_top) n = 0;  // the shortcut covers this token
+      m = max(m, n);
+    }
+    return m;
+  }
+};
 
 template <int H, int D, int TN>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -129,19 +151,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const Params p) {
   using C = Cfg<H, D, TN>;
   constexpr uint32_t kIdesc = idesc_f16(kTileS, TN, 0, 0, 0);
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // Declared aligned (and checked) rather than rounded up through an integer: pointers derived
+  // from the array keep the shared address space, so the epilogue's w reads are LDS, not
+  // generic loads.
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {  // the 128B-swizzled tiles need a 1024-byte aligned base
+    if (threadIdx.x == 0) report_timeout(p.status, 0x7e);
+    return;
+  }
   uint8_t* sq = smem;                                   // 2 x Q_BYTES
   uint8_t* sk = sq + 2 * C::Q_BYTES;                    // NK x kBlockBytes
-  float* sw = reinterpret_cast<float*>(sk + C::NK * kBlockBytes);  // kEpiWarps x 128
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sw + kEpiWarps * 128);
+  float* sw = reinterpret_cast<float*>(sk + C::NK * kBlockBytes);  // kGroups x kWStage
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sw + kGroups * kWStage);
   uint64_t* kfull = bars;
   uint64_t* kempty = kfull + C::NK;
   uint64_t* qfull = kempty + C::NK;
   uint64_t* qempty = qfull + 2;
   uint64_t* afull = qempty + 2;
   uint64_t* aempty = afull + C::NACC;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aempty + C::NACC);
+  uint64_t* wdone = aempty + C::NACC;  // [epilogue group] its 4 warps are done with the group's w
+  uint64_t* wready = wdone + kGroups;  // [epilogue group] the next token group's w is written
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wready + kGroups);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -155,9 +185,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&qfull[i], 1);
       mbar_init(&qempty[i], 1);
     }
+    for (int i = 0; i < kGroups; ++i) {
+      mbar_init(&wdone[i], 4);
+      mbar_init(&wready[i], 1);
+    }
     for (int i = 0; i < C::NACC; ++i) {
       mbar_init(&afull[i], 1);
-      mbar_init(&aempty[i], C::ALT ? kEpiWarps / 2 : kEpiWarps);  // the warps that read the buffer
+      mbar_init(&aempty[i], C::SPLIT * 4);  // the warps that read the buffer
     }
     fence_mbarrier_init();
   }
@@ -176,13 +210,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long beg = (long long)blockIdx.x * p.total_items / gridDim.x;
   const long long end = (long long)(blockIdx.x + 1) * p.total_items / gridDim.x;
 
+  // Every role walks the same (group, s-tile) sequence; a group's q tile is loaded (and waited
+  // for) before its first tile that is not past every token's visibility.
   if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------- TMA producer: k tiles
     if (lane == 0) {
       int cur_g = -1, rows = 0;
-      bool started = false;
-      uint32_t q_it = 0, k_it = 0;
+      int ks = 0;          // k stage
+      uint32_t kph = 0;    // its phase
       int g = (int)(beg / p.n_stiles), st = (int)(beg % p.n_stiles) - 1;
+      GroupRowsAhead<C::TPT> ahead;
+      ahead.load(p, g);  // the first group of the range
       for (long long it = beg; it < end; ++it) {
         if (++st == p.n_stiles) {
           st = 0;
@@ -190,39 +228,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (g != cur_g) {
           cur_g = g;
-          rows = group_rows<C::TPT>(p, g);
-          started = false;
+          rows = ahead.rows(p);
+          ahead.load(p, g + 1);
         }
         if (st * kTileS >= rows) continue;
-        if (!started) {
-          const int b = q_it & 1;
-          if (!mbar_wait(&qempty[b], ((q_it >> 1) & 1) ^ 1, p.status, 1)) break;
-          mbar_arrive_expect_tx(&qfull[b], C::Q_BYTES);
-#pragma unroll
-          for (int kb = 0; kb < C::KB; ++kb)
-            tma_load_2d(sq + b * C::Q_BYTES + kb * C::QB_BYTES, &tm_q, &qfull[b], kb * 64, g * TN);
-          ++q_it;
-          started = true;
-        }
         bool ok = true;
 #pragma unroll
         for (int kb = 0; kb < C::KB; ++kb) {
-          const int s = k_it % C::NK;
-          if (!mbar_wait(&kempty[s], ((k_it / C::NK) & 1) ^ 1, p.status, 2)) { ok = false; break; }
-          mbar_arrive_expect_tx(&kfull[s], kBlockBytes);
-          tma_load_2d(sk + s * kBlockBytes, &tm_k, &kfull[s], kb * 64, st * kTileS);
-          ++k_it;
+          if (!mbar_wait(&kempty[ks], kph ^ 1, p.status, 2)) { ok = false; break; }
+          mbar_arrive_expect_tx(&kfull[ks], kBlockBytes);
+          tma_load_2d(sk + ks * kBlockBytes, &tm_k, &kfull[ks], kb * 64, st * kTileS);
+          if (++ks == C::NK) {
+            ks = 0;
+            kph ^= 1;
+          }
         }
         if (!ok) break;
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------- MMA issuer
+  } else if (warp == 2) {
+    // ------------------------------------------------------------- TMA producer: q tiles
+    // On a warp of its own, so that the next group's q tile loads as soon as its buffer is
+    // free (when the group before the current one has finished), not only when the k
+    // producer reaches that group a few stages ahead of the products.
     if (lane == 0) {
-      int cur_g = -1, rows = 0, qb = -1;
+      int cur_g = -1, rows = 0;
       bool started = false;
-      uint32_t q_it = 0, k_it = 0, a_it = 0;
+      uint32_t q_it = 0;
       int g = (int)(beg / p.n_stiles), st = (int)(beg % p.n_stiles) - 1;
+      GroupRowsAhead<C::TPT> ahead;
+      ahead.load(p, g);  // the first group of the range
       for (long long it = beg; it < end; ++it) {
         if (++st == p.n_stiles) {
           st = 0;
@@ -230,7 +265,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (g != cur_g) {
           cur_g = g;
-          rows = group_rows<C::TPT>(p, g);
+          rows = ahead.rows(p);
+          ahead.load(p, g + 1);
+          started = false;
+        }
+        if (started || st * kTileS >= rows) continue;
+        const int b = q_it & 1;
+        if (!mbar_wait(&qempty[b], ((q_it >> 1) & 1) ^ 1, p.status, 1)) break;
+        mbar_arrive_expect_tx(&qfull[b], C::Q_BYTES);
+#pragma unroll
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_2d(sq + b * C::Q_BYTES + kb * C::QB_BYTES, &tm_q, &qfull[b], kb * 64, g * TN);
+        ++q_it;
+        started = true;
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------- MMA issuer
+    // Lean between products: its scheduler is shared with four epilogue warps that wake up
+    // when a tile completes, so descriptors are built once and offset by constants, and the
+    // stage / buffer indices are running counters.
+    if (lane == 0) {
+      // descriptor address field = byte address >> 4 (bits 0..13); offsets below never carry out
+      const uint64_t adesc0 = desc_sw128(smem_u32(sk), 16, 1024);
+      const uint64_t bdesc0 = desc_sw128(smem_u32(sq), 16, 1024);
+      int cur_g = -1, rows = 0, qb = -1;
+      bool started = false;
+      uint32_t q_it = 0;
+      int ks = 0, ab = 0;
+      uint32_t kph = 0, aph = 0;
+      int g = (int)(beg / p.n_stiles), st = (int)(beg % p.n_stiles) - 1;
+      GroupRowsAhead<C::TPT> ahead;
+      ahead.load(p, g);  // the first group of the range
+      for (long long it = beg; it < end; ++it) {
+        if (++st == p.n_stiles) {
+          st = 0;
+          ++g;
+        }
+        if (g != cur_g) {
+          cur_g = g;
+          rows = ahead.rows(p);
+          ahead.load(p, g + 1);
           started = false;
         }
         if (st * kTileS >= rows) continue;
@@ -242,42 +317,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           started = true;
           tc_fence_after();
         }
-        const int ab = a_it % C::NACC;
-        if (!mbar_wait(&aempty[ab], ((a_it / C::NACC) & 1) ^ 1, p.status, 4)) break;
+        if (!mbar_wait(&aempty[ab], aph ^ 1, p.status, 4)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + ab * TN;
-        const uint32_t q_addr = smem_u32(sq + qb * C::Q_BYTES);
+        const uint64_t bq = bdesc0 + (uint64_t)((qb * C::Q_BYTES) >> 4);
         bool ok = true;
 #pragma unroll
         for (int kb = 0; kb < C::KB; ++kb) {
-          const int s = k_it % C::NK;
-          if (!mbar_wait(&kfull[s], (k_it / C::NK) & 1, p.status, 5)) { ok = false; break; }
+          if (!mbar_wait(&kfull[ks], kph, p.status, 5)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(sk + s * kBlockBytes);
+          const uint64_t a0 = adesc0 + (uint64_t)((ks * kBlockBytes) >> 4);
+          const uint64_t b0 = bq + (uint64_t)((kb * C::QB_BYTES) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t adesc = desc_sw128(a_addr + kk * 32, 16, 1024);
-            const uint64_t bdesc = desc_sw128(q_addr + kb * C::QB_BYTES + kk * 32, 16, 1024);
-            tc_mma_f16(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0);
+          for (int kk = 0; kk < 4; ++kk)  // 16 columns = 32 bytes = 2 address units per step
+            tc_mma_f16(d_tmem, a0 + 2 * kk, b0 + 2 * kk, kIdesc, (kb | kk) != 0);
+          tc_commit(&kempty[ks]);  // k stage is free once these MMAs complete
+          if (++ks == C::NK) {
+            ks = 0;
+            kph ^= 1;
           }
-          tc_commit(&kempty[s]);  // k stage is free once these MMAs complete
-          ++k_it;
         }
         if (!ok) break;
         tc_commit(&afull[ab]);
-        ++a_it;
+        if (++ab == C::NACC) {
+          ab = 0;
+          aph ^= 1;
+        }
       }
     }
   } else if (warp >= 4) {
     // --------------------------------------------------------------------- epilogue
     const int e = warp - 4;
-    const int quad = warp & 3;   // TMEM lanes 32*quad .. 32*quad+31
-    const int grp = e >> 2;      // epilogue group
-    // first token of a tile this warp reduces: all of them for narrow tiles (the groups take
-    // alternate tiles), its group's half for wide ones
-    const int tok0 = C::ALT ? 0 : grp * C::TOKW;
-    float* my_w = sw + e * 128;  // this warp's w[t, h] for its tokens, fp32
-    constexpr int WPL = (C::TOKW * H) / 32;  // w values per lane per group
+    const int quad = warp & 3;             // TMEM lanes 32*quad .. 32*quad+31
+    const int grp = e >> 2;                // epilogue group 0..kGroups-1
+    const int set = grp / C::SPLIT;        // the tiles of this group: the set's turns
+    const int tok0 = (grp % C::SPLIT) * C::TOKW;  // first token of a tile this warp reduces
+    float* my_w = sw + grp * kWStage;      // the group's w[t, h] for its tokens, fp32 (shared by its 4 warps)
+    constexpr int NW = C::TOKW * H;        // w values a warp holds per token group
+    constexpr int WPL = (NW + 31) / 32;    // ... per lane
     // the next group's w and visibility are loaded into registers one group ahead
     float w_next[WPL];
     int nvis_next[C::TOKW];
@@ -287,16 +364,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < WPL; ++i) {
         const int idx = lane + 32 * i;
         const int t = t0 + idx / H;
-        w_next[i] = t < p.T ? __half2float(p.w[(int64_t)t * H + (idx % H)]) : 0.f;
+        w_next[i] = (idx < NW && t < p.T) ? __half2float(p.w[(int64_t)t * H + (idx % H)]) : 0.f;
       }
 #pragma unroll
       for (int j = 0; j < C::TOKW; ++j) nvis_next[j] = (t0 + j < p.T) ? n_visible(p, t0 + j) : 0;
     };
     int cur_g = -1, rows = 0;
-    uint32_t a_it = 0;
+    uint32_t a_it = 0, gc = 0;  // gc: group changes so far (the w barriers' phase)
     int nvis[C::TOKW];
     if (beg < end) prefetch((int)(beg / p.n_stiles));
     int g = (int)(beg / p.n_stiles), st = (int)(beg % p.n_stiles) - 1;
+    GroupRowsAhead<C::TPT> ahead;
+    ahead.load(p, g);  // the first group of the range
     for (long long it = beg; it < end; ++it) {
       if (++st == p.n_stiles) {
         st = 0;
@@ -304,20 +383,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (g != cur_g) {
         cur_g = g;
-        rows = group_rows<C::TPT>(p, g);
+        rows = ahead.rows(p);
+        ahead.load(p, g + 1);
+        // one copy of w per epilogue group: its 4 warps say they are done with the previous
+        // token group's, its first warp waits for that, writes the new one and says so
         __syncwarp();
+        if (lane == 0) mbar_arrive(&wdone[grp]);
+        if (quad == 0) {
+          if (!mbar_wait(&wdone[grp], gc & 1, p.status, 7)) break;
 #pragma unroll
-        for (int i = 0; i < WPL; ++i) my_w[lane + 32 * i] = w_next[i];
+          for (int i = 0; i < WPL; ++i)
+            if (lane + 32 * i < NW) my_w[lane + 32 * i] = w_next[i];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&wready[grp]);
+        }
+        if (!mbar_wait(&wready[grp], gc & 1, p.status, 8)) break;
+        ++gc;
 #pragma unroll
         for (int j = 0; j < C::TOKW; ++j) nvis[j] = nvis_next[j];
-        __syncwarp();
         const long long next_group_item = (long long)(g + 1) * p.n_stiles;
         if (next_group_item < end) prefetch(g + 1);
       }
       const int row = st * kTileS + quad * 32 + lane;
       const int t0 = g * C::TPT + tok0;
       if (st * kTileS >= rows) {
-        if (p.write_masked && row < p.S && (!C::ALT || (st & 1) == grp)) {
+        if (p.write_masked && row < p.S && (st % C::ROT) == set) {
 #pragma unroll
           for (int j = 0; j < C::TOKW; ++j)
             if (t0 + j < p.T) p.scores[(int64_t)(t0 + j) * p.ld + row] = -INFINITY;
@@ -325,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const uint32_t my_it = a_it++;
-      if (C::ALT && (int)(my_it & 1) != grp) continue;  // the other group's tile
+      if ((int)(my_it % C::ROT) != set) continue;  // another set's tile
       const int ab = my_it % C::NACC;
       if (!mbar_wait(&afull[ab], (my_it / C::NACC) & 1, p.status, 6)) break;
       tc_fence_after();
@@ -335,15 +425,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t col = (tok0 + j) * H;
         // sum_h w[h] * max(0, acc[h]): ReLU in scalar, products in packed f32x2 pairs
         uint64_t a01 = 0, a23 = 0;  // two pair accumulators (bit pattern 0 = +0.0f, +0.0f)
-        constexpr int CH = H >= 32 ? 32 : H;
+        constexpr int CW = H < 32 ? H : 32;  // columns read per TMEM wait (register budget)
 #pragma unroll
-        for (int c = 0; c < H; c += CH) {
-          float v[CH];
-          if constexpr (CH == 32) tmem_ld32(t_row + col + c, v);
-          else tmem_ld16(t_row + col + c, v);
+        for (int c = 0; c < H; c += CW) {
+          float v[CW];
+          if constexpr (CW == 64) {
+            tmem_ld32(t_row + col + c, *reinterpret_cast<float(*)[32]>(&v[0]));
+            tmem_ld32(t_row + col + c + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
+          } else if constexpr (CW == 32) {
+            tmem_ld32(t_row + col + c, v);
+          } else {
+            tmem_ld16(t_row + col + c, v);
+          }
           tc_wait_ld();
 #pragma unroll
-          for (int h = 0; h < CH; h += 4) {
+          for (int h = 0; h < CW; h += 4) {
             const float4 w4 = *reinterpret_cast<const float4*>(&my_w[j * H + c + h]);
             a01 = ffma2(pack_f2(w4.x, w4.y), pack_f2(fmaxf(v[h], 0.f), fmaxf(v[h + 1], 0.f)), a01);
             a23 = ffma2(pack_f2(w4.z, w4.w), pack_f2(fmaxf(v[h + 2], 0.f), fmaxf(v[h + 3], 0.f)), a23);

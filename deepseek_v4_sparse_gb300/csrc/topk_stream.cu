@@ -523,7 +523,7 @@ struct KParams {
 __global__ void __launch_bounds__(kThreads) topk_row_kernel(const KParams p) {
   pdl_wait();
   pdl_trigger();
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(16) uint8_t smem_raw[];
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem_raw + sizeof(Shared));
   const int t = blockIdx.x;
@@ -536,8 +536,9 @@ __global__ void __launch_bounds__(kThreads) topk_row_kernel(const KParams p) {
   }
   const float* row = p.scores + (int64_t)t * p.ld;
   if (p.S <= kStageMax) {
-    float* srow = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(bitmap + (p.S + 31) / 32) + 15) &
-                                           ~uintptr_t(15));
+    // offsets from the (16-byte aligned) base, so that srow stays a shared-space pointer
+    const size_t srow_off = (sizeof(Shared) + (size_t)((p.S + 31) / 32) * sizeof(uint32_t) + 15) & ~size_t(15);
+    float* srow = reinterpret_cast<float*>(smem_raw + srow_off);
     __shared__ uint64_t row_bar;
     if (!stage_row(row, n, srow, &row_bar, p.status)) return;
     if (topk_row_hist(sh, bitmap, srow, n, p.k_top, out, cnt_out)) return;
