@@ -139,6 +139,22 @@ def test_score_shapes_both_tile_widths(H, D):
         check_scores(scores.cpu().numpy(), ref, raw.positions, ratio, S, exact=True)
 
 
+def test_score_work_split_sparse_tiles():
+    # the scorer splits its items over CTAs by the tiles that are scored: here far fewer than
+    # there are CTAs, after leading token groups that see nothing (their rows are written -inf
+    # by whichever CTA holds them), with groups of differing widths in between
+    S, ratio = 3000, 4
+    nv = [0] * 21 + [5, 130, 0, 700, 1, 2999, 3000, 64, 0, 256, 257]
+    positions = [n * ratio - 1 if n > 0 else -1 for n in nv]
+    raw = _edge_inputs("score_split", positions, S, kind="int", kv_dtype="f16", w_kind="pow2")
+    d = to_device(raw)
+    scores = ds4x.indexer_score(d["q"], d["w"], d["k"], d["positions"], ratio, S=S)
+    torch.cuda.synchronize()
+    assert ds4x.device_status() == ds4x.OK
+    ref = oracle.indexer_score(raw.q, raw.w, raw.k, raw.positions, ratio, S=S)
+    check_scores(scores.cpu().numpy(), ref, raw.positions, ratio, S, exact=True)
+
+
 def test_all_equal_scores_tie_break():
     # q = 0 -> every visible score is exactly 0 -> the k lowest rows win
     S, T = 900, 5
