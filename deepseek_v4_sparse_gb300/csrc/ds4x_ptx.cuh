@@ -106,6 +106,32 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// Whole-warp forms: called by all 32 lanes of a converged warp, executed by one elected lane.
+// Keeping the issuing warp converged lets its loop-invariant operands (tensor map, barrier and
+// descriptor addresses) live in uniform registers instead of being moved there per instruction.
+__device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_elect(void* smem_dst, const CUtensorMap* map, uint64_t* bar,
+                                                  int32_t x, int32_t y) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];\n\t}" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+// A bounded wait whose outcome is the same in every lane of the (converged) warp.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* status, int site) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, site));
+}
+
 // --------------------------------------------------------------------------------- tcgen05
 // TMEM allocation (whole warp). The allocated base address is written to *dst (smem).
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {

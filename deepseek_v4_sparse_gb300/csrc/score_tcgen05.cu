@@ -23,9 +23,10 @@
 // 12 stages, which is what a pass over a long k needs to keep enough bytes in flight.
 //
 // Warp roles (384 threads, one CTA per SM, persistent over a contiguous range of tiles):
-//   warp 0      TMA producer of k tiles (one lane), one per (group, s-tile)
-//   warp 1      MMA issuer (one lane) + TMEM allocation
-//   warp 2      TMA producer of q tiles (one lane), one per token group
+//   warp 0      TMA producer of k tiles, one per (group, s-tile)
+//   warp 1      MMA issuer + TMEM allocation
+//   warp 2      TMA producer of q tiles, one per token group
+//   (each a converged warp issuing through one elected lane)
 //   warps 4..   epilogue, groups of four: warp%4 selects the 32-lane TMEM quadrant; the groups
 //               split a tile's tokens or, when a tile holds fewer tokens than there are
 //               groups, take turns over the tiles
@@ -67,7 +68,8 @@ struct Cfg {
   static constexpr int KB = D / 64;                // 64-wide blocks along D
   static constexpr int Q_BYTES = TN * D * 2;       // one q tile
   static constexpr int QB_BYTES = TN * 128;        // one 64-wide block of the q tile
-  static constexpr int FIXED = 2 * Q_BYTES + kGroups * kWStage * 4 + 512;  // q, w of the epilogue groups, barriers
+  static constexpr int NQ = 2;                        // q tile buffers
+  static constexpr int FIXED = NQ * Q_BYTES + kGroups * kWStage * 4 + 512;  // q, w of the epilogue groups, barriers
   static constexpr int NK_FIT = (kSmemBudget - FIXED) / kBlockBytes;
   static constexpr int NK = NK_FIT < 12 ? NK_FIT : 12;  // k stages (one 64-wide block each)
   static constexpr int SMEM = FIXED + NK * kBlockBytes;
@@ -160,14 +162,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   uint8_t* sq = smem;                                   // 2 x Q_BYTES
-  uint8_t* sk = sq + 2 * C::Q_BYTES;                    // NK x kBlockBytes
+  uint8_t* sk = sq + C::NQ * C::Q_BYTES;                // NK x kBlockBytes
   float* sw = reinterpret_cast<float*>(sk + C::NK * kBlockBytes);  // kGroups x kWStage
   uint64_t* bars = reinterpret_cast<uint64_t*>(sw + kGroups * kWStage);
   uint64_t* kfull = bars;
   uint64_t* kempty = kfull + C::NK;
   uint64_t* qfull = kempty + C::NK;
-  uint64_t* qempty = qfull + 2;
-  uint64_t* afull = qempty + 2;
+  uint64_t* qempty = qfull + C::NQ;
+  uint64_t* afull = qempty + C::NQ;
   uint64_t* aempty = afull + C::NACC;
   uint64_t* wdone = aempty + C::NACC;  // [epilogue group] its 4 warps are done with the group's w
   uint64_t* wready = wdone + kGroups;  // [epilogue group] the next token group's w is written
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&kfull[i], 1);
       mbar_init(&kempty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::NQ; ++i) {
       mbar_init(&qfull[i], 1);
       mbar_init(&qempty[i], 1);
     }
@@ -214,135 +216,130 @@ __global__ void __launch_bounds__(kThreads, 1)
   // for) before its first tile that is not past every token's visibility.
   if (warp == 0) {
     // ------------------------------------------------------------- TMA producer: k tiles
-    if (lane == 0) {
-      int cur_g = -1, rows = 0;
-      int ks = 0;          // k stage
-      uint32_t kph = 0;    // its phase
-      int g = (int)(beg / p.n_stiles), st = (int)(beg % p.n_stiles) - 1;
-      GroupRowsAhead<C::TPT> ahead;
-      ahead.load(p, g);  // the first group of the range
-      for (long long it = beg; it < end; ++it) {
-        if (++st == p.n_stiles) {
-          st = 0;
-          ++g;
-        }
-        if (g != cur_g) {
-          cur_g = g;
-          rows = ahead.rows(p);
-          ahead.load(p, g + 1);
-        }
-        if (st * kTileS >= rows) continue;
-        bool ok = true;
-#pragma unroll
-        for (int kb = 0; kb < C::KB; ++kb) {
-          if (!mbar_wait(&kempty[ks], kph ^ 1, p.status, 2)) { ok = false; break; }
-          mbar_arrive_expect_tx(&kfull[ks], kBlockBytes);
-          tma_load_2d(sk + ks * kBlockBytes, &tm_k, &kfull[ks], kb * 64, st * kTileS);
-          if (++ks == C::NK) {
-            ks = 0;
-            kph ^= 1;
-          }
-        }
-        if (!ok) break;
+    int cur_g = -1, rows = 0;
+    int ks = 0;          // k stage
+    uint32_t kph = 0;    // its phase
+    int g = (int)(beg / p.n_stiles), st = (int)(beg % p.n_stiles) - 1;
+    GroupRowsAhead<C::TPT> ahead;
+    ahead.load(p, g);  // the first group of the range
+    for (long long it = beg; it < end; ++it) {
+      if (++st == p.n_stiles) {
+        st = 0;
+        ++g;
       }
+      if (g != cur_g) {
+        cur_g = g;
+        rows = ahead.rows(p);
+        ahead.load(p, g + 1);
+      }
+      if (st * kTileS >= rows) continue;
+      bool ok = true;
+#pragma unroll
+      for (int kb = 0; kb < C::KB; ++kb) {
+        if (!mbar_wait_warp(&kempty[ks], kph ^ 1, p.status, 2)) { ok = false; break; }
+        mbar_arrive_expect_tx_elect(&kfull[ks], kBlockBytes);
+        tma_load_2d_elect(sk + ks * kBlockBytes, &tm_k, &kfull[ks], kb * 64, st * kTileS);
+        if (++ks == C::NK) {
+          ks = 0;
+          kph ^= 1;
+        }
+      }
+      if (!ok) break;
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------- TMA producer: q tiles
     // On a warp of its own, so that the next group's q tile loads as soon as its buffer is
     // free (when the group before the current one has finished), not only when the k
     // producer reaches that group a few stages ahead of the products.
-    if (lane == 0) {
-      int cur_g = -1, rows = 0;
-      bool started = false;
-      uint32_t q_it = 0;
-      int g = (int)(beg / p.n_stiles), st = (int)(beg % p.n_stiles) - 1;
-      GroupRowsAhead<C::TPT> ahead;
-      ahead.load(p, g);  // the first group of the range
-      for (long long it = beg; it < end; ++it) {
-        if (++st == p.n_stiles) {
-          st = 0;
-          ++g;
-        }
-        if (g != cur_g) {
-          cur_g = g;
-          rows = ahead.rows(p);
-          ahead.load(p, g + 1);
-          started = false;
-        }
-        if (started || st * kTileS >= rows) continue;
-        const int b = q_it & 1;
-        if (!mbar_wait(&qempty[b], ((q_it >> 1) & 1) ^ 1, p.status, 1)) break;
-        mbar_arrive_expect_tx(&qfull[b], C::Q_BYTES);
-#pragma unroll
-        for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_2d(sq + b * C::Q_BYTES + kb * C::QB_BYTES, &tm_q, &qfull[b], kb * 64, g * TN);
-        ++q_it;
-        started = true;
+    int cur_g = -1, rows = 0;
+    bool started = false;
+    uint32_t q_it = 0;
+    int g = (int)(beg / p.n_stiles), st = (int)(beg % p.n_stiles) - 1;
+    GroupRowsAhead<C::TPT> ahead;
+    ahead.load(p, g);  // the first group of the range
+    for (long long it = beg; it < end; ++it) {
+      if (++st == p.n_stiles) {
+        st = 0;
+        ++g;
       }
+      if (g != cur_g) {
+        cur_g = g;
+        rows = ahead.rows(p);
+        ahead.load(p, g + 1);
+        started = false;
+      }
+      if (started || st * kTileS >= rows) continue;
+      const int b = q_it % C::NQ;
+      if (!mbar_wait_warp(&qempty[b], ((q_it / C::NQ) & 1) ^ 1, p.status, 1)) break;
+      mbar_arrive_expect_tx_elect(&qfull[b], C::Q_BYTES);
+#pragma unroll
+      for (int kb = 0; kb < C::KB; ++kb)
+        tma_load_2d_elect(sq + b * C::Q_BYTES + kb * C::QB_BYTES, &tm_q, &qfull[b], kb * 64, g * TN);
+      ++q_it;
+      started = true;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------- MMA issuer
-    // Lean between products: its scheduler is shared with four epilogue warps that wake up
-    // when a tile completes, so descriptors are built once and offset by constants, and the
-    // stage / buffer indices are running counters.
-    if (lane == 0) {
-      // descriptor address field = byte address >> 4 (bits 0..13); offsets below never carry out
-      const uint64_t adesc0 = desc_sw128(smem_u32(sk), 16, 1024);
-      const uint64_t bdesc0 = desc_sw128(smem_u32(sq), 16, 1024);
-      int cur_g = -1, rows = 0, qb = -1;
-      bool started = false;
-      uint32_t q_it = 0;
-      int ks = 0, ab = 0;
-      uint32_t kph = 0, aph = 0;
-      int g = (int)(beg / p.n_stiles), st = (int)(beg % p.n_stiles) - 1;
-      GroupRowsAhead<C::TPT> ahead;
-      ahead.load(p, g);  // the first group of the range
-      for (long long it = beg; it < end; ++it) {
-        if (++st == p.n_stiles) {
-          st = 0;
-          ++g;
-        }
-        if (g != cur_g) {
-          cur_g = g;
-          rows = ahead.rows(p);
-          ahead.load(p, g + 1);
-          started = false;
-        }
-        if (st * kTileS >= rows) continue;
-        if (!started) {
-          if (qb >= 0) tc_commit(&qempty[qb]);  // previous group's q tile is free once its MMAs finish
-          qb = q_it & 1;
-          if (!mbar_wait(&qfull[qb], (q_it >> 1) & 1, p.status, 3)) break;
-          ++q_it;
-          started = true;
-          tc_fence_after();
-        }
-        if (!mbar_wait(&aempty[ab], aph ^ 1, p.status, 4)) break;
+    // The whole warp runs the loop (converged, so that descriptors and addresses stay in uniform
+    // registers) and one elected lane issues each product and commit.  Lean between products:
+    // descriptors are built once and offset by constants, stage and buffer indices are running
+    // counters.
+    // descriptor address field = byte address >> 4 (bits 0..13); offsets below never carry out
+    const uint64_t adesc0 = desc_sw128(smem_u32(sk), 16, 1024);
+    const uint64_t bdesc0 = desc_sw128(smem_u32(sq), 16, 1024);
+    int cur_g = -1, rows = 0, qb = -1;
+    bool started = false;
+    uint32_t q_it = 0;
+    int ks = 0, ab = 0;
+    uint32_t kph = 0, aph = 0;
+    int g = (int)(beg / p.n_stiles), st = (int)(beg % p.n_stiles) - 1;
+    GroupRowsAhead<C::TPT> ahead;
+    ahead.load(p, g);  // the first group of the range
+    for (long long it = beg; it < end; ++it) {
+      if (++st == p.n_stiles) {
+        st = 0;
+        ++g;
+      }
+      if (g != cur_g) {
+        cur_g = g;
+        rows = ahead.rows(p);
+        ahead.load(p, g + 1);
+        started = false;
+      }
+      if (st * kTileS >= rows) continue;
+      if (!started) {
+        if (qb >= 0) tc_commit_elect(&qempty[qb]);  // previous group's q tile is free once its MMAs finish
+        qb = q_it % C::NQ;
+        if (!mbar_wait_warp(&qfull[qb], (q_it / C::NQ) & 1, p.status, 3)) break;
+        ++q_it;
+        started = true;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + ab * TN;
-        const uint64_t bq = bdesc0 + (uint64_t)((qb * C::Q_BYTES) >> 4);
-        bool ok = true;
+      }
+      if (!mbar_wait_warp(&aempty[ab], aph ^ 1, p.status, 4)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + ab * TN;
+      const uint64_t bq = bdesc0 + (uint64_t)((qb * C::Q_BYTES) >> 4);
+      bool ok = true;
 #pragma unroll
-        for (int kb = 0; kb < C::KB; ++kb) {
-          if (!mbar_wait(&kfull[ks], kph, p.status, 5)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t a0 = adesc0 + (uint64_t)((ks * kBlockBytes) >> 4);
-          const uint64_t b0 = bq + (uint64_t)((kb * C::QB_BYTES) >> 4);
+      for (int kb = 0; kb < C::KB; ++kb) {
+        if (!mbar_wait_warp(&kfull[ks], kph, p.status, 5)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t a0 = adesc0 + (uint64_t)((ks * kBlockBytes) >> 4);
+        const uint64_t b0 = bq + (uint64_t)((kb * C::QB_BYTES) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // 16 columns = 32 bytes = 2 address units per step
-            tc_mma_f16(d_tmem, a0 + 2 * kk, b0 + 2 * kk, kIdesc, (kb | kk) != 0);
-          tc_commit(&kempty[ks]);  // k stage is free once these MMAs complete
-          if (++ks == C::NK) {
-            ks = 0;
-            kph ^= 1;
-          }
+        for (int kk = 0; kk < 4; ++kk)  // 16 columns = 32 bytes = 2 address units per step
+          tc_mma_f16_elect(d_tmem, a0 + 2 * kk, b0 + 2 * kk, kIdesc, (kb | kk) != 0);
+        tc_commit_elect(&kempty[ks]);  // k stage is free once these MMAs complete
+        if (++ks == C::NK) {
+          ks = 0;
+          kph ^= 1;
         }
-        if (!ok) break;
-        tc_commit(&afull[ab]);
-        if (++ab == C::NACC) {
-          ab = 0;
-          aph ^= 1;
-        }
+      }
+      if (!ok) break;
+      tc_commit_elect(&afull[ab]);
+      if (++ab == C::NACC) {
+        ab = 0;
+        aph ^= 1;
       }
     }
   } else if (warp >= 4) {
