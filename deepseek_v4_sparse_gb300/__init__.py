@@ -29,6 +29,7 @@ EXPORTS = (
     "ds4x_index_and_attend", "ds4x_workspace_bytes", "ds4x_status_string",
     "ds4x_last_launch_count", "ds4x_device_status", "ds4x_selftest_bounded_wait",
     "ds4x_topk_static_scratch", "ds4x_decode", "ds4x_decode_workspace_bytes",
+    "ds4x_index_and_attend_host", "ds4x_index_and_attend_host_bytes",
 )
 
 _lock = threading.Lock()
@@ -60,6 +61,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                               i32, i32, i32, f32, P, P, P, P, sz, P]
         lib.ds4x_workspace_bytes.argtypes = [i32, i32, i32]
         lib.ds4x_workspace_bytes.restype = sz
+        lib.ds4x_index_and_attend_host.argtypes = [P, P, P, P, P, P, ctypes.c_int, i32, i32, i32, i32, i32,
+                                                   i32, i32, i32, f32, P, P, P, i32, P, sz, P]
+        lib.ds4x_index_and_attend_host_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
+        lib.ds4x_index_and_attend_host_bytes.restype = sz
         lib.ds4x_decode.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, P, i32, i32, i32, i32, i32, i32, i32,
                                     i32, i32, f32, P, P, P, P, P, sz, ctypes.POINTER(i32), P]
         lib.ds4x_decode_workspace_bytes.argtypes = [i32, i32]
@@ -70,6 +75,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.ds4x_device_status.argtypes = [P, ctypes.c_int]
         lib.ds4x_selftest_bounded_wait.argtypes = [i64, P]
         for f in ("ds4x_indexer_score", "ds4x_topk", "ds4x_sparse_attn", "ds4x_index_and_attend", "ds4x_decode",
+                  "ds4x_index_and_attend_host",
                   "ds4x_last_launch_count", "ds4x_device_status", "ds4x_selftest_bounded_wait"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
@@ -225,6 +231,51 @@ def index_and_attend(q, w, k, positions, q_attn, kv, ratio: int, k_top: int = 51
                                       dt, T, H, D, S, ratio, k_top, Hq, Dkv, scale, _ptr(indices),
                                       _ptr(out), _ptr(lse), _ptr(workspace), wbytes, _stream(stream))
     _check("ds4x_index_and_attend", rc)
+    return indices, out, lse
+
+
+def _host_ptr(t):
+    """A contiguous CPU tensor's host address (page-locked memory lets the copies overlap)."""
+    if t is None:
+        return None
+    if t.is_cuda or not t.is_contiguous():
+        raise ValueError("host tensors passed to ds4x_index_and_attend_host must be contiguous CPU tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def index_and_attend_host_bytes(T: int, H: int, D: int, S: int, k_top: int, Hq: int, Dkv: int,
+                                n_chunks: int = 0) -> int:
+    return int(load().ds4x_index_and_attend_host_bytes(T, H, D, S, k_top, Hq, Dkv, n_chunks))
+
+
+def index_and_attend_host(q, w, k, positions, q_attn, kv, ratio: int, k_top: int = 512, S: int | None = None,
+                          scale: float | None = None, n_chunks: int = 0, indices=None, out=None, lse=None,
+                          device_buffer=None, want_lse: bool = True, device=None, stream=None):
+    """The whole path on host (CPU) tensors: copies in, computes, copies out, overlapped by sub-chunks
+    of tokens.  Outputs are page-locked CPU tensors, valid once `stream` is synchronised.
+    Returns (indices, out, lse)."""
+    torch = _torch()
+    dt = _kv_dtype(q_attn)
+    T, H, D = q.shape
+    _, Hq, Dkv = q_attn.shape
+    S = k.shape[0] if S is None else S
+    scale = 1.0 / math.sqrt(Dkv) if scale is None else scale
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if indices is None:
+        indices = torch.empty((T, k_top), dtype=torch.int32).pin_memory()
+    if out is None:
+        out = torch.empty(q_attn.shape, dtype=q_attn.dtype).pin_memory()
+    if lse is None and want_lse:
+        lse = torch.empty((T, Hq), dtype=torch.float32).pin_memory()
+    need = index_and_attend_host_bytes(T, H, D, S, k_top, Hq, Dkv, n_chunks)
+    if device_buffer is None:
+        device_buffer = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
+    dbytes = device_buffer.numel() * device_buffer.element_size()
+    rc = load().ds4x_index_and_attend_host(
+        _host_ptr(q), _host_ptr(w), _host_ptr(k), _host_ptr(positions), _host_ptr(q_attn), _host_ptr(kv), dt, T,
+        H, D, S, ratio, k_top, Hq, Dkv, scale, _host_ptr(indices), _host_ptr(out), _host_ptr(lse), n_chunks,
+        _ptr(device_buffer), dbytes, _stream(stream))
+    _check("ds4x_index_and_attend_host", rc)
     return indices, out, lse
 
 

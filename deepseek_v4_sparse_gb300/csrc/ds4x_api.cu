@@ -2,10 +2,13 @@
 //
 // Host-side argument validation happens here, before anything is launched; the kernels and
 // their launchers live in score_tcgen05.cu, topk_stream.cu and sparse_mqa.cu.  The library
-// allocates no device memory: the fused entry carves the caller's workspace.
+// allocates no device memory: the fused entry carves the caller's workspace, and the
+// host-buffer entry the caller's device buffer.
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
+
+#include <mutex>
 
 #include "ds4x_internal.h"
 #include "ds4x_ptx.cuh"
@@ -122,6 +125,81 @@ __global__ void bounded_wait_selftest_kernel(int* status, unsigned long long tim
 
 using namespace ds4x;
 
+namespace {
+// ------------------------------------------------------------- the host-buffer fused path
+// Device staging of ds4x_index_and_attend_host: [k | kv | fused workspace of one sub-chunk |
+// two slots of one sub-chunk's per-token inputs and outputs], every part 256-byte aligned.
+struct HostLayout {
+  int n = 0, tc = 0;                                 // sub-chunks, tokens per sub-chunk
+  size_t k = 0, kv = 0, ws = 0, ws_bytes = 0, slot0 = 0, slot = 0, total = 0;
+  size_t q = 0, w = 0, pos = 0, qa = 0, idx = 0, out = 0, lse = 0;  // offsets within a slot
+};
+
+int default_host_chunks(int T) {  // sub-chunks of about 512 tokens (a few CTA waves each)
+  const int n = T / 512;
+  return n < 1 ? 1 : n > 8 ? 8 : n;
+}
+
+HostLayout host_layout(int T, int H, int D, int S, int k_top, int Hq, int Dkv, int n_chunks) {
+  HostLayout L;
+  L.n = n_chunks > 0 ? (n_chunks < T ? n_chunks : T) : default_host_chunks(T);
+  L.tc = (T + L.n - 1) / L.n;
+  L.n = (T + L.tc - 1) / L.tc;  // no empty sub-chunk
+  const size_t tc = (size_t)L.tc, e16 = 2;
+  size_t o = 0;
+  L.k = o;
+  o += round256((size_t)S * D * e16);
+  L.kv = o;
+  o += round256((size_t)S * Dkv * e16);
+  L.ws = o;
+  L.ws_bytes = fused_workspace_bytes(L.tc, S, k_top);
+  o += round256(L.ws_bytes);
+  size_t s = 0;
+  L.q = s;
+  s += round256(tc * H * D * e16);
+  L.w = s;
+  s += round256(tc * H * e16);
+  L.pos = s;
+  s += round256(tc * sizeof(int32_t));
+  L.qa = s;
+  s += round256(tc * Hq * Dkv * e16);
+  L.idx = s;
+  s += round256(tc * k_top * sizeof(int32_t));
+  L.out = s;
+  s += round256(tc * Hq * Dkv * e16);
+  L.lse = s;
+  s += round256(tc * Hq * sizeof(float));
+  L.slot = s;
+  L.slot0 = o;
+  L.total = o + 2 * s;
+  return L;
+}
+
+// Copy streams and events of the host-buffer path, one set per device, created on first use;
+// a call holds the mutex while it enqueues (the work itself runs after it returns).
+struct HostPipe {
+  std::mutex m;
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, in_done[2] = {}, work_done[2] = {}, out_done[2] = {};
+};
+HostPipe g_host_pipe[kMaxDevices];
+
+cudaError_t host_pipe_init(HostPipe& hp) {
+  if (hp.ready) return cudaSuccess;
+  cudaError_t e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming);
+  for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+    e = cudaEventCreateWithFlags(&hp.in_done[i], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.work_done[i], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.out_done[i], cudaEventDisableTiming);
+  }
+  if (e == cudaSuccess) hp.ready = true;
+  return e;
+}
+}  // namespace
+
 extern "C" {
 
 const char* ds4x_status_string(int status) {
@@ -212,6 +290,86 @@ int ds4x_index_and_attend(const void* q, const void* w, const void* k, const int
   return scope.done(run_index_and_attend(q, w, k, positions, q_attn, kv, kv_dtype == DS4X_BF16 ? 1 : 0, T, H, D, S,
                                          ratio, k_top, scale, indices, out, lse, workspace, workspace_bytes,
                                          static_cast<cudaStream_t>(stream)));
+}
+
+size_t ds4x_index_and_attend_host_bytes(int32_t T, int32_t H, int32_t D, int32_t S, int32_t k_top, int32_t Hq,
+                                        int32_t Dkv, int32_t n_chunks) {
+  if (T <= 0 || S < 0 || H <= 0 || D <= 0 || k_top <= 0 || Hq <= 0 || Dkv <= 0 || n_chunks < 0) return 0;
+  return host_layout(T, H, D, S, k_top, Hq, Dkv, n_chunks).total;
+}
+
+int ds4x_index_and_attend_host(const void* q, const void* w, const void* k, const int32_t* positions,
+                               const void* q_attn, const void* kv, ds4x_dtype kv_dtype, int32_t T, int32_t H,
+                               int32_t D, int32_t S, int32_t ratio, int32_t k_top, int32_t Hq, int32_t Dkv,
+                               float scale, int32_t* indices, void* out, float* lse, int32_t n_chunks,
+                               void* device_buffer, size_t device_bytes, void* stream) {
+  CallScope scope;
+  if (T < 0 || S < 0 || H <= 0 || D <= 0 || Hq <= 0 || Dkv <= 0 || ratio < 1 || k_top < 1 || n_chunks < 0)
+    return DS4X_ERR_INVALID;
+  if (kv_dtype != DS4X_F16 && kv_dtype != DS4X_BF16) return DS4X_ERR_INVALID;
+  if (k_top > DS4X_MAX_KTOP) return DS4X_ERR_UNSUPPORTED;
+  if (T == 0) return scope.done(DS4X_OK);
+  if (!q || !w || !positions || !q_attn || !indices || !out || (S > 0 && (!k || !kv)) || !device_buffer)
+    return DS4X_ERR_INVALID;
+  if (!aligned16(device_buffer)) return DS4X_ERR_INVALID;
+  if (!score_shape_supported(H, D) || !attn_shape_supported(Hq, Dkv)) return DS4X_ERR_UNSUPPORTED;
+  const HostLayout L = host_layout(T, H, D, S, k_top, Hq, Dkv, n_chunks);
+  if (device_bytes < L.total) return DS4X_ERR_WORKSPACE;
+
+  HostPipe& hp = g_host_pipe[current_device()];
+  std::lock_guard<std::mutex> lock(hp.m);
+  if (host_pipe_init(hp) != cudaSuccess) return DS4X_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(device_buffer);
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+#define DS4X_CK(x) \
+  if ((x) != cudaSuccess) return DS4X_ERR_CUDA
+  // the copies start after everything enqueued on the caller's stream (an earlier call's
+  // kernels may still use this device buffer)
+  DS4X_CK(cudaEventRecord(hp.start, st));
+  DS4X_CK(cudaStreamWaitEvent(hp.in, hp.start, 0));
+  DS4X_CK(cudaStreamWaitEvent(hp.out, hp.start, 0));
+  if (S > 0) {
+    DS4X_CK(cudaMemcpyAsync(base + L.k, k, (size_t)S * D * 2, h2d, hp.in));
+    DS4X_CK(cudaMemcpyAsync(base + L.kv, kv, (size_t)S * Dkv * 2, h2d, hp.in));
+  }
+  const size_t qt = (size_t)H * D * 2, wt = (size_t)H * 2, at = (size_t)Hq * Dkv * 2;
+  const size_t it = (size_t)k_top * sizeof(int32_t), lt = (size_t)Hq * sizeof(float);
+  for (int j = 0; j < L.n; ++j) {
+    const int b = j & 1;
+    const size_t t0 = (size_t)j * L.tc;
+    const int tn = (int)((size_t)T - t0 < (size_t)L.tc ? (size_t)T - t0 : (size_t)L.tc);
+    uint8_t* sl = base + L.slot0 + b * L.slot;
+    // inputs of sub-chunk j, once sub-chunk j-2 (same slot) has been computed
+    if (j >= 2) DS4X_CK(cudaStreamWaitEvent(hp.in, hp.work_done[b], 0));
+    DS4X_CK(cudaMemcpyAsync(sl + L.q, static_cast<const uint8_t*>(q) + t0 * qt, tn * qt, h2d, hp.in));
+    DS4X_CK(cudaMemcpyAsync(sl + L.w, static_cast<const uint8_t*>(w) + t0 * wt, tn * wt, h2d, hp.in));
+    DS4X_CK(cudaMemcpyAsync(sl + L.pos, positions + t0, tn * sizeof(int32_t), h2d, hp.in));
+    DS4X_CK(cudaMemcpyAsync(sl + L.qa, static_cast<const uint8_t*>(q_attn) + t0 * at, tn * at, h2d, hp.in));
+    DS4X_CK(cudaEventRecord(hp.in_done[b], hp.in));
+    // the work, once the inputs are in and sub-chunk j-2's outputs are out of the slot
+    DS4X_CK(cudaStreamWaitEvent(st, hp.in_done[b], 0));
+    if (j >= 2) DS4X_CK(cudaStreamWaitEvent(st, hp.out_done[b], 0));
+    const int rc = run_index_and_attend(sl + L.q, sl + L.w, S > 0 ? base + L.k : nullptr,
+                                        reinterpret_cast<const int32_t*>(sl + L.pos), sl + L.qa,
+                                        S > 0 ? base + L.kv : nullptr, kv_dtype == DS4X_BF16 ? 1 : 0, tn, H, D, S,
+                                        ratio, k_top, scale, reinterpret_cast<int32_t*>(sl + L.idx), sl + L.out,
+                                        lse ? reinterpret_cast<float*>(sl + L.lse) : nullptr, base + L.ws,
+                                        L.ws_bytes, st);
+    if (rc != DS4X_OK) return rc;
+    DS4X_CK(cudaEventRecord(hp.work_done[b], st));
+    // outputs of sub-chunk j
+    DS4X_CK(cudaStreamWaitEvent(hp.out, hp.work_done[b], 0));
+    DS4X_CK(cudaMemcpyAsync(indices + t0 * k_top, sl + L.idx, tn * it, d2h, hp.out));
+    DS4X_CK(cudaMemcpyAsync(static_cast<uint8_t*>(out) + t0 * at, sl + L.out, tn * at, d2h, hp.out));
+    if (lse) DS4X_CK(cudaMemcpyAsync(lse + t0 * Hq, sl + L.lse, tn * lt, d2h, hp.out));
+    DS4X_CK(cudaEventRecord(hp.out_done[b], hp.out));
+  }
+  // later work on the caller's stream (a synchronisation included) sees the outputs
+  DS4X_CK(cudaStreamWaitEvent(st, hp.out_done[(L.n - 1) & 1], 0));
+  if (L.n > 1) DS4X_CK(cudaStreamWaitEvent(st, hp.out_done[L.n & 1], 0));
+#undef DS4X_CK
+  return scope.done(DS4X_OK);
 }
 
 int ds4x_device_status(void* stream, int clear) {

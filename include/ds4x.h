@@ -171,6 +171,39 @@ int ds4x_index_and_attend(const void* q, const void* w, const void* k, const int
 size_t ds4x_workspace_bytes(int32_t T, int32_t S, int32_t k_top);
 
 /* ---------------------------------------------------------------------------
+ * ds4x_index_and_attend_host — ds4x_index_and_attend on HOST buffers: the inputs are copied
+ *   to the device, the path runs, the outputs are copied back, and the copies overlap the
+ *   work.  The tokens are cut into n_chunks sub-chunks (0: the library chooses); sub-chunk j
+ *   is copied in on an internal stream while sub-chunk j-1 is computed on `stream` and
+ *   sub-chunk j-2's outputs are copied out on a second internal stream, so that both copy
+ *   directions and the kernels run at once.  The shared rows k and kv are copied once, first.
+ *   Results are those of ds4x_index_and_attend on each sub-chunk (the same per token).
+ *
+ *   q, w, positions, q_attn, k, kv: host memory, layouts as in ds4x_index_and_attend.
+ *   indices, out, lse (lse may be NULL): host memory, written by the call.
+ *   Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for the copies to
+ *   run asynchronously and overlap; pageable memory gives the same results, serialised.
+ *   device_buffer: device memory the call owns for its duration, 16-byte aligned, at least
+ *   ds4x_index_and_attend_host_bytes(...) bytes (staging for k, kv, two sub-chunks of
+ *   per-token inputs and outputs, and the fused workspace).
+ *   Ordering: the copies start after all work enqueued on `stream` before the call; on return
+ *   everything is enqueued and `stream` waits for the last copy out, so a synchronisation of
+ *   `stream` (or any work enqueued on it later) sees the outputs in host memory.  The host
+ *   buffers must not be touched until then.
+ *   Errors: as ds4x_index_and_attend; DS4X_ERR_WORKSPACE when device_bytes is too small,
+ *   DS4X_ERR_INVALID for NULL or misaligned pointers or n_chunks < 0.
+ * ------------------------------------------------------------------------- */
+int ds4x_index_and_attend_host(const void* q, const void* w, const void* k, const int32_t* positions,
+                               const void* q_attn, const void* kv, ds4x_dtype kv_dtype,
+                               int32_t T, int32_t H, int32_t D, int32_t S, int32_t ratio,
+                               int32_t k_top, int32_t Hq, int32_t Dkv, float scale,
+                               int32_t* indices, void* out, float* lse, int32_t n_chunks,
+                               void* device_buffer, size_t device_bytes, void* stream);
+
+size_t ds4x_index_and_attend_host_bytes(int32_t T, int32_t H, int32_t D, int32_t S, int32_t k_top,
+                                        int32_t Hq, int32_t Dkv, int32_t n_chunks);
+
+/* ---------------------------------------------------------------------------
  * ds4x_decode — the decode loop: n_steps query tokens at consecutive positions
  * pos0, pos0+1, ..., one fused step (ds4x_index_and_attend with T = 1) each, with the
  * compressed rows appended as the positions complete them ([K]: decode at long context;

@@ -124,3 +124,38 @@ def test_workspace_sizes(lib):
     # the decode loop sizes its workspace for one token at full capacity
     assert ds4x.decode_workspace_bytes(262208, 512) >= ds4x.workspace_bytes(1, 262208, 512) >= 262208 * 4
     assert ds4x.decode_workspace_bytes(0, 512) == 0
+
+
+def _host(lib, T=64, S=100, H=64, k_top=512, n_chunks=0, dtype=1, buf=0x10000, nbytes=1 << 40, q=0x10000):
+    A = 0x10000
+    return lib.ds4x_index_and_attend_host(_p(q), _p(A), _p(A), _p(A), _p(A), _p(A), dtype, T, H, 128, S, 4, k_top, 64,
+                                          512, 0.1, _p(A), _p(A), None, n_chunks, _p(buf) if buf else None, nbytes,
+                                          None)
+
+
+def test_host_path_arguments_rejected_without_launch(lib):
+    assert _host(lib, n_chunks=-1) == ds4x.ERR_INVALID
+    assert _host(lib, dtype=5) == ds4x.ERR_INVALID
+    assert _host(lib, buf=0) == ds4x.ERR_INVALID                  # no device buffer
+    assert _host(lib, buf=0x10004) == ds4x.ERR_INVALID            # device buffer not 16-byte aligned
+    assert _host(lib, q=0) == ds4x.ERR_INVALID
+    assert _host(lib, H=48) == ds4x.ERR_UNSUPPORTED
+    assert _host(lib, k_top=2048) == ds4x.ERR_UNSUPPORTED
+    assert _host(lib, nbytes=16) == ds4x.ERR_WORKSPACE
+    assert _host(lib, T=0) == ds4x.OK                            # nothing to do, nothing enqueued
+
+
+def test_host_path_staging_sizes(lib):
+    T, H, D, S, k_top, Hq, Dkv = 2048, 64, 128, 2048, 512, 64, 512
+    per_token = H * D * 2 + H * 2 + 4 + Hq * Dkv * 2 + k_top * 4 + Hq * Dkv * 2 + Hq * 4
+    shared = S * D * 2 + S * Dkv * 2
+    for n in (1, 3, 4, 8):
+        tc = -(-T // n)
+        b = ds4x.index_and_attend_host_bytes(T, H, D, S, k_top, Hq, Dkv, n)
+        # k and kv, the fused workspace of one sub-chunk, two slots of one sub-chunk's tokens
+        low = shared + ds4x.workspace_bytes(tc, S, k_top) + 2 * tc * per_token
+        assert low <= b <= low + 20 * 256
+    assert ds4x.index_and_attend_host_bytes(T, H, D, S, k_top, Hq, Dkv, 0) == \
+        ds4x.index_and_attend_host_bytes(T, H, D, S, k_top, Hq, Dkv, 4)      # default: sub-chunks of ~512 tokens
+    assert ds4x.index_and_attend_host_bytes(0, H, D, S, k_top, Hq, Dkv, 0) == 0
+    assert ds4x.index_and_attend_host_bytes(T, H, D, S, k_top, Hq, Dkv, -1) == 0
