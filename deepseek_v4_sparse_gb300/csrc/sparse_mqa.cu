@@ -23,7 +23,8 @@
 // c+2 and O^T of chunk c+1 interleave in the tensor pipe.  Buffers are released in 128-dim
 // pieces: a chunk's slot pair as its O^T product completes (the next gather starts early), a
 // pair of q blocks as the token's last S product passes it, a d-block of O^T as soon as the
-// output warps hold it in registers.
+// output warps hold it in registers.  O^T rotates over six 64-column TMEM slots (a token uses
+// four), so the next token's first products do not wait for the previous token's output.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -50,7 +51,8 @@ constexpr int kOffP = kOffKV + 2 * kBufBytes;
 constexpr int kOffAlpha = kOffP + 2 * kPBytes;  // float[64] rescale factors of one chunk
 constexpr int kOffLM = kOffAlpha + kHq * 4;     // float[2 tokens][3 (l, m, 1/l)][64]
 constexpr int kOffBars = kOffLM + 2 * 3 * kHq * 4;
-constexpr int kNumBars = 2 * kPairs + 2 * 2 * kPairs + 2 + 2 + 2 + 2 + 2 * kPairs + 2 + 2;
+constexpr int kOSlots = 6;                      // O^T slots of 64 columns (a token uses 4)
+constexpr int kNumBars = 2 * kPairs + 2 * 2 * kPairs + 2 + 2 + 2 + 2 + 2 * kOSlots + 2 + 2;
 constexpr int kOffTmemSlot = kOffBars + kNumBars * 8;
 constexpr int kSmem = kOffTmemSlot + 16;
 constexpr int kThreads = 15 * 32;
@@ -58,7 +60,11 @@ constexpr int kSWarp = 12;   // issues S, allocates TMEM
 constexpr int kOWarp = 13;   // issues O^T
 constexpr int kQWarp = 14;   // loads q_attn of each token by TMA
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;
+// TMEM: S in columns [0, 128) (two buffers of 64), O^T in six slots of 64 from column 128.  A
+// token's 128-dim block db accumulates in slot (4 * token + db) % 6, so the next token's first
+// two blocks start in slots the previous token does not use while its output is drained, and
+// its last two reuse the slots drained first.
+constexpr uint32_t kColO = 128;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kSoftBar = 1, kEpiBar = 2, kGroupThreads = 128;
 constexpr int kMaxSplit = (DS4X_MAX_KTOP + kRows - 1) / kRows;  // items a token can be split into
@@ -203,15 +209,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* sempty = sfull + 2;
   uint64_t* pfull = sempty + 2;
   uint64_t* pempty = pfull + 2;
-  uint64_t* ofull = pempty + 2;             // [d-block]
-  uint64_t* oempty = ofull + kPairs;        // [d-block]
-  uint64_t* lready = oempty + kPairs;            // [token parity] l, m of a token written
+  uint64_t* ofull = pempty + 2;             // [O^T slot]
+  uint64_t* oempty = ofull + kOSlots;       // [O^T slot]
+  uint64_t* lready = oempty + kOSlots;           // [token parity] l, m of a token written
   uint64_t* lfree = lready + 2;             // [token parity] ... and read by the output warps
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nch = p.nchunks;
+  auto oslot = [](uint32_t tok_i, int db) { return (int)((4u * (tok_i % 3u) + (uint32_t)db) % kOSlots); };
   // work item it: token it / nsplit, chunks [c0, c1) of it (all of them when nsplit = 1)
   auto item_of = [&](int it, int& t, int& c0, int& c1) {
     t = it / p.nsplit;
@@ -235,6 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kPairs; ++i) {
       mbar_init(&qfull[i], 1);
       mbar_init(&qempty[i], 1);
+    }
+    for (int i = 0; i < kOSlots; ++i) {
       mbar_init(&ofull[i], 1);
       mbar_init(&oempty[i], 4);
     }
@@ -357,6 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kOWarp) {
     // --------------------------------------------------------------- O^T += V^T P^T
     uint32_t gc = 0, tok_i = 0;
+    uint32_t o_ph = 0;  // bit s: phase of O^T slot s's empty barrier (uses completed, mod 2)
     bool ok = true;
     const uint32_t kv_addr = smem_u32(skv);
     const uint32_t p_addr = smem_u32(sp);
@@ -369,19 +379,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int db = 0; db < kPairs; ++db) {
-          // an item's first product overwrites O^T: the previous item's output must have read it
+          const int os = oslot(tok_i, db);
+          // an item's first product overwrites its O^T slot: the output that last read it is done
           if (c == c0) {
-            if (!mbar_wait(&oempty[db], (tok_i & 1) ^ 1, p.status, 34)) { ok = false; break; }
+            if (!mbar_wait(&oempty[os], ((o_ph >> os) & 1u) ^ 1u, p.status, 34)) { ok = false; break; }
+            o_ph ^= 1u << os;
             tc_fence_after();
           }
 #pragma unroll
           for (int ks = 0; ks < kRows / 16; ++ks) {
             const uint64_t a = desc_sw128(kv_addr + b * kBufBytes + (2 * db) * kSlotBytes + ks * 2048, kSlotBytes, 1024);
             const uint64_t bd = desc_sw128(p_addr + pb * kPBytes + ks * 32, 16, 1024);
-            tc_mma_f16_elect(tmem + kColO + db * kHq, a, bd, kIdescO, (c > c0 || ks > 0));
+            tc_mma_f16_elect(tmem + kColO + os * kHq, a, bd, kIdescO, (c > c0 || ks > 0));
           }
           tc_commit_elect(&kvempty[b * kPairs + db]);  // this 128-dim slice of the chunk is free
-          if (c == c1 - 1) tc_commit_elect(&ofull[db]);
+          if (c == c1 - 1) tc_commit_elect(&ofull[os]);
         }
         if (!ok) break;
         tc_commit_elect(&pempty[pb]);
@@ -477,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
           for (int q2 = 0; q2 < 2 * kPairs; ++q2) {  // 4 d-blocks x 2 halves of 32 heads
             float v[32];
-            const uint32_t ta = tmem + t_lane + kColO + (q2 >> 1) * kHq + (q2 & 1) * 32;
+            const uint32_t ta = tmem + t_lane + kColO + oslot(tok_i, q2 >> 1) * kHq + (q2 & 1) * 32;
             tmem_ld32(ta, v);
             tc_wait_ld();
 #pragma unroll
@@ -555,6 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp - 8;
     const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
     uint32_t tok_i = 0;
+    uint32_t f_ph = 0;  // bit s: phase of O^T slot s's full barrier
     bool ok = true;
     const bool odd = lane & 1;
     for (int it = blockIdx.x; it < p.items && ok; it += gridDim.x, ++tok_i) {
@@ -574,14 +587,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t* orow = reinterpret_cast<uint32_t*>(p.out + (int64_t)t * kHq * kDkv);
 #pragma unroll 1
       for (int db = 0; db < kPairs; ++db) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&ofull[db], tok_i & 1, p.status, 44));
+        const int os = oslot(tok_i, db);
+        ok = __all_sync(0xffffffffu, mbar_wait(&ofull[os], (f_ph >> os) & 1u, p.status, 44));
         if (!ok) break;
+        f_ph ^= 1u << os;
         tc_fence_after();
         float v[64];
         {
           float va[32], vb[32];
-          tmem_ld32(tmem + t_lane + kColO + db * kHq, va);
-          tmem_ld32(tmem + t_lane + kColO + db * kHq + 32, vb);
+          tmem_ld32(tmem + t_lane + kColO + os * kHq, va);
+          tmem_ld32(tmem + t_lane + kColO + os * kHq + 32, vb);
           tc_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -591,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&oempty[db]);
+        if (lane == 0) mbar_arrive(&oempty[os]);
         if (p.nsplit > 1) {  // split item: unnormalized fp32 sums, merged by the combine kernel
           float* po = p.part_o + (int64_t)it * kHq * kDkv + db * 128 + quad * 32 + lane;
 #pragma unroll
