@@ -159,6 +159,9 @@ WORKLOADS = {
                             kind="normal", kv_dtype="bf16"),
     "prefill_64k": Workload("prefill_64k", T=2048, H=64, D=128, S=16384, ratio=4, pos0=63488,
                             kind="normal", kv_dtype="bf16"),
+    # ratio-128 layer kind: every pooled row is attended (n_vis <= 512: sequential indices, no scoring)
+    "pooled_64k_r128": Workload("pooled_64k_r128", T=2048, H=64, D=128, S=512, ratio=128, pos0=63488,
+                                kind="normal", kv_dtype="bf16"),
     "decode_1m": Workload("decode_1m", T=1, H=64, D=128, S=262144, ratio=4, pos0=1048575,
                           kind="normal", kv_dtype="bf16", decode_steps=256, extra_rows=64),
 }

@@ -140,9 +140,8 @@ def test_score_shapes_both_tile_widths(H, D):
 
 
 def test_score_work_split_sparse_tiles():
-    # the scorer splits its items over CTAs by the tiles that are scored: here far fewer than
-    # there are CTAs, after leading token groups that see nothing (their rows are written -inf
-    # by whichever CTA holds them), with groups of differing widths in between
+    # far fewer scored tiles than CTAs, after leading token groups that see nothing (their rows
+    # are written -inf by whichever CTA holds them), with groups of differing widths in between
     S, ratio = 3000, 4
     nv = [0] * 21 + [5, 130, 0, 700, 1, 2999, 3000, 64, 0, 256, 257]
     positions = [n * ratio - 1 if n > 0 else -1 for n in nv]
@@ -297,3 +296,24 @@ def test_full_size_sampled(name):
     nv = np.minimum(wl.S, (inp.positions.astype(np.int64) + 1) // wl.ratio)
     assert np.all(np.diff(allidx, axis=1) > 0)
     assert np.all(allidx[:, 0] >= 0) and np.all(allidx[:, -1] < nv)
+
+
+def test_pooled_ratio128_all_rows():
+    # the ratio-128 layer kind: a token at the end of a 64k chunk sees at most 512 pooled rows, so
+    # the fused path skips scoring and attends every visible row (sequential indices)
+    wl = synth.WORKLOADS["pooled_64k_r128"]
+    T = 96
+    inp = synth.make_inputs(wl, seed=5, T=T, pos0=wl.pos0 + wl.T - T)
+    d = to_device(inp)
+    fidx, fout, flse = ds4x.index_and_attend(d["q"], d["w"], d["k"], d["positions"], d["q_attn"], d["kv"],
+                                             wl.ratio, wl.k_top, S=wl.S, scale=wl.scale)
+    torch.cuda.synchronize()
+    assert ds4x.device_status() == ds4x.OK
+    gidx = fidx.cpu().numpy()
+    ref_scores = oracle.indexer_score(inp.q, inp.w, inp.k, inp.positions, wl.ratio, S=wl.S)
+    ref_idx, _ = oracle.topk(ref_scores, inp.positions, wl.S, wl.ratio, wl.k_top)
+    assert np.array_equal(gidx, ref_idx)
+    nv = [n_vis(p, wl.ratio, wl.S) for p in inp.positions]
+    assert all(np.array_equal(gidx[t, :nv[t]], np.arange(nv[t])) for t in range(T))
+    ref_out, ref_lse = oracle.sparse_attn(inp.q_attn, inp.kv, wl.kv_dtype, gidx, wl.S, wl.scale)
+    check_attn(host16(fout), ref_out, wl.kv_dtype, flse.cpu().numpy(), ref_lse)
