@@ -44,6 +44,10 @@ def _bind(lib):
     lib.ds4x_ref_sparse_attn.argtypes = [P, P, ctypes.c_int, P, i32, i32, i32, i32, i32, f32, P, P]
     lib.ds4x_ref_index_and_attend.argtypes = [P, P, P, P, P, P, ctypes.c_int, i32, i32, i32, i32,
                                               i32, i32, i32, i32, f32, P, P, P]
+    lib.ds4x_ref_local_pooled_attn.argtypes = [P, P, P, ctypes.c_int, P, P, i32, i32, i32, i32, i32, i32,
+                                               i32, i32, f32, P, P]
+    lib.ds4x_ref_index_and_attend_local.argtypes = [P, P, P, P, P, P, P, ctypes.c_int, i32, i32, i32, i32,
+                                                    i32, i32, i32, i32, i32, i32, i32, f32, P, P, P]
     lib.ds4x_ref_decode.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, P, i32, i32, i32, i32, i32, i32,
                                     i32, i32, i32, f32, P, P, P, P, P]
     lib.ds4x_ref_n_visible.argtypes = [i64, i64, i64]
@@ -53,7 +57,8 @@ def _bind(lib):
     lib.ds4x_ref_encode16.argtypes = [ctypes.c_double, ctypes.c_int]
     lib.ds4x_ref_encode16.restype = ctypes.c_uint16
     for f in ("ds4x_ref_indexer_score", "ds4x_ref_topk_ex", "ds4x_ref_sparse_attn",
-              "ds4x_ref_index_and_attend", "ds4x_ref_decode"):
+              "ds4x_ref_index_and_attend", "ds4x_ref_decode", "ds4x_ref_local_pooled_attn",
+              "ds4x_ref_index_and_attend_local"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -139,6 +144,40 @@ class Oracle:
         assert rc == 0, rc
         return idx, out, lse
 
+    def local_pooled_attn(self, q_attn, kv, kv_local, dtype, indices, positions, S, local_pos0, window,
+                          scale):
+        """One softmax over the selected pooled rows of kv [>=S, Dkv] and the raw window rows
+        of kv_local [L, Dkv] (row r = position local_pos0 + r). Returns (out bits, lse)."""
+        q_attn, kv, kv_local = _c(q_attn, np.uint16), _c(kv, np.uint16), _c(kv_local, np.uint16)
+        indices, positions = _c(indices, np.int32), _c(positions, np.int32)
+        T, Hq, Dkv = q_attn.shape
+        k_top = indices.shape[1]
+        out = np.empty((T, Hq, Dkv), dtype=np.uint16)
+        lse = np.empty((T, Hq), dtype=np.float32)
+        rc = self.lib.ds4x_ref_local_pooled_attn(_ptr(q_attn), _ptr(kv), _ptr(kv_local), DTYPES[dtype],
+                                                 _ptr(indices), _ptr(positions), T, Hq, Dkv, S, k_top,
+                                                 local_pos0, kv_local.shape[0], window, scale, _ptr(out),
+                                                 _ptr(lse))
+        assert rc == 0, rc
+        return out, lse
+
+    def index_and_attend_local(self, q, w, k, positions, q_attn, kv, kv_local, kv_dtype, S, ratio, k_top,
+                               local_pos0, window, scale):
+        """The whole path with local-plus-pooled attention. Returns (indices, out bits, lse)."""
+        q, w, k = _c(q, np.uint16), _c(w, np.uint16), _c(k, np.uint16)
+        q_attn, kv, kv_local = _c(q_attn, np.uint16), _c(kv, np.uint16), _c(kv_local, np.uint16)
+        positions = _c(positions, np.int32)
+        T, H, D = q.shape
+        _, Hq, Dkv = q_attn.shape
+        idx = np.empty((T, k_top), dtype=np.int32)
+        out = np.empty((T, Hq, Dkv), dtype=np.uint16)
+        lse = np.empty((T, Hq), dtype=np.float32)
+        rc = self.lib.ds4x_ref_index_and_attend_local(
+            _ptr(q), _ptr(w), _ptr(k), _ptr(positions), _ptr(q_attn), _ptr(kv), _ptr(kv_local),
+            DTYPES[kv_dtype], T, H, D, S, ratio, k_top, Hq, Dkv, local_pos0, kv_local.shape[0], window, scale,
+            _ptr(idx), _ptr(out), _ptr(lse))
+        assert rc == 0, rc
+        return idx, out, lse
 
     def decode(self, q, w, q_attn, k, kv, kv_dtype, S0, pos0, ratio, k_new, kv_new, k_top, scale):
         """The decode loop on copies of k / kv (capacity = their row count).
@@ -202,3 +241,11 @@ def index_and_attend(*a, **kw):
 
 def decode(*a, **kw):
     return default().decode(*a, **kw)
+
+
+def local_pooled_attn(*a, **kw):
+    return default().local_pooled_attn(*a, **kw)
+
+
+def index_and_attend_local(*a, **kw):
+    return default().index_and_attend_local(*a, **kw)

@@ -22,6 +22,14 @@
  *  - The decode loop: one pooled row per `ratio` positions ("How I turned one oversized
  *    DeepSeek optimization into three merged oMLX PRs", section "The three changes that
  *    merged"), decode at long context ("How I made DeepSeek 12x faster on a Mac Studio").
+ *  - Local-plus-pooled attention: "How I turned one oversized DeepSeek optimization into
+ *    three merged oMLX PRs", section "The three changes that merged", item 1 (compressed
+ *    attention draws on local and pooled key/value state; the native kernel takes both in
+ *    one pass), and the ds4.c overview, section on the disk cache layout (the live raw
+ *    sliding-window KV rows are state of their own).  The pages give no window size and no
+ *    rule for joining the two sources; the reading here: the raw rows of the positions
+ *    p - window + 1 .. p (none below 0) join the selected pooled rows in one softmax with
+ *    the same query and scale, nothing de-duplicated.
  *  - The formula (which the pages leave unstated) is this library's definition:
  *    score[t,s] = sum_h w[t,h] * ReLU(q[t,h,:] . k[s,:]), row s visible iff
  *    (s+1)*ratio <= p+1, ties to the lower row index, indices ascending, attention with
@@ -33,7 +41,10 @@
  * invariants of the selection, the closed-form attention cases (zero query ->
  * mean of the rows, one row -> that row, two rows -> logistic weights), and for the
  * decode loop the closed-form row count per step, the appended bytes and a numpy
- * brute-force of every step on tiny inputs.
+ * brute-force of every step on tiny inputs; for local-plus-pooled attention a textbook
+ * sliding-window attention in numpy, a numpy softmax over the union of both sources, the
+ * log-sum-exp merge of the two one-source results, the exact mean for a zero query and a
+ * one-row window.
  */
 #include <math.h>
 #include <stdint.h>
@@ -294,17 +305,69 @@ int ds4x_ref_sparse_attn(const uint16_t* q_attn, const uint16_t* kv, int dtype,
   return 0;
 }
 
+/* ---- local-plus-pooled attention ---------------------------------------------------- */
+
+/* The raw rows in a token's sliding window: the positions a with p - window < a <= p and
+ * a >= 0 that kv_local holds (its row r is the raw row of position local_pos0 + r, r < L),
+ * in ascending position.  Writes their kv_local row numbers and returns how many. */
+static int32_t ref_window_rows(int64_t p, int32_t window, int64_t local_pos0, int32_t L,
+                               int32_t* rows) {
+  int32_t n = 0;
+  for (int64_t a = p - window + 1; a <= p; ++a) {
+    if (a < 0) continue;
+    int64_t r = a - local_pos0;
+    if (r < 0 || r >= L) continue;
+    rows[n++] = (int32_t)r;
+  }
+  return n;
+}
+
+/* One softmax over two row sources: the token's valid selected pooled rows (as in
+ * ds4x_ref_sparse_attn) followed by the raw rows of its sliding window.  Both sources are
+ * keys and values; the logits share q_attn and scale.  window = 0 or L = 0 gives
+ * ds4x_ref_sparse_attn. */
+int ds4x_ref_local_pooled_attn(const uint16_t* q_attn, const uint16_t* kv,
+                               const uint16_t* kv_local, int dtype, const int32_t* indices,
+                               const int32_t* positions, int32_t T, int32_t Hq, int32_t Dkv,
+                               int32_t S, int32_t k_top, int32_t local_pos0, int32_t L,
+                               int32_t window, float scale, uint16_t* out, float* lse) {
+  if (T < 0 || Hq <= 0 || Dkv <= 0 || S < 0 || k_top < 1 || L < 0 || window < 0 || local_pos0 < 0)
+    return -1;
+  const int64_t cap = (int64_t)k_top + window;
+#pragma omp parallel
+  {
+    double* qd = (double*)malloc(sizeof(double) * (size_t)Hq * Dkv);
+    double* rd = (double*)malloc(sizeof(double) * (size_t)cap * Dkv);
+    double* logit = (double*)malloc(sizeof(double) * (size_t)cap);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)Dkv);
+    int32_t* wrows = (int32_t*)malloc(sizeof(int32_t) * (size_t)(window > 0 ? window : 1));
+#pragma omp for schedule(dynamic, 1)
+    for (int32_t t = 0; t < T; ++t) {
+      const int32_t* sel = indices + (int64_t)t * k_top;
+      int32_t nv = 0;
+      for (int32_t j = 0; j < k_top; ++j)
+        if (sel[j] >= 0 && sel[j] < S)
+          ref_decode_n(kv + (int64_t)sel[j] * Dkv, Dkv, dtype, rd + (int64_t)(nv++) * Dkv);
+      const int32_t nw = ref_window_rows(positions[t], window, local_pos0, L, wrows);
+      for (int32_t j = 0; j < nw; ++j)
+        ref_decode_n(kv_local + (int64_t)wrows[j] * Dkv, Dkv, dtype, rd + (int64_t)(nv++) * Dkv);
+      ref_decode_n(q_attn + (int64_t)t * Hq * Dkv, (int64_t)Hq * Dkv, dtype, qd);
+      ref_attend_token(qd, rd, nv, Hq, Dkv, (double)scale, dtype,
+                       out + (int64_t)t * Hq * Dkv, lse ? lse + (int64_t)t * Hq : NULL,
+                       logit, acc);
+    }
+    free(qd); free(rd); free(logit); free(acc); free(wrows);
+  }
+  return 0;
+}
+
 /* ---- the whole path ----------------------------------------------------------------- */
 
-/* score -> top-k (with the shortcut) -> attention.  A token covered by the shortcut
- * (n_vis <= k_top) is never scored. */
-int ds4x_ref_index_and_attend(const uint16_t* q, const uint16_t* w, const uint16_t* k,
-                              const int32_t* positions, const uint16_t* q_attn,
-                              const uint16_t* kv, int kv_dtype, int32_t T, int32_t H,
-                              int32_t D, int32_t S, int32_t ratio, int32_t k_top,
-                              int32_t Hq, int32_t Dkv, float scale, int32_t* indices,
-                              uint16_t* out, float* lse) {
-  if (T < 0 || H <= 0 || D <= 0 || S < 0 || ratio < 1 || k_top < 1) return -1;
+/* score -> top-k (with the shortcut): the indices of every token.  A token covered by the
+ * shortcut (n_vis <= k_top) is never scored. */
+static void ref_index_select(const uint16_t* q, const uint16_t* w, const uint16_t* k,
+                             const int32_t* positions, int32_t T, int32_t H, int32_t D,
+                             int32_t S, int32_t ratio, int32_t k_top, int32_t* indices) {
   double* kd = (double*)malloc(sizeof(double) * (size_t)((int64_t)S * D + 1));
   ref_decode_n(k, (int64_t)S * D, REF_F16, kd);
 #pragma omp parallel
@@ -328,7 +391,33 @@ int ds4x_ref_index_and_attend(const uint16_t* q, const uint16_t* w, const uint16
     free(qd); free(wd); free(row);
   }
   free(kd);
+}
+
+/* score -> top-k (with the shortcut) -> attention. */
+int ds4x_ref_index_and_attend(const uint16_t* q, const uint16_t* w, const uint16_t* k,
+                              const int32_t* positions, const uint16_t* q_attn,
+                              const uint16_t* kv, int kv_dtype, int32_t T, int32_t H,
+                              int32_t D, int32_t S, int32_t ratio, int32_t k_top,
+                              int32_t Hq, int32_t Dkv, float scale, int32_t* indices,
+                              uint16_t* out, float* lse) {
+  if (T < 0 || H <= 0 || D <= 0 || S < 0 || ratio < 1 || k_top < 1) return -1;
+  ref_index_select(q, w, k, positions, T, H, D, S, ratio, k_top, indices);
   return ds4x_ref_sparse_attn(q_attn, kv, kv_dtype, indices, T, Hq, Dkv, S, k_top, scale, out, lse);
+}
+
+/* score -> top-k (with the shortcut) -> local-plus-pooled attention. */
+int ds4x_ref_index_and_attend_local(const uint16_t* q, const uint16_t* w, const uint16_t* k,
+                                    const int32_t* positions, const uint16_t* q_attn,
+                                    const uint16_t* kv, const uint16_t* kv_local, int kv_dtype,
+                                    int32_t T, int32_t H, int32_t D, int32_t S, int32_t ratio,
+                                    int32_t k_top, int32_t Hq, int32_t Dkv, int32_t local_pos0,
+                                    int32_t L, int32_t window, float scale, int32_t* indices,
+                                    uint16_t* out, float* lse) {
+  if (T < 0 || H <= 0 || D <= 0 || S < 0 || ratio < 1 || k_top < 1 || L < 0 || window < 0)
+    return -1;
+  ref_index_select(q, w, k, positions, T, H, D, S, ratio, k_top, indices);
+  return ds4x_ref_local_pooled_attn(q_attn, kv, kv_local, kv_dtype, indices, positions, T, Hq,
+                                    Dkv, S, k_top, local_pos0, L, window, scale, out, lse);
 }
 
 /* ---- the decode loop ------------------------------------------------------------------ */

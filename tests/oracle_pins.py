@@ -16,7 +16,11 @@ Independent facts used:
   * closed-form attention cases (zero query, single row, two rows) and a textbook
     float64 numpy softmax-attention;
   * for the decode loop: the closed-form row count of every step, the appended bytes, and a
-    numpy brute-force (definition score, sorted() ranking, textbook attention) of each step.
+    numpy brute-force (definition score, sorted() ranking, textbook attention) of each step;
+  * for local-plus-pooled attention: a textbook float64 causal sliding-window attention, a
+    float64 softmax over the union of both row sources, the log-sum-exp merge identity of two
+    one-source results, the exact rational mean for a zero query, a one-row window giving that
+    row, and the pooled result whenever no raw row is in reach.
 """
 from __future__ import annotations
 
@@ -423,11 +427,157 @@ def check_decode_steps_brute_force(o):
         assert np.allclose(lse[i], m[:, 0] + np.log(pr.sum(axis=1)), rtol=1e-6, atol=1e-6)
 
 
+# ------------------------------------------------------------ local-plus-pooled attention
+def _softmax_rows(qf, V, scale):
+    """Textbook float64 softmax attention of the heads qf [Hq, Dkv] over the rows V [n, Dkv]."""
+    logits = scale * qf @ V.T
+    m = logits.max(axis=1, keepdims=True)
+    p = np.exp(logits - m)
+    return (p / p.sum(axis=1, keepdims=True)) @ V, m[:, 0] + np.log(p.sum(axis=1))
+
+
+def _raw_window(p, W, local_pos0, L):
+    """Positions of the raw rows a token at p attends: p-W < a <= p, a >= 0, held by the buffer."""
+    return [a for a in range(p - W + 1, p + 1) if a >= 0 and local_pos0 <= a < local_pos0 + L]
+
+
+def check_local_only_vs_textbook(o):
+    # no pooled row at all: causal sliding-window attention over a raw sequence X, of which the
+    # buffer holds positions 6..19; tokens before, inside and after the buffer, and p < 0
+    rng = np.random.default_rng(11)
+    N, Dkv, Hq, W, lp0, L = 24, 32, 4, 5, 6, 14
+    X = synth.to_bf16_bits(rng.standard_normal((N, Dkv)))
+    pos = np.array([0, 3, 6, 8, 10, 13, 19, 21, 30, -2], dtype=np.int32)
+    T = len(pos)
+    qa = synth.to_bf16_bits(rng.standard_normal((T, Hq, Dkv)))
+    ind = np.full((T, 4), -1, dtype=np.int32)
+    scale = 0.3
+    out, lse = o.local_pooled_attn(qa, X[:2], X[lp0:lp0 + L], "bf16", ind, pos, 2, lp0, W, scale)
+    Xf = _bits_val(X, "bf16")
+    for t, p in enumerate(pos):
+        rows = [a for a in range(max(0, p - W + 1, lp0), min(p, lp0 + L - 1) + 1)]
+        assert rows == _raw_window(int(p), W, lp0, L)
+        if not rows:
+            assert np.all(out[t] == 0) and np.all(np.isneginf(lse[t])), (t, p)
+            continue
+        if len(rows) == 1:                                   # one row: softmax weight exactly 1
+            assert all(np.array_equal(out[t, h], X[rows[0]]) for h in range(Hq))
+        ref, rlse = _softmax_rows(_bits_val(qa[t], "bf16"), Xf[rows], scale)
+        assert np.allclose(_bits_val(out[t], "bf16"), ref, rtol=2 ** -8, atol=1e-6), (t, p)
+        assert np.allclose(lse[t], rlse, rtol=1e-6, atol=1e-6)
+
+
+def _union_case(seed, dtype):
+    rng = np.random.default_rng(seed)
+    S, N, Dkv, Hq, W, lp0, k_top = 30, 40, 32, 4, 7, 9, 6
+    L = 25                                                   # raw positions 9..33
+    kv = synth.to_bits(rng.standard_normal((S, Dkv)), dtype)
+    X = synth.to_bits(rng.standard_normal((N, Dkv)), dtype)
+    pos = np.array([9, 12, 20, 33, 36, 5], dtype=np.int32)
+    T = len(pos)
+    qa = synth.to_bits(rng.standard_normal((T, Hq, Dkv)), dtype)
+    ind = np.stack([rng.choice(S, k_top, replace=False) for _ in range(T)]).astype(np.int32)
+    ind[1, -2:] = -1
+    ind[2, 0] = S + 3                                        # out of range -> skipped
+    ind[4, :] = -1                                           # window rows only
+    return dict(S=S, W=W, lp0=lp0, L=L, kv=kv, X=X, kv_local=X[lp0:lp0 + L], pos=pos, qa=qa, ind=ind)
+
+
+def check_local_pooled_union_vs_textbook(o):
+    c = _union_case(12, "bf16")
+    scale = 1.0 / math.sqrt(32)
+    out, lse = o.local_pooled_attn(c["qa"], c["kv"], c["kv_local"], "bf16", c["ind"], c["pos"], c["S"],
+                                   c["lp0"], c["W"], scale)
+    kvf, Xf = _bits_val(c["kv"], "bf16"), _bits_val(c["X"], "bf16")
+    for t, p in enumerate(c["pos"]):
+        pooled = [int(i) for i in c["ind"][t] if 0 <= i < c["S"]]
+        raw = _raw_window(int(p), c["W"], c["lp0"], c["L"])
+        V = np.concatenate([kvf[pooled], Xf[raw]])
+        ref, rlse = _softmax_rows(_bits_val(c["qa"][t], "bf16"), V, scale)
+        assert np.allclose(_bits_val(out[t], "bf16"), ref, rtol=2 ** -8, atol=1e-6), t
+        assert np.allclose(lse[t], rlse, rtol=1e-6, atol=1e-6), t
+
+
+def check_local_pooled_lse_merge(o):
+    # softmax over a union = the two one-source results weighted by exp(lse_i - lse):
+    #   lse = log(e^lse_p + e^lse_l),  out = e^(lse_p - lse) out_p + e^(lse_l - lse) out_l
+    c = _union_case(13, "f16")
+    scale = 0.2
+    T = len(c["pos"])
+    out, lse = o.local_pooled_attn(c["qa"], c["kv"], c["kv_local"], "f16", c["ind"], c["pos"], c["S"],
+                                   c["lp0"], c["W"], scale)
+    out_p, lse_p = o.sparse_attn(c["qa"], c["kv"], "f16", c["ind"], c["S"], scale)
+    none = np.full_like(c["ind"], -1)
+    out_l, lse_l = o.local_pooled_attn(c["qa"], c["kv"], c["kv_local"], "f16", none, c["pos"], c["S"],
+                                       c["lp0"], c["W"], scale)
+    lp, ll = lse_p.astype(np.float64), lse_l.astype(np.float64)
+    merged_lse = np.logaddexp(lp, ll)
+    assert np.allclose(lse, merged_lse, rtol=1e-6, atol=1e-6)
+    wp = np.exp(lp - merged_lse)[..., None]
+    wl = np.exp(ll - merged_lse)[..., None]
+    op, ol = _bits_val(out_p, "f16"), _bits_val(out_l, "f16")
+    merged = wp * op + wl * ol
+    got = _bits_val(out, "f16")
+    # every output carries one f16 rounding (2^-11 relative, 2^-25 absolute below the normal
+    # range) and the lse values are fp32 (the weights then err by ~1e-6 relative)
+    bound = (2 ** -11 * (wp * np.abs(op) + wl * np.abs(ol) + np.abs(got)) + 1e-5 * (np.abs(op) + np.abs(ol))
+             + 2 ** -24)
+    assert np.all(np.abs(got - merged) <= bound), np.abs(got - merged).max()
+    assert T == out.shape[0]
+
+
+def check_local_zero_query_is_mean(o):
+    # equal logits: the output is the exact rational mean of every pooled and raw row, rounded once
+    c = _union_case(14, "bf16")
+    qa = np.zeros_like(c["qa"])
+    out, lse = o.local_pooled_attn(qa, c["kv"], c["kv_local"], "bf16", c["ind"], c["pos"], c["S"],
+                                   c["lp0"], c["W"], 0.5)
+    kvf, Xf = _bits_val(c["kv"], "bf16"), _bits_val(c["X"], "bf16")
+    for t, p in enumerate(c["pos"]):
+        rows = [kvf[int(i)] for i in c["ind"][t] if 0 <= i < c["S"]]
+        rows += [Xf[a] for a in _raw_window(int(p), c["W"], c["lp0"], c["L"])]
+        n = len(rows)
+        mean = [_rne_fraction(sum(Fraction(float(r[d])) for r in rows) / n, 7, 8) for d in range(len(rows[0]))]
+        for h in range(qa.shape[1]):
+            got = _bits_val(out[t, h], "bf16")
+            assert all(Fraction(float(g)) == m for g, m in zip(got, mean)), (t, h)
+            assert abs(lse[t, h] - math.log(n)) < 1e-6
+
+
+def check_local_window_off_is_sparse_attn(o):
+    # no raw row in reach (window 0, an empty buffer, a buffer past every token): the pooled
+    # result, bit for bit
+    c = _union_case(15, "bf16")
+    ref = o.sparse_attn(c["qa"], c["kv"], "bf16", c["ind"], c["S"], 0.25)
+    for kv_local, lp0, W in ((c["kv_local"], c["lp0"], 0), (c["kv_local"][:0], c["lp0"], 7),
+                             (c["kv_local"], 1000, 7)):
+        got = o.local_pooled_attn(c["qa"], c["kv"], kv_local, "bf16", c["ind"], c["pos"], c["S"], lp0, W, 0.25)
+        assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
+
+
+def check_index_and_attend_local_composes(o):
+    wl = synth.WORKLOADS["tiny_exact"]
+    inp = synth.make_inputs(wl, seed=0, T=6, S=1024)
+    pos = np.array([5, 2047, 2048, 2051, 4000, 4095], dtype=np.int32)
+    rng = np.random.default_rng(16)
+    lp0, L, W = 1990, 2106, 64
+    kv_local = synth.to_f16_bits(rng.integers(-2, 3, size=(L, wl.Dkv)).astype(np.float64))
+    idx, out, lse = o.index_and_attend_local(inp.q, inp.w, inp.k, pos, inp.q_attn, inp.kv, kv_local, "f16",
+                                             wl.S, wl.ratio, wl.k_top, lp0, W, wl.scale)
+    idx2, _, _ = o.index_and_attend(inp.q, inp.w, inp.k, pos, inp.q_attn, inp.kv, "f16", wl.S, wl.ratio,
+                                    wl.k_top, wl.scale)
+    out2, lse2 = o.local_pooled_attn(inp.q_attn, inp.kv, kv_local, "f16", idx2, pos, wl.S, lp0, W, wl.scale)
+    assert np.array_equal(idx, idx2)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
 ALL_CHECKS = [
     check_f16_decode_exhaustive, check_bf16_decode_exhaustive, check_encode_rne,
     check_visibility, check_golden_example, check_scores_int64_closed_form,
     check_scores_float_vs_numpy, check_topk_brute_force, check_topk_invariants,
     check_shortcut, check_attn_zero_query_is_mean, check_attn_single_row,
     check_attn_two_rows_logistic, check_attn_vs_textbook, check_index_and_attend_composes,
-    check_decode_schedule, check_decode_steps_brute_force,
+    check_decode_schedule, check_decode_steps_brute_force, check_local_only_vs_textbook,
+    check_local_pooled_union_vs_textbook, check_local_pooled_lse_merge, check_local_zero_query_is_mean,
+    check_local_window_off_is_sparse_attn, check_index_and_attend_local_composes,
 ]

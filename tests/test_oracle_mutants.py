@@ -39,6 +39,15 @@ MUTANTS = {
     "decode_append_one_early": ("(int64_t)S < (p + 1) / ratio) {", "(int64_t)S <= (p + 1) / ratio) {"),
     "decode_position_shifted": ("const int64_t p = (int64_t)pos0 + i;", "const int64_t p = (int64_t)pos0 + i + 1;"),
     "decode_first_staged_row_only": ("kv_new + (int64_t)a * Dkv,", "kv_new,"),
+    "window_shifted_one_back": ("for (int64_t a = p - window + 1; a <= p; ++a) {",
+                                "for (int64_t a = p - window; a < p; ++a) {"),
+    "window_excludes_own_position": ("for (int64_t a = p - window + 1; a <= p; ++a) {",
+                                     "for (int64_t a = p - window + 1; a < p; ++a) {"),
+    "window_buffer_offset_sign": ("int64_t r = a - local_pos0;", "int64_t r = a - local_pos0 - 1;"),
+    "window_rows_dropped": ("for (int32_t j = 0; j < nw; ++j)", "for (int32_t j = 0; j < 0; ++j)"),
+    "window_rows_from_pooled_kv": ("ref_decode_n(kv_local + (int64_t)wrows[j] * Dkv",
+                                   "ref_decode_n(kv + (int64_t)wrows[j] * Dkv"),
+    "window_of_first_token": ("ref_window_rows(positions[t], window", "ref_window_rows(positions[0], window"),
     "w_index_transposed": ("ref_decode_n(w + (int64_t)t * H, H, REF_F16, wd);\n      int64_t n",
                            "ref_decode_n(w + (int64_t)t, H, REF_F16, wd);\n      int64_t n"),
 }
