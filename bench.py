@@ -77,6 +77,10 @@ def workload_config(wl: synth.Workload, l2_note: str) -> dict:
         "T": wl.T, "S": wl.S, "H": wl.H, "D": wl.D, "ratio": wl.ratio, "k_top": wl.k_top,
         "Hq": wl.Hq, "Dkv": wl.Dkv, "kv_dtype": wl.kv_dtype, "seed": 0,
         "l2": l2_note,
+        **({"window": wl.window,
+            "attention": f"local-plus-pooled: each token's top-{wl.k_top} pooled rows and the raw rows of its "
+                         f"last {wl.window} positions in one softmax (kv_local[{wl.T + wl.window - 1},{wl.Dkv}])"}
+           if wl.window > 0 else {}),
     }
 
 
@@ -85,16 +89,22 @@ def visible_rows(wl: synth.Workload) -> np.ndarray:
     return np.minimum(wl.S, (p + 1) // wl.ratio)
 
 
+def window_rows(wl: synth.Workload) -> np.ndarray:
+    """Raw rows each token attends: its last `window` positions (none below 0)."""
+    p = wl.pos0 + np.arange(wl.T, dtype=np.int64)
+    return np.minimum(p + 1, wl.window) if wl.window > 0 else np.zeros(wl.T, dtype=np.int64)
+
+
 def algorithmic(wl: synth.Workload) -> dict:
     nv = visible_rows(wl)
     scored = nv[nv > wl.k_top]
-    sel = np.minimum(nv, wl.k_top)
+    sel = np.minimum(nv, wl.k_top) + window_rows(wl)
     return {
         # scoring: one multiply-add per (token, head, dim, visible row)
         "score_flops": float(2 * wl.H * wl.D * scored.sum()),
         # top-k: read every visible score once, write k_top indices per token
         "topk_bytes": float(4 * scored.sum() + 4 * wl.k_top * wl.T),
-        # attention: two products of 2*Hq*Dkv flops per (token, selected row)
+        # attention: two products of 2*Hq*Dkv flops per (token, attended row: pooled and window)
         "attn_flops": float(4 * wl.Hq * wl.Dkv * sel.sum()),
         "attn_gather_bytes": float(2 * wl.Dkv * sel.sum()),
     }
@@ -179,6 +189,17 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------- CPU oracle
+def oracle_path(o, wl: synth.Workload, inp, sel):
+    """The oracle's whole path on the tokens `sel` of the chunk."""
+    if wl.window > 0:
+        o.index_and_attend_local(inp.q[sel], inp.w[sel], inp.k, inp.positions[sel], inp.q_attn[sel], inp.kv,
+                                 inp.kv_local, wl.kv_dtype, wl.S, wl.ratio, wl.k_top, inp.local_pos0, wl.window,
+                                 wl.scale)
+    else:
+        o.index_and_attend(inp.q[sel], inp.w[sel], inp.k, inp.positions[sel], inp.q_attn[sel], inp.kv,
+                           wl.kv_dtype, wl.S, wl.ratio, wl.k_top, wl.scale)
+
+
 def cpu_baseline(wl: synth.Workload, inp, target_s: float = 12.0, first: int = 16):
     """The oracle as it stands (whole path, fp64, OpenMP over tokens) on a bounded sample of
     the workload's tokens; returns (tokens/s, threads, description)."""
@@ -189,8 +210,7 @@ def cpu_baseline(wl: synth.Workload, inp, target_s: float = 12.0, first: int = 1
     def run(n):
         sel = np.linspace(0, wl.T - 1, n).astype(np.int64)
         t0 = time.perf_counter()
-        o.index_and_attend(inp.q[sel], inp.w[sel], inp.k, inp.positions[sel], inp.q_attn[sel], inp.kv,
-                           wl.kv_dtype, wl.S, wl.ratio, wl.k_top, wl.scale)
+        oracle_path(o, wl, inp, sel)
         return time.perf_counter() - t0
 
     dt = run(first)
@@ -214,8 +234,7 @@ def run_reference(args, wl):
 
     def step():
         sel = np.sort(rng.choice(wl.T, per_step, replace=False))
-        o.index_and_attend(inp.q[sel], inp.w[sel], inp.k, inp.positions[sel], inp.q_attn[sel], inp.kv,
-                           wl.kv_dtype, wl.S, wl.ratio, wl.k_top, wl.scale)
+        oracle_path(o, wl, inp, sel)
 
     for _ in range(args.warmup):
         step()
@@ -407,9 +426,12 @@ def main():
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory()
     h = {"q": pinned16(inp.q), "w": pinned16(inp.w), "k": pinned16(inp.k), "q_attn": pinned16(inp.q_attn),
          "kv": pinned16(inp.kv), "positions": torch.from_numpy(inp.positions.copy()).pin_memory()}
+    win = wl.window > 0
+    if win:
+        h["kv_local"] = pinned16(inp.kv_local)
     kvt = torch.bfloat16 if wl.kv_dtype == "bf16" else torch.float16
     dt_of = {"q": torch.float16, "w": torch.float16, "k": torch.float16, "q_attn": kvt, "kv": kvt,
-             "positions": torch.int32}
+             "positions": torch.int32, "kv_local": kvt}
     d = {n: h[n].to(dev).view(dt_of[n]) for n in h}
     T, S, k_top = wl.T, wl.S, wl.k_top
     scores = torch.empty((T, S), dtype=torch.float32, device=dev)
@@ -417,15 +439,20 @@ def main():
     cnt = torch.empty((T,), dtype=torch.int32, device=dev)
     out = torch.empty_like(d["q_attn"])
     lse = torch.empty((T, wl.Hq), dtype=torch.float32, device=dev)
-    ws = torch.empty((max(1, ds4x.workspace_bytes(T, S, k_top)),), dtype=torch.uint8, device=dev)
+    ws = torch.empty((max(1, ds4x.workspace_bytes_local(T, S, k_top, wl.window)),), dtype=torch.uint8, device=dev)
     tws_n = ds4x.topk_workspace_bytes(T, S, k_top)
     tws = torch.empty((max(1, tws_n),), dtype=torch.uint8, device=dev) if tws_n else None
     flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def fused():
-        ds4x.index_and_attend(d["q"], d["w"], d["k"], d["positions"], d["q_attn"], d["kv"], wl.ratio, k_top,
-                              S=S, scale=wl.scale, indices=idx, out=out, lse=lse, workspace=ws, stream=stream)
+        if win:
+            ds4x.index_and_attend_local(d["q"], d["w"], d["k"], d["positions"], d["q_attn"], d["kv"], d["kv_local"],
+                                        wl.ratio, inp.local_pos0, wl.window, k_top, S=S, scale=wl.scale,
+                                        indices=idx, out=out, lse=lse, workspace=ws, stream=stream)
+        else:
+            ds4x.index_and_attend(d["q"], d["w"], d["k"], d["positions"], d["q_attn"], d["kv"], wl.ratio, k_top,
+                                  S=S, scale=wl.scale, indices=idx, out=out, lse=lse, workspace=ws, stream=stream)
         return ds4x.last_launch_count()
 
     def staged(ev):
@@ -437,7 +464,11 @@ def main():
                   stream=stream)
         n += ds4x.last_launch_count()
         ev[2].record(stream)
-        ds4x.sparse_attn(d["q_attn"], d["kv"], idx, S=S, scale=wl.scale, out=out, lse=lse, stream=stream)
+        if win:
+            ds4x.local_pooled_attn(d["q_attn"], d["kv"], d["kv_local"], idx, d["positions"], inp.local_pos0,
+                                   wl.window, S=S, scale=wl.scale, out=out, lse=lse, stream=stream)
+        else:
+            ds4x.sparse_attn(d["q_attn"], d["kv"], idx, S=S, scale=wl.scale, out=out, lse=lse, stream=stream)
         n += ds4x.last_launch_count()
         ev[3].record(stream)
         return n
@@ -492,13 +523,21 @@ def main():
         # the public host-buffer call: it copies the inputs in, runs the path and copies the
         # outputs back, overlapping the copies with the work by sub-chunks of tokens
         hv = {n: h[n].view(dt_of[n]) for n in h}
-        hbuf = torch.empty((ds4x.index_and_attend_host_bytes(T, wl.H, wl.D, S, k_top, wl.Hq, wl.Dkv,
-                                                             args.host_chunks),), dtype=torch.uint8, device=dev)
+        L = inp.kv_local.shape[0] if win else 0
+        hbuf = torch.empty((ds4x.index_and_attend_local_host_bytes(T, wl.H, wl.D, S, k_top, wl.Hq, wl.Dkv, L,
+                                                                   wl.window, args.host_chunks),),
+                           dtype=torch.uint8, device=dev)
 
         def e2e_step():
-            ds4x.index_and_attend_host(hv["q"], hv["w"], hv["k"], hv["positions"], hv["q_attn"], hv["kv"], wl.ratio,
-                                       k_top, S=S, scale=wl.scale, n_chunks=args.host_chunks, indices=h_idx,
-                                       out=h_out, lse=h_lse, device_buffer=hbuf, stream=stream)
+            if win:
+                ds4x.index_and_attend_local_host(hv["q"], hv["w"], hv["k"], hv["positions"], hv["q_attn"], hv["kv"],
+                                                 hv["kv_local"], wl.ratio, inp.local_pos0, wl.window, k_top, S=S,
+                                                 scale=wl.scale, n_chunks=args.host_chunks, indices=h_idx, out=h_out,
+                                                 lse=h_lse, device_buffer=hbuf, stream=stream)
+            else:
+                ds4x.index_and_attend_host(hv["q"], hv["w"], hv["k"], hv["positions"], hv["q_attn"], hv["kv"],
+                                           wl.ratio, k_top, S=S, scale=wl.scale, n_chunks=args.host_chunks,
+                                           indices=h_idx, out=h_out, lse=h_lse, device_buffer=hbuf, stream=stream)
 
         e2e_step()
         barrier()
@@ -515,7 +554,8 @@ def main():
             e_ms = float(t.item())
         e2e = {"value": world * T / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms,
-               "call": "ds4x_index_and_attend_host (page-locked host buffers; copies in, work and copies out "
+               "call": ("ds4x_index_and_attend_local_host" if win else "ds4x_index_and_attend_host") +
+                       " (page-locked host buffers; copies in, work and copies out "
                        "overlapped by sub-chunks of tokens)", "host_chunks": args.host_chunks}
 
     # ------------------------------------------------------------------ roofline

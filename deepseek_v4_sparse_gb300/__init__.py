@@ -24,12 +24,15 @@ LIB_PATH = os.path.join(_HERE, "libds4x.so")
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
 F16, BF16 = 0, 1
 MAX_KTOP = 1024
+MAX_WINDOW = 1024
 EXPORTS = (
     "ds4x_indexer_score", "ds4x_topk", "ds4x_topk_workspace_bytes", "ds4x_sparse_attn",
     "ds4x_index_and_attend", "ds4x_workspace_bytes", "ds4x_status_string",
     "ds4x_last_launch_count", "ds4x_device_status", "ds4x_selftest_bounded_wait",
     "ds4x_topk_static_scratch", "ds4x_decode", "ds4x_decode_workspace_bytes",
     "ds4x_index_and_attend_host", "ds4x_index_and_attend_host_bytes",
+    "ds4x_local_pooled_attn", "ds4x_index_and_attend_local", "ds4x_workspace_bytes_local",
+    "ds4x_index_and_attend_local_host", "ds4x_index_and_attend_local_host_bytes",
 )
 
 _lock = threading.Lock()
@@ -65,6 +68,17 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                                    i32, i32, i32, f32, P, P, P, i32, P, sz, P]
         lib.ds4x_index_and_attend_host_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
         lib.ds4x_index_and_attend_host_bytes.restype = sz
+        lib.ds4x_local_pooled_attn.argtypes = [P, P, P, ctypes.c_int, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                               i32, f32, P, P, P]
+        lib.ds4x_index_and_attend_local.argtypes = [P, P, P, P, P, P, P, ctypes.c_int, i32, i32, i32, i32, i32,
+                                                    i32, i32, i32, i32, i32, i32, f32, P, P, P, P, sz, P]
+        lib.ds4x_workspace_bytes_local.argtypes = [i32, i32, i32, i32]
+        lib.ds4x_workspace_bytes_local.restype = sz
+        lib.ds4x_index_and_attend_local_host.argtypes = [P, P, P, P, P, P, P, ctypes.c_int, i32, i32, i32, i32,
+                                                         i32, i32, i32, i32, i32, i32, i32, f32, P, P, P, i32, P,
+                                                         sz, P]
+        lib.ds4x_index_and_attend_local_host_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, i32]
+        lib.ds4x_index_and_attend_local_host_bytes.restype = sz
         lib.ds4x_decode.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, P, i32, i32, i32, i32, i32, i32, i32,
                                     i32, i32, f32, P, P, P, P, P, sz, ctypes.POINTER(i32), P]
         lib.ds4x_decode_workspace_bytes.argtypes = [i32, i32]
@@ -75,7 +89,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.ds4x_device_status.argtypes = [P, ctypes.c_int]
         lib.ds4x_selftest_bounded_wait.argtypes = [i64, P]
         for f in ("ds4x_indexer_score", "ds4x_topk", "ds4x_sparse_attn", "ds4x_index_and_attend", "ds4x_decode",
-                  "ds4x_index_and_attend_host",
+                  "ds4x_index_and_attend_host", "ds4x_local_pooled_attn", "ds4x_index_and_attend_local",
+                  "ds4x_index_and_attend_local_host",
                   "ds4x_last_launch_count", "ds4x_device_status", "ds4x_selftest_bounded_wait"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
@@ -276,6 +291,104 @@ def index_and_attend_host(q, w, k, positions, q_attn, kv, ratio: int, k_top: int
         H, D, S, ratio, k_top, Hq, Dkv, scale, _host_ptr(indices), _host_ptr(out), _host_ptr(lse), n_chunks,
         _ptr(device_buffer), dbytes, _stream(stream))
     _check("ds4x_index_and_attend_host", rc)
+    return indices, out, lse
+
+
+# ------------------------------------------------------------------ local-plus-pooled attention
+def _rows(t):
+    return 0 if t is None else int(t.shape[0])
+
+
+def workspace_bytes_local(T: int, S: int, k_top: int, window: int) -> int:
+    return int(load().ds4x_workspace_bytes_local(T, S, k_top, window))
+
+
+def local_pooled_attn(q_attn, kv, kv_local, indices, positions, local_pos0: int, window: int,
+                      S: int | None = None, scale: float | None = None, out=None, lse=None,
+                      want_lse: bool = True, stream=None):
+    """One softmax over the selected pooled rows of kv and the raw window rows of kv_local
+    [L, 512] (row r = position local_pos0 + r). Returns (out, lse)."""
+    torch = _torch()
+    dt = _kv_dtype(q_attn)
+    if kv.dtype != q_attn.dtype or (kv_local is not None and kv_local.dtype != q_attn.dtype):
+        raise ValueError("kv, kv_local and q_attn must have the same dtype")
+    T, Hq, Dkv = q_attn.shape
+    S = kv.shape[0] if S is None else S
+    k_top = indices.shape[1]
+    scale = 1.0 / math.sqrt(Dkv) if scale is None else scale
+    if out is None:
+        out = torch.empty_like(q_attn)
+    if lse is None and want_lse:
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=q_attn.device)
+    rc = load().ds4x_local_pooled_attn(_ptr(q_attn), _ptr(kv), _ptr(kv_local), dt, _ptr(indices), _ptr(positions),
+                                       T, Hq, Dkv, S, k_top, local_pos0, _rows(kv_local), window, scale, _ptr(out),
+                                       _ptr(lse), _stream(stream))
+    _check("ds4x_local_pooled_attn", rc)
+    return out, lse
+
+
+def index_and_attend_local(q, w, k, positions, q_attn, kv, kv_local, ratio: int, local_pos0: int, window: int,
+                           k_top: int = 512, S: int | None = None, scale: float | None = None, indices=None,
+                           out=None, lse=None, workspace=None, want_lse: bool = True, stream=None):
+    """The whole path with local-plus-pooled attention. Returns (indices, out, lse)."""
+    torch = _torch()
+    dt = _kv_dtype(q_attn)
+    T, H, D = q.shape
+    _, Hq, Dkv = q_attn.shape
+    S = k.shape[0] if S is None else S
+    scale = 1.0 / math.sqrt(Dkv) if scale is None else scale
+    dev = q.device
+    if indices is None:
+        indices = torch.empty((T, k_top), dtype=torch.int32, device=dev)
+    if out is None:
+        out = torch.empty_like(q_attn)
+    if lse is None and want_lse:
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
+    need = workspace_bytes_local(T, S, k_top, window)
+    if workspace is None and need > 0:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().ds4x_index_and_attend_local(_ptr(q), _ptr(w), _ptr(k), _ptr(positions), _ptr(q_attn), _ptr(kv),
+                                            _ptr(kv_local), dt, T, H, D, S, ratio, k_top, Hq, Dkv, local_pos0,
+                                            _rows(kv_local), window, scale, _ptr(indices), _ptr(out), _ptr(lse),
+                                            _ptr(workspace), wbytes, _stream(stream))
+    _check("ds4x_index_and_attend_local", rc)
+    return indices, out, lse
+
+
+def index_and_attend_local_host_bytes(T: int, H: int, D: int, S: int, k_top: int, Hq: int, Dkv: int, L: int,
+                                      window: int, n_chunks: int = 0) -> int:
+    return int(load().ds4x_index_and_attend_local_host_bytes(T, H, D, S, k_top, Hq, Dkv, L, window, n_chunks))
+
+
+def index_and_attend_local_host(q, w, k, positions, q_attn, kv, kv_local, ratio: int, local_pos0: int,
+                                window: int, k_top: int = 512, S: int | None = None, scale: float | None = None,
+                                n_chunks: int = 0, indices=None, out=None, lse=None, device_buffer=None,
+                                want_lse: bool = True, device=None, stream=None):
+    """index_and_attend_host with the raw window (kv_local a CPU tensor too)."""
+    torch = _torch()
+    dt = _kv_dtype(q_attn)
+    T, H, D = q.shape
+    _, Hq, Dkv = q_attn.shape
+    S = k.shape[0] if S is None else S
+    L = _rows(kv_local)
+    scale = 1.0 / math.sqrt(Dkv) if scale is None else scale
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if indices is None:
+        indices = torch.empty((T, k_top), dtype=torch.int32).pin_memory()
+    if out is None:
+        out = torch.empty(q_attn.shape, dtype=q_attn.dtype).pin_memory()
+    if lse is None and want_lse:
+        lse = torch.empty((T, Hq), dtype=torch.float32).pin_memory()
+    need = index_and_attend_local_host_bytes(T, H, D, S, k_top, Hq, Dkv, L, window, n_chunks)
+    if device_buffer is None:
+        device_buffer = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
+    dbytes = device_buffer.numel() * device_buffer.element_size()
+    rc = load().ds4x_index_and_attend_local_host(
+        _host_ptr(q), _host_ptr(w), _host_ptr(k), _host_ptr(positions), _host_ptr(q_attn), _host_ptr(kv),
+        _host_ptr(kv_local), dt, T, H, D, S, ratio, k_top, Hq, Dkv, local_pos0, L, window, scale,
+        _host_ptr(indices), _host_ptr(out), _host_ptr(lse), n_chunks, _ptr(device_buffer), dbytes, _stream(stream))
+    _check("ds4x_index_and_attend_local_host", rc)
     return indices, out, lse
 
 

@@ -33,6 +33,24 @@ int current_device() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Window arguments: local_pos0 >= 0, L >= 0, 0 <= window <= DS4X_MAX_WINDOW, and a buffer (16-byte
+// aligned when it is device memory) whenever a row of it can be attended.
+int check_window(const void* kv_local, int32_t local_pos0, int32_t L, int32_t window, bool device) {
+  if (local_pos0 < 0 || L < 0 || window < 0) return DS4X_ERR_INVALID;
+  if (window > DS4X_MAX_WINDOW) return DS4X_ERR_UNSUPPORTED;
+  if (window > 0 && L > 0 && (!kv_local || (device && !aligned16(kv_local)))) return DS4X_ERR_INVALID;
+  return DS4X_OK;
+}
+
+LocalWindow window_of(const void* kv_local, int32_t local_pos0, int32_t L, int32_t window) {
+  LocalWindow lw;
+  lw.kv_local = kv_local;
+  lw.local_pos0 = local_pos0;
+  lw.L = L;
+  lw.window = window;
+  return lw;
+}
+
 }  // namespace
 
 void call_begin() { t_launches = 0; }
@@ -74,16 +92,18 @@ size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
 }  // namespace
 
 // Workspace of the fused path: [scores T x S fp32 | top-k scratch | split-attention scratch].
-size_t fused_workspace_bytes(int T, int S, int k_top) {
-  if (T <= 0 || S <= 0 || k_top <= 0) return 0;
-  return round256((size_t)T * (size_t)S * sizeof(float)) + round256(topk_workspace_bytes(T, S, k_top)) +
-         attn_partial_bytes(T, k_top);
+size_t fused_workspace_bytes(int T, int S, int k_top, int window) {
+  if (T <= 0 || k_top <= 0 || (S <= 0 && window <= 0)) return 0;
+  const size_t front = S > 0 ? round256((size_t)T * (size_t)S * sizeof(float)) +
+                                   round256(topk_workspace_bytes(T, S, k_top))
+                             : 0;
+  return front + attn_partial_bytes(T, k_top, window > 0 ? window : 0);
 }
 
 int run_index_and_attend(const void* q, const void* w, const void* k, const int32_t* positions, const void* q_attn,
                          const void* kv, int bf16, int T, int H, int D, int S, int ratio, int k_top, float scale,
                          int32_t* indices, void* out, float* lse, void* workspace, size_t workspace_bytes,
-                         cudaStream_t st) {
+                         cudaStream_t st, const LocalWindow& local) {
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const size_t score_bytes = round256((size_t)T * (size_t)S * sizeof(float));
   const size_t topk_bytes = S > 0 ? round256(topk_workspace_bytes(T, S, k_top)) : 0;
@@ -99,10 +119,10 @@ int run_index_and_attend(const void* q, const void* w, const void* k, const int3
     rc = launch_topk(ta, st);
   }
   if (rc == DS4X_OK) {
-    const size_t used = score_bytes + topk_bytes;
-    const bool room = S > 0 && workspace_bytes > used;
+    const size_t used = S > 0 ? score_bytes + topk_bytes : 0;
+    const bool room = ws != nullptr && workspace_bytes > used;
     AttnArgs aa{q_attn, kv, bf16, indices, T, 64, 512, S, k_top, scale, out, lse,
-                room ? ws + used : nullptr, room ? workspace_bytes - used : 0};
+                room ? ws + used : nullptr, room ? workspace_bytes - used : 0, positions, local};
     rc = launch_sparse_attn(aa, st);
   }
   return rc;
@@ -131,7 +151,7 @@ namespace {
 // two slots of one sub-chunk's per-token inputs and outputs], every part 256-byte aligned.
 struct HostLayout {
   int n = 0, tc = 0;                                 // sub-chunks, tokens per sub-chunk
-  size_t k = 0, kv = 0, ws = 0, ws_bytes = 0, slot0 = 0, slot = 0, total = 0;
+  size_t k = 0, kv = 0, kvl = 0, ws = 0, ws_bytes = 0, slot0 = 0, slot = 0, total = 0;
   size_t q = 0, w = 0, pos = 0, qa = 0, idx = 0, out = 0, lse = 0;  // offsets within a slot
 };
 
@@ -140,7 +160,9 @@ int default_host_chunks(int T) {  // sub-chunks of about 512 tokens (a few CTA w
   return n < 1 ? 1 : n > 8 ? 8 : n;
 }
 
-HostLayout host_layout(int T, int H, int D, int S, int k_top, int Hq, int Dkv, int n_chunks) {
+HostLayout host_layout(int T, int H, int D, int S, int k_top, int Hq, int Dkv, int n_chunks, int Lrows = 0,
+                       int window = 0) {
+  const bool win = window > 0 && Lrows > 0;
   HostLayout L;
   L.n = n_chunks > 0 ? (n_chunks < T ? n_chunks : T) : default_host_chunks(T);
   L.tc = (T + L.n - 1) / L.n;
@@ -151,8 +173,10 @@ HostLayout host_layout(int T, int H, int D, int S, int k_top, int Hq, int Dkv, i
   o += round256((size_t)S * D * e16);
   L.kv = o;
   o += round256((size_t)S * Dkv * e16);
+  L.kvl = o;
+  o += win ? round256((size_t)Lrows * Dkv * e16) : 0;
   L.ws = o;
-  L.ws_bytes = fused_workspace_bytes(L.tc, S, k_top);
+  L.ws_bytes = fused_workspace_bytes(L.tc, S, k_top, win ? window : 0);
   o += round256(L.ws_bytes);
   size_t s = 0;
   L.q = s;
@@ -292,17 +316,74 @@ int ds4x_index_and_attend(const void* q, const void* w, const void* k, const int
                                          static_cast<cudaStream_t>(stream)));
 }
 
+size_t ds4x_workspace_bytes_local(int32_t T, int32_t S, int32_t k_top, int32_t window) {
+  if (window < 0 || window > DS4X_MAX_WINDOW) return 0;
+  return fused_workspace_bytes(T, S, k_top, window);
+}
+
+int ds4x_local_pooled_attn(const void* q_attn, const void* kv, const void* kv_local, ds4x_dtype dtype,
+                           const int32_t* indices, const int32_t* positions, int32_t T, int32_t Hq, int32_t Dkv,
+                           int32_t S, int32_t k_top, int32_t local_pos0, int32_t L, int32_t window, float scale,
+                           void* out, float* lse, void* stream) {
+  CallScope scope;
+  if (T < 0 || S < 0 || Hq <= 0 || Dkv <= 0 || k_top < 1) return DS4X_ERR_INVALID;
+  if (dtype != DS4X_F16 && dtype != DS4X_BF16) return DS4X_ERR_INVALID;
+  const int wrc = check_window(kv_local, local_pos0, L, window, true);
+  if (wrc != DS4X_OK) return wrc;
+  if (k_top > DS4X_MAX_KTOP) return DS4X_ERR_UNSUPPORTED;
+  if (T == 0) return scope.done(DS4X_OK);
+  if (!q_attn || !indices || !out || !positions || (S > 0 && !kv)) return DS4X_ERR_INVALID;
+  if (!aligned16(q_attn) || (kv && !aligned16(kv)) || !aligned16(indices) || !aligned16(positions) ||
+      !aligned16(out) || (lse && !aligned16(lse)))
+    return DS4X_ERR_INVALID;
+  if (!attn_shape_supported(Hq, Dkv)) return DS4X_ERR_UNSUPPORTED;
+  AttnArgs a{q_attn, kv, dtype == DS4X_BF16 ? 1 : 0, indices, T, Hq, Dkv, S, k_top, scale, out, lse, nullptr, 0,
+             positions, window_of(kv_local, local_pos0, L, window)};
+  return scope.done(launch_sparse_attn(a, static_cast<cudaStream_t>(stream)));
+}
+
+int ds4x_index_and_attend_local(const void* q, const void* w, const void* k, const int32_t* positions,
+                                const void* q_attn, const void* kv, const void* kv_local, ds4x_dtype kv_dtype,
+                                int32_t T, int32_t H, int32_t D, int32_t S, int32_t ratio, int32_t k_top,
+                                int32_t Hq, int32_t Dkv, int32_t local_pos0, int32_t L, int32_t window, float scale,
+                                int32_t* indices, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  CallScope scope;
+  if (T < 0 || S < 0 || H <= 0 || D <= 0 || Hq <= 0 || Dkv <= 0 || ratio < 1 || k_top < 1)
+    return DS4X_ERR_INVALID;
+  if (kv_dtype != DS4X_F16 && kv_dtype != DS4X_BF16) return DS4X_ERR_INVALID;
+  const int wrc = check_window(kv_local, local_pos0, L, window, true);
+  if (wrc != DS4X_OK) return wrc;
+  if (k_top > DS4X_MAX_KTOP) return DS4X_ERR_UNSUPPORTED;
+  if (T == 0) return scope.done(DS4X_OK);
+  if (!q || !w || !positions || !q_attn || !indices || !out || (S > 0 && (!k || !kv))) return DS4X_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(w) || (k && !aligned16(k)) || !aligned16(positions) || !aligned16(q_attn) ||
+      (kv && !aligned16(kv)) || !aligned16(indices) || !aligned16(out) || (lse && !aligned16(lse)) ||
+      (workspace && !aligned16(workspace)))
+    return DS4X_ERR_INVALID;
+  if (!score_shape_supported(H, D) || !attn_shape_supported(Hq, Dkv)) return DS4X_ERR_UNSUPPORTED;
+  if (S > 0 && (workspace == nullptr || workspace_bytes < fused_workspace_bytes(T, S, k_top, window)))
+    return DS4X_ERR_WORKSPACE;
+  return scope.done(run_index_and_attend(q, w, k, positions, q_attn, kv, kv_dtype == DS4X_BF16 ? 1 : 0, T, H, D, S,
+                                         ratio, k_top, scale, indices, out, lse, workspace, workspace_bytes,
+                                         static_cast<cudaStream_t>(stream),
+                                         window_of(kv_local, local_pos0, L, window)));
+}
+
 size_t ds4x_index_and_attend_host_bytes(int32_t T, int32_t H, int32_t D, int32_t S, int32_t k_top, int32_t Hq,
                                         int32_t Dkv, int32_t n_chunks) {
   if (T <= 0 || S < 0 || H <= 0 || D <= 0 || k_top <= 0 || Hq <= 0 || Dkv <= 0 || n_chunks < 0) return 0;
   return host_layout(T, H, D, S, k_top, Hq, Dkv, n_chunks).total;
 }
 
-int ds4x_index_and_attend_host(const void* q, const void* w, const void* k, const int32_t* positions,
-                               const void* q_attn, const void* kv, ds4x_dtype kv_dtype, int32_t T, int32_t H,
-                               int32_t D, int32_t S, int32_t ratio, int32_t k_top, int32_t Hq, int32_t Dkv,
-                               float scale, int32_t* indices, void* out, float* lse, int32_t n_chunks,
-                               void* device_buffer, size_t device_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+// The host-buffer fused path with an optional raw window (kv_local is host memory, copied once).
+int host_path(const void* q, const void* w, const void* k, const int32_t* positions, const void* q_attn,
+              const void* kv, ds4x_dtype kv_dtype, int32_t T, int32_t H, int32_t D, int32_t S, int32_t ratio,
+              int32_t k_top, int32_t Hq, int32_t Dkv, float scale, int32_t* indices, void* out, float* lse,
+              int32_t n_chunks, void* device_buffer, size_t device_bytes, void* stream, const LocalWindow& lw) {
   CallScope scope;
   if (T < 0 || S < 0 || H <= 0 || D <= 0 || Hq <= 0 || Dkv <= 0 || ratio < 1 || k_top < 1 || n_chunks < 0)
     return DS4X_ERR_INVALID;
@@ -313,8 +394,9 @@ int ds4x_index_and_attend_host(const void* q, const void* w, const void* k, cons
     return DS4X_ERR_INVALID;
   if (!aligned16(device_buffer)) return DS4X_ERR_INVALID;
   if (!score_shape_supported(H, D) || !attn_shape_supported(Hq, Dkv)) return DS4X_ERR_UNSUPPORTED;
-  const HostLayout L = host_layout(T, H, D, S, k_top, Hq, Dkv, n_chunks);
+  const HostLayout L = host_layout(T, H, D, S, k_top, Hq, Dkv, n_chunks, lw.L, lw.window);
   if (device_bytes < L.total) return DS4X_ERR_WORKSPACE;
+  LocalWindow dlw = lw;  // the window rows' device copy
 
   HostPipe& hp = g_host_pipe[current_device()];
   std::lock_guard<std::mutex> lock(hp.m);
@@ -332,6 +414,10 @@ int ds4x_index_and_attend_host(const void* q, const void* w, const void* k, cons
   if (S > 0) {
     DS4X_CK(cudaMemcpyAsync(base + L.k, k, (size_t)S * D * 2, h2d, hp.in));
     DS4X_CK(cudaMemcpyAsync(base + L.kv, kv, (size_t)S * Dkv * 2, h2d, hp.in));
+  }
+  if (lw.active()) {
+    DS4X_CK(cudaMemcpyAsync(base + L.kvl, lw.kv_local, (size_t)lw.L * Dkv * 2, h2d, hp.in));
+    dlw.kv_local = base + L.kvl;
   }
   const size_t qt = (size_t)H * D * 2, wt = (size_t)H * 2, at = (size_t)Hq * Dkv * 2;
   const size_t it = (size_t)k_top * sizeof(int32_t), lt = (size_t)Hq * sizeof(float);
@@ -355,7 +441,7 @@ int ds4x_index_and_attend_host(const void* q, const void* w, const void* k, cons
                                         S > 0 ? base + L.kv : nullptr, kv_dtype == DS4X_BF16 ? 1 : 0, tn, H, D, S,
                                         ratio, k_top, scale, reinterpret_cast<int32_t*>(sl + L.idx), sl + L.out,
                                         lse ? reinterpret_cast<float*>(sl + L.lse) : nullptr, base + L.ws,
-                                        L.ws_bytes, st);
+                                        L.ws_bytes, st, dlw);
     if (rc != DS4X_OK) return rc;
     DS4X_CK(cudaEventRecord(hp.work_done[b], st));
     // outputs of sub-chunk j
@@ -370,6 +456,39 @@ int ds4x_index_and_attend_host(const void* q, const void* w, const void* k, cons
   if (L.n > 1) DS4X_CK(cudaStreamWaitEvent(st, hp.out_done[L.n & 1], 0));
 #undef DS4X_CK
   return scope.done(DS4X_OK);
+}
+}  // namespace
+
+extern "C" {
+
+int ds4x_index_and_attend_host(const void* q, const void* w, const void* k, const int32_t* positions,
+                               const void* q_attn, const void* kv, ds4x_dtype kv_dtype, int32_t T, int32_t H,
+                               int32_t D, int32_t S, int32_t ratio, int32_t k_top, int32_t Hq, int32_t Dkv,
+                               float scale, int32_t* indices, void* out, float* lse, int32_t n_chunks,
+                               void* device_buffer, size_t device_bytes, void* stream) {
+  return host_path(q, w, k, positions, q_attn, kv, kv_dtype, T, H, D, S, ratio, k_top, Hq, Dkv, scale, indices, out,
+                   lse, n_chunks, device_buffer, device_bytes, stream, LocalWindow());
+}
+
+size_t ds4x_index_and_attend_local_host_bytes(int32_t T, int32_t H, int32_t D, int32_t S, int32_t k_top,
+                                              int32_t Hq, int32_t Dkv, int32_t L, int32_t window,
+                                              int32_t n_chunks) {
+  if (T <= 0 || S < 0 || H <= 0 || D <= 0 || k_top <= 0 || Hq <= 0 || Dkv <= 0 || n_chunks < 0 || L < 0 ||
+      window < 0 || window > DS4X_MAX_WINDOW)
+    return 0;
+  return host_layout(T, H, D, S, k_top, Hq, Dkv, n_chunks, L, window).total;
+}
+
+int ds4x_index_and_attend_local_host(const void* q, const void* w, const void* k, const int32_t* positions,
+                                     const void* q_attn, const void* kv, const void* kv_local, ds4x_dtype kv_dtype,
+                                     int32_t T, int32_t H, int32_t D, int32_t S, int32_t ratio, int32_t k_top,
+                                     int32_t Hq, int32_t Dkv, int32_t local_pos0, int32_t L, int32_t window,
+                                     float scale, int32_t* indices, void* out, float* lse, int32_t n_chunks,
+                                     void* device_buffer, size_t device_bytes, void* stream) {
+  const int rc = check_window(kv_local, local_pos0, L, window, false);
+  if (rc != DS4X_OK) return rc;
+  return host_path(q, w, k, positions, q_attn, kv, kv_dtype, T, H, D, S, ratio, k_top, Hq, Dkv, scale, indices, out,
+                   lse, n_chunks, device_buffer, device_bytes, stream, window_of(kv_local, local_pos0, L, window));
 }
 
 int ds4x_device_status(void* stream, int clear) {

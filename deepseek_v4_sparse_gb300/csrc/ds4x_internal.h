@@ -67,6 +67,14 @@ struct TopkArgs {
 size_t topk_workspace_bytes(int T, int S, int k_top);
 int launch_topk(const TopkArgs& a, cudaStream_t stream);
 
+// The raw sliding window joined to the pooled rows (window = 0 or L = 0: none): a token at p also
+// attends to kv_local row r for every position a = local_pos0 + r with p - window < a <= p.
+struct LocalWindow {
+  const void* kv_local = nullptr;  // [L, Dkv], kv dtype
+  int local_pos0 = 0, L = 0, window = 0;
+  bool active() const { return window > 0 && L > 0; }
+};
+
 struct AttnArgs {
   const void* q_attn;  // [T, Hq, Dkv]
   const void* kv;      // [S, Dkv]
@@ -77,19 +85,21 @@ struct AttnArgs {
   void* out;
   float* lse;
   void* partial;         // scratch for the split mode (NULL: every token on one CTA)
-  size_t partial_bytes;  // used only when >= attn_partial_bytes(T, k_top)
+  size_t partial_bytes;  // used only when >= attn_partial_bytes(T, k_top, window)
+  const int32_t* positions = nullptr;  // [T], read only with an active window
+  LocalWindow local = {};
 };
 int launch_sparse_attn(const AttnArgs& a, cudaStream_t stream);
 bool attn_shape_supported(int Hq, int Dkv);
 // Scratch the split mode wants for T tokens on the current device (0: no split at this T).
-size_t attn_partial_bytes(int T, int k_top);
+size_t attn_partial_bytes(int T, int k_top, int window);
 
 // The fused path (score -> top-k -> attention, Hq = 64, Dkv = 512) on validated arguments, and
 // the workspace it needs: [scores T x S fp32 | top-k scratch | split-attention scratch].
-size_t fused_workspace_bytes(int T, int S, int k_top);
+size_t fused_workspace_bytes(int T, int S, int k_top, int window = 0);
 int run_index_and_attend(const void* q, const void* w, const void* k, const int32_t* positions, const void* q_attn,
                          const void* kv, int bf16, int T, int H, int D, int S, int ratio, int k_top, float scale,
                          int32_t* indices, void* out, float* lse, void* workspace, size_t workspace_bytes,
-                         cudaStream_t st);
+                         cudaStream_t st, const LocalWindow& local = LocalWindow());
 
 }  // namespace ds4x

@@ -7,6 +7,13 @@
 // by an index list, kv rows serving as both key and value), fed by the top-512 of "How I made
 // DeepSeek 12x faster on a Mac Studio", section "1: the kernels".
 //
+// Local-plus-pooled (same page and item: the native kernel that takes local and pooled state in
+// one pass): with a window W the row list of token t grows by the raw rows of positions
+// p-W+1 .. p held in kv_local, as extra 64-row chunks after the pooled ones, in the same softmax.
+// A pooled chunk gathers through the indices; a window chunk through the token's position.  The
+// window code is a template branch (kWin): the pooled-only kernel carries none of it (its chunk
+// tests measurably slowed that kernel when they were runtime branches).
+//
 // One CTA per SM, persistent over tokens.  A token's selected rows are processed in chunks of
 // 64, double-buffered in shared memory (each row is gathered with 16-byte cp.async into the
 // 128B-swizzled layout both products read: 8 slots of 64 dims per chunk).  Per chunk:
@@ -28,6 +35,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <limits.h>
 #include <math.h>
 
 #include "ds4x_internal.h"
@@ -74,12 +82,16 @@ struct Params {
   const uint16_t* kv;        // [S, 512]; never read through an invalid index
   const uint16_t* zero_src;  // any valid address: source of the zero-filled (size 0) copies
   const int32_t* indices;
+  const uint16_t* kv_local;  // [L, 512] raw rows of the window, row r = position local_pos0 + r
+  const int32_t* positions;  // [T], read for the window chunks only
   uint16_t* out;
   float* lse;
   int* status;
   float* part_o;   // split mode: per item, sum_j 2^(x_j - m) kv_j  [items, 64, 512] fp32 (unnormalized)
   float* part_ml;  // split mode: per item, m [64] then l [64] (m in log2 units of the scaled logits)
   int T, S, k_top, nchunks;
+  int npc;                      // chunks [0, npc) hold pooled rows, [npc, nchunks) the window's
+  int L, local_pos0, window;
   int nsplit, cps, items;  // a token's chunks are spread over nsplit items of cps chunks each
   float scale_log2;
 };
@@ -185,7 +197,7 @@ __device__ __forceinline__ uint16_t to16(float x) {
   }
 }
 
-template <bool kBf16>
+template <bool kBf16, bool kWin>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_mqa_kernel(const __grid_constant__ CUtensorMap tm_q, const Params p) {
   constexpr uint32_t kIdescS = idesc_f16(64, kHq, kBf16 ? 1 : 0, 0, 0);
@@ -281,11 +293,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r = (pt >> 3) + 16 * i;
       dst_off[i] = r * 128 + ((ch ^ (r & 7)) << 4);
     }
+    // a chunk's row sources, loaded a chunk ahead: a pooled chunk's indices, a window chunk's
+    // token position (in idx[0])
     auto load_idx = [&](int t, int c, int32_t (&idx)[4]) {
+      if (!kWin || c < p.npc) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int j = c * kRows + (pt >> 3) + 16 * i;
-        idx[i] = (t < p.T && j < p.k_top) ? __ldg(p.indices + (int64_t)t * p.k_top + j) : -1;
+        for (int i = 0; i < 4; ++i) {
+          const int j = c * kRows + (pt >> 3) + 16 * i;
+          idx[i] = (t < p.T && j < p.k_top) ? __ldg(p.indices + (int64_t)t * p.k_top + j) : -1;
+        }
+      } else {
+        idx[0] = t < p.T ? __ldg(p.positions + t) : INT_MIN;
       }
     };
     uint32_t gc = 0;
@@ -301,11 +319,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       item_of(it, t, c0, c1);
       for (int c = c0; c < c1 && ok; ++c, ++gc) {
         const char* src[4];
+        if (!kWin || c < p.npc) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          src[i] = (idx[i] >= 0 && idx[i] < p.S)
-                       ? reinterpret_cast<const char*>(p.kv + (int64_t)idx[i] * kDkv) + ch * 16
-                       : nullptr;
+          for (int i = 0; i < 4; ++i)
+            src[i] = (idx[i] >= 0 && idx[i] < p.S)
+                         ? reinterpret_cast<const char*>(p.kv + (int64_t)idx[i] * kDkv) + ch * 16
+                         : nullptr;
+        } else {
+          // window row jl of the token sits at position p - W + 1 + jl, buffer row that - local_pos0
+          const int lc = (c - p.npc) * kRows;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int jl = lc + (pt >> 3) + 16 * i;
+            const int64_t a = (int64_t)idx[0] - p.window + 1 + jl, r = a - p.local_pos0;
+            src[i] = (jl < p.window && a >= 0 && r >= 0 && r < p.L)
+                         ? reinterpret_cast<const char*>(p.kv_local + r * kDkv) + ch * 16
+                         : nullptr;
+          }
+        }
         // the next chunk's indices are on their way while this chunk is issued
         {
           int nt, nc;
@@ -412,10 +443,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t gc = 0, tok_i = 0;
     bool ok = true;
     // validity of the 64 rows of a chunk: two ballots over per-lane index loads, one chunk ahead
+    // (a window chunk loads the token's position into i0 instead)
     auto load_valid = [&](int t, int ci, int32_t& i0, int32_t& i1) {
-      const int j0 = ci * kRows + lane, j1 = j0 + 32;
-      i0 = (t < p.T && ci < nch && j0 < p.k_top) ? __ldg(p.indices + (int64_t)t * p.k_top + j0) : -1;
-      i1 = (t < p.T && ci < nch && j1 < p.k_top) ? __ldg(p.indices + (int64_t)t * p.k_top + j1) : -1;
+      if (!kWin || ci < p.npc) {
+        const int j0 = ci * kRows + lane, j1 = j0 + 32;
+        i0 = (t < p.T && ci < nch && j0 < p.k_top) ? __ldg(p.indices + (int64_t)t * p.k_top + j0) : -1;
+        i1 = (t < p.T && ci < nch && j1 < p.k_top) ? __ldg(p.indices + (int64_t)t * p.k_top + j1) : -1;
+      } else {
+        i0 = t < p.T ? __ldg(p.positions + t) : INT_MIN;
+        i1 = 0;
+      }
+    };
+    auto window_row_valid = [&](int32_t pos, int ci, int j) {
+      const int jl = (ci - p.npc) * kRows + j;
+      const int64_t a = (int64_t)pos - p.window + 1 + jl, r = a - p.local_pos0;
+      return jl < p.window && a >= 0 && r >= 0 && r < p.L;
     };
     int32_t ni0, ni1;
     {
@@ -428,8 +470,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       item_of(it, t, c0, c1);
       float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;  // running max (scaled, log2) and sum
       for (int ci = c0; ci < c1; ++ci, ++gc) {
-        const uint32_t v0 = __ballot_sync(0xffffffffu, ni0 >= 0 && ni0 < p.S) >> (2 * e);
-        const uint32_t v1 = __ballot_sync(0xffffffffu, ni1 >= 0 && ni1 < p.S) >> (2 * e);
+        const bool pooled = !kWin || ci < p.npc;
+        const bool ok0 = pooled ? (ni0 >= 0 && ni0 < p.S) : window_row_valid(ni0, ci, lane);
+        const bool ok1 = pooled ? (ni1 >= 0 && ni1 < p.S) : window_row_valid(ni0, ci, lane + 32);
+        const uint32_t v0 = __ballot_sync(0xffffffffu, ok0) >> (2 * e);
+        const uint32_t v1 = __ballot_sync(0xffffffffu, ok1) >> (2 * e);
         {
           int nt, nc;
           next_chunk(it, t, ci, c1, nt, nc);
@@ -709,15 +754,18 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
     lse[(int64_t)t * kHq + h] = L > 0.f ? (mx + log2f(L)) * 0.69314718055994531f : -INFINITY;
 }
 
-// Split plan: when the tokens fill less than half of the SMs, a token's chunks are spread over
-// up to sms / T items (at least one chunk each) and merged by combine_kernel.
-void split_plan(int T, int k_top, int sms, int& nsplit, int& cps) {
-  const int nch = (k_top + kRows - 1) / kRows;
+// Chunks of one token: the pooled rows', then the window's.
+int chunks_of(int k_top, int window) { return (k_top + kRows - 1) / kRows + (window + kRows - 1) / kRows; }
+
+// Split plan: when the tokens fill less than half of the SMs, a token's nch chunks are spread over
+// up to sms / T items (at least one chunk each, at most kMaxSplit) and merged by combine_kernel.
+void split_plan(int T, int nch, int sms, int& nsplit, int& cps) {
   nsplit = 1;
   cps = nch;
   if (T <= 0 || 2 * T > sms || nch < 2) return;
   int want = sms / T;
   if (want > nch) want = nch;
+  if (want > kMaxSplit) want = kMaxSplit;
   cps = (nch + want - 1) / want;
   nsplit = (nch + cps - 1) / cps;
 }
@@ -750,8 +798,10 @@ template <bool kBf16>
 int launch_impl(const AttnArgs& a, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(sparse_mqa_kernel<kBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(sparse_mqa_kernel<kBf16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(sparse_mqa_kernel<kBf16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
+            cudaSuccess)
       return DS4X_ERR_CUDA;
     attr_set = true;
   }
@@ -772,13 +822,20 @@ int launch_impl(const AttnArgs& a, cudaStream_t stream) {
   p.kv = static_cast<const uint16_t*>(a.kv);
   p.zero_src = static_cast<const uint16_t*>(a.q_attn);
   p.indices = a.indices;
+  const bool win = a.local.active();
+  p.kv_local = win ? static_cast<const uint16_t*>(a.local.kv_local) : nullptr;
+  p.positions = win ? a.positions : nullptr;
+  p.L = win ? a.local.L : 0;
+  p.local_pos0 = win ? a.local.local_pos0 : 0;
+  p.window = win ? a.local.window : 0;
   p.out = static_cast<uint16_t*>(a.out);
   p.lse = a.lse;
   p.status = device_status_ptr();
   p.T = a.T;
   p.S = a.S;
   p.k_top = a.k_top;
-  p.nchunks = (a.k_top + kRows - 1) / kRows;
+  p.npc = (a.k_top + kRows - 1) / kRows;
+  p.nchunks = chunks_of(a.k_top, p.window);
   p.scale_log2 = a.scale * 1.4426950408889634f;
   const int sms = device_sm_count();
   p.nsplit = 1;
@@ -787,7 +844,7 @@ int launch_impl(const AttnArgs& a, cudaStream_t stream) {
   p.part_ml = nullptr;
   if (a.partial) {
     int ns, cps;
-    split_plan(a.T, a.k_top, sms, ns, cps);
+    split_plan(a.T, p.nchunks, sms, ns, cps);
     const size_t need = partial_bytes_for(a.T, ns);
     if (ns > 1 && a.partial_bytes >= need) {
       p.nsplit = ns;
@@ -798,7 +855,8 @@ int launch_impl(const AttnArgs& a, cudaStream_t stream) {
   }
   p.items = a.T * p.nsplit;
   const int grid = p.items < sms ? p.items : sms;
-  if (launch_pdl(sparse_mqa_kernel<kBf16>, dim3(grid), dim3(kThreads), (size_t)kSmem, stream, tq, p) != cudaSuccess)
+  if (launch_pdl(win ? sparse_mqa_kernel<kBf16, true> : sparse_mqa_kernel<kBf16, false>, dim3(grid), dim3(kThreads),
+                 (size_t)kSmem, stream, tq, p) != cudaSuccess)
     return DS4X_ERR_CUDA;
   count_launch();
   if (p.nsplit > 1) {
@@ -814,9 +872,9 @@ int launch_impl(const AttnArgs& a, cudaStream_t stream) {
 
 bool attn_shape_supported(int Hq, int Dkv) { return Hq == kHq && Dkv == kDkv; }
 
-size_t attn_partial_bytes(int T, int k_top) {
+size_t attn_partial_bytes(int T, int k_top, int window) {
   int ns, cps;
-  split_plan(T, k_top, device_sm_count(), ns, cps);
+  split_plan(T, chunks_of(k_top, window), device_sm_count(), ns, cps);
   return partial_bytes_for(T, ns);
 }
 

@@ -66,6 +66,8 @@ typedef enum {
  *   attention heads Hq = 64, attention dim Dkv = 512
  *   1 <= k_top <= DS4X_MAX_KTOP                                                  */
 #define DS4X_MAX_KTOP 1024
+/*   0 <= window <= DS4X_MAX_WINDOW for the local-plus-pooled entries                 */
+#define DS4X_MAX_WINDOW 1024
 
 /* ---------------------------------------------------------------------------
  * ds4x_indexer_score — the lightning-indexer scorer ([K] #830/#831).
@@ -202,6 +204,61 @@ int ds4x_index_and_attend_host(const void* q, const void* w, const void* k, cons
 
 size_t ds4x_index_and_attend_host_bytes(int32_t T, int32_t H, int32_t D, int32_t S, int32_t k_top,
                                         int32_t Hq, int32_t Dkv, int32_t n_chunks);
+
+/* ---------------------------------------------------------------------------
+ * Local-plus-pooled attention ([A]: ratio-128 compressed attention draws on local and pooled
+ * key/value state, and the native kernel takes both in one pass; the ds4.c overview keeps the
+ * live raw sliding-window KV rows as state of their own).  The pages give no window size and no
+ * joining rule; this library's definition:
+ *
+ *   the rows of token t (position p = positions[t]) are its valid selected pooled rows
+ *   kv[indices[t, j]] (as in ds4x_sparse_attn) followed by the raw window rows kv_local[r] for
+ *   every position a = local_pos0 + r with  max(0, p - window + 1) <= a <= p  and  0 <= r < L;
+ *   out and lse are the softmax attention of ds4x_sparse_attn over all of these rows at once
+ *   (same query, same scale, nothing de-duplicated).
+ *
+ *   kv_local [L, Dkv] of the kv dtype: raw rows of consecutive positions starting at
+ *   local_pos0 >= 0.  For a prefill chunk at positions pos0..pos0+T-1 it holds positions
+ *   pos0-window+1 (or 0) .. pos0+T-1: the previous window-1 raw rows and the chunk's own.
+ *   Window positions outside the buffer are not attended.  window = 0 or L = 0 gives exactly
+ *   the pooled-only result (kv_local may then be NULL).  0 <= window <= DS4X_MAX_WINDOW.
+ *   The window rows are extra 64-row chunks of the same kernel, after the pooled ones.
+ * ------------------------------------------------------------------------- */
+
+/* Attention alone over the two row sources; arguments otherwise as ds4x_sparse_attn, plus
+ * positions [T] int32 (device). */
+int ds4x_local_pooled_attn(const void* q_attn, const void* kv, const void* kv_local, ds4x_dtype dtype,
+                           const int32_t* indices, const int32_t* positions, int32_t T, int32_t Hq,
+                           int32_t Dkv, int32_t S, int32_t k_top, int32_t local_pos0, int32_t L,
+                           int32_t window, float scale, void* out, float* lse, void* stream);
+
+/* The whole path with the window: ds4x_index_and_attend's indices, then ds4x_local_pooled_attn.
+ * workspace: at least ds4x_workspace_bytes_local(T, S, k_top, window) bytes (the split mode of
+ * small T divides the pooled and the window chunks alike); may be NULL when that is 0. */
+int ds4x_index_and_attend_local(const void* q, const void* w, const void* k, const int32_t* positions,
+                                const void* q_attn, const void* kv, const void* kv_local,
+                                ds4x_dtype kv_dtype, int32_t T, int32_t H, int32_t D, int32_t S,
+                                int32_t ratio, int32_t k_top, int32_t Hq, int32_t Dkv,
+                                int32_t local_pos0, int32_t L, int32_t window, float scale,
+                                int32_t* indices, void* out, float* lse, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+size_t ds4x_workspace_bytes_local(int32_t T, int32_t S, int32_t k_top, int32_t window);
+
+/* ds4x_index_and_attend_host with the window: kv_local is HOST memory too, copied once with k
+ * and kv; device_buffer of at least ds4x_index_and_attend_local_host_bytes(...) bytes. */
+int ds4x_index_and_attend_local_host(const void* q, const void* w, const void* k,
+                                     const int32_t* positions, const void* q_attn, const void* kv,
+                                     const void* kv_local, ds4x_dtype kv_dtype, int32_t T, int32_t H,
+                                     int32_t D, int32_t S, int32_t ratio, int32_t k_top, int32_t Hq,
+                                     int32_t Dkv, int32_t local_pos0, int32_t L, int32_t window,
+                                     float scale, int32_t* indices, void* out, float* lse,
+                                     int32_t n_chunks, void* device_buffer, size_t device_bytes,
+                                     void* stream);
+
+size_t ds4x_index_and_attend_local_host_bytes(int32_t T, int32_t H, int32_t D, int32_t S,
+                                              int32_t k_top, int32_t Hq, int32_t Dkv, int32_t L,
+                                              int32_t window, int32_t n_chunks);
 
 /* ---------------------------------------------------------------------------
  * ds4x_decode — the decode loop: n_steps query tokens at consecutive positions

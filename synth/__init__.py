@@ -138,6 +138,7 @@ class Workload:
     k_top: int = 512
     decode_steps: int = 0   # >0: a decode loop of this many single-token steps
     extra_rows: int = 0     # rows appended during the decode loop
+    window: int = 0         # >0: raw sliding-window rows joined to the pooled ones (local-plus-pooled)
     tags: tuple = field(default_factory=tuple)
 
     @property
@@ -162,6 +163,9 @@ WORKLOADS = {
     # ratio-128 layer kind: every pooled row is attended (n_vis <= 512: sequential indices, no scoring)
     "pooled_64k_r128": Workload("pooled_64k_r128", T=2048, H=64, D=128, S=512, ratio=128, pos0=63488,
                                 kind="normal", kv_dtype="bf16"),
+    # local-plus-pooled attention: the 8k chunk with a 128-position raw window per token
+    "prefill_8k_local128": Workload("prefill_8k_local128", T=2048, H=64, D=128, S=2048, ratio=4, pos0=6144,
+                                    kind="normal", kv_dtype="bf16", window=128),
     "decode_1m": Workload("decode_1m", T=1, H=64, D=128, S=262144, ratio=4, pos0=1048575,
                           kind="normal", kv_dtype="bf16", decode_steps=256, extra_rows=64),
 }
@@ -177,6 +181,8 @@ class Inputs:
     positions: np.ndarray  # [T] int32
     q_attn: np.ndarray     # [T, Hq, Dkv] uint16 (kv dtype bits)
     kv: np.ndarray         # [rows, Dkv] uint16 (kv dtype bits)
+    kv_local: np.ndarray | None = None  # [L, Dkv] raw window rows (kv dtype bits), row r = position local_pos0 + r
+    local_pos0: int = 0
 
 
 _PARALLEL_MIN = 1 << 24
@@ -227,7 +233,19 @@ def make_inputs(wl: Workload, seed: int = 0, T: int | None = None, S: int | None
     q_attn = _bits(seed, wl, "q_attn", T * Hq * Dkv, (-2, 2), kvd).reshape(T, Hq, Dkv)
     kv = _bits(seed, wl, "kv", rows * Dkv, (-2, 2), kvd).reshape(rows, Dkv)
     positions = (pos0 + np.arange(T, dtype=np.int64)).astype(np.int32)
-    return Inputs(wl, q, w, k, positions, q_attn, kv)
+    kv_local, local_pos0 = None, 0
+    if wl.window > 0:
+        # the raw rows a prefill chunk needs: the window - 1 positions before it and its own
+        local_pos0 = max(0, pos0 - wl.window + 1)
+        L = pos0 + T - local_pos0
+        kv_local = _bits(seed, wl, "kv_local", L * Dkv, (-2, 2), kvd).reshape(L, Dkv)
+    return Inputs(wl, q, w, k, positions, q_attn, kv, kv_local, local_pos0)
+
+
+def local_rows(seed: int, tag: str, L: int, Dkv: int, kind: str, kv_dtype: str) -> np.ndarray:
+    """A raw-window row buffer [L, Dkv] for edge-case tests (kv dtype bits)."""
+    wl = Workload(tag, T=0, H=1, D=1, S=0, ratio=1, pos0=0, kind=kind, kv_dtype=kv_dtype, Dkv=Dkv)
+    return _bits(seed, wl, "kv_local", L * Dkv, (-2, 2), kv_dtype).reshape(L, Dkv)
 
 
 def custom_inputs(seed: int, tag: str, T: int, H: int, D: int, rows: int, Hq: int, Dkv: int,

@@ -94,6 +94,28 @@ def few_rows_bound(kv_bits: np.ndarray, indices: np.ndarray, ref_bits: np.ndarra
     return bound
 
 
+def window_positions(p: int, window: int, local_pos0: int, L: int):
+    """Raw positions a token at p attends in local-plus-pooled attention."""
+    return [a for a in range(max(0, p - window + 1, local_pos0), min(p, local_pos0 + L - 1) + 1)]
+
+
+def union_rows_bound(kv_bits, indices, S, kv_local_bits, positions, local_pos0, window, ref_bits, dtype):
+    """few_rows_bound over the union of a token's pooled rows and its raw window rows."""
+    u = 2.0 ** -9 if dtype == "bf16" else 2.0 ** -11
+    kv = synth.bits_to_f32(kv_bits, dtype).astype(np.float64)
+    kvl = synth.bits_to_f32(kv_local_bits, dtype).astype(np.float64)
+    ref = synth.bits_to_f32(ref_bits, dtype).astype(np.float64)
+    L = kvl.shape[0]
+    bound = np.zeros_like(ref)
+    for t in range(ref.shape[0]):
+        rows = [kv[int(i)] for i in indices[t] if 0 <= i < S]
+        rows += [kvl[a - local_pos0] for a in window_positions(int(positions[t]), window, local_pos0, L)]
+        if rows:
+            V = np.stack(rows)
+            bound[t] = 2 * u * np.abs(V[None, :, :] - ref[t][:, None, :]).max(axis=1)
+    return bound
+
+
 def check_attn(gpu_bits: np.ndarray, ref_bits: np.ndarray, dtype: str, gpu_lse=None, ref_lse=None,
                extra=None):
     g = synth.bits_to_f32(gpu_bits, dtype).astype(np.float64)

@@ -159,3 +159,54 @@ def test_host_path_staging_sizes(lib):
         ds4x.index_and_attend_host_bytes(T, H, D, S, k_top, Hq, Dkv, 4)      # default: sub-chunks of ~512 tokens
     assert ds4x.index_and_attend_host_bytes(0, H, D, S, k_top, Hq, Dkv, 0) == 0
     assert ds4x.index_and_attend_host_bytes(T, H, D, S, k_top, Hq, Dkv, -1) == 0
+
+
+def _local_attn(lib, T=4, S=10, L=100, lp0=0, window=128, kv_local=0x10000, dtype=1, positions=0x10000, k_top=512):
+    A = 0x10000
+    return lib.ds4x_local_pooled_attn(_p(A), _p(A), _p(kv_local) if kv_local else None, dtype, _p(A),
+                                      _p(positions) if positions else None, T, 64, 512, S, k_top, lp0, L, window, 0.1,
+                                      _p(A), None, None)
+
+
+def _local_fused(lib, T=4, S=10, L=100, lp0=0, window=128, ws=0, nbytes=0):
+    A = 0x10000
+    return lib.ds4x_index_and_attend_local(_p(A), _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), 1, T, 64, 128, S, 4, 512,
+                                           64, 512, lp0, L, window, 0.1, _p(A), _p(A), None,
+                                           _p(ws) if ws else None, nbytes, None)
+
+
+def test_local_arguments_rejected_without_launch(lib):
+    assert _local_attn(lib, lp0=-1) == ds4x.ERR_INVALID                 # buffer before position 0
+    assert _local_attn(lib, L=-1) == ds4x.ERR_INVALID
+    assert _local_attn(lib, window=-1) == ds4x.ERR_INVALID
+    assert _local_attn(lib, window=ds4x.MAX_WINDOW + 1) == ds4x.ERR_UNSUPPORTED
+    assert _local_attn(lib, kv_local=0) == ds4x.ERR_INVALID             # rows in reach but no buffer
+    assert _local_attn(lib, kv_local=0x10008) == ds4x.ERR_INVALID       # misaligned buffer
+    assert _local_attn(lib, positions=0) == ds4x.ERR_INVALID            # positions are required
+    assert _local_attn(lib, dtype=3) == ds4x.ERR_INVALID
+    assert _local_attn(lib, k_top=2048) == ds4x.ERR_UNSUPPORTED
+    assert _local_attn(lib, T=0) == ds4x.OK                             # nothing to do
+    assert _local_fused(lib, lp0=-5) == ds4x.ERR_INVALID
+    assert _local_fused(lib) == ds4x.ERR_WORKSPACE                      # S > 0 needs the score workspace
+    assert _local_fused(lib, ws=0x10000, nbytes=16) == ds4x.ERR_WORKSPACE
+    A = 0x10000
+    assert lib.ds4x_index_and_attend_local_host(
+        _p(A), _p(A), _p(A), _p(A), _p(A), _p(A), None, 1, 4, 64, 128, 10, 4, 512, 64, 512, 0, 100, 128, 0.1,
+        _p(A), _p(A), None, 0, _p(A), 1 << 40, None) == ds4x.ERR_INVALID    # window rows but no host buffer
+
+
+def test_local_workspace_and_staging_sizes(lib):
+    T, H, D, S, k_top, Hq, Dkv = 2048, 64, 128, 2048, 512, 64, 512
+    # a full chunk never splits: the window adds nothing to the workspace
+    assert ds4x.workspace_bytes_local(T, S, k_top, 128) == ds4x.workspace_bytes(T, S, k_top)
+    assert ds4x.workspace_bytes_local(T, S, k_top, 0) == ds4x.workspace_bytes(T, S, k_top)
+    # one token splits its chunks; the window's chunks take part, so the split scratch can grow
+    assert ds4x.workspace_bytes_local(1, S, k_top, 128) >= ds4x.workspace_bytes(1, S, k_top)
+    assert ds4x.workspace_bytes_local(1, S, k_top, ds4x.MAX_WINDOW + 1) == 0
+    L = T + 127
+    for n in (1, 4):
+        plain = ds4x.index_and_attend_host_bytes(T, H, D, S, k_top, Hq, Dkv, n)
+        local = ds4x.index_and_attend_local_host_bytes(T, H, D, S, k_top, Hq, Dkv, L, 128, n)
+        # the window's rows are staged once, beside k and kv
+        assert L * Dkv * 2 <= local - plain <= L * Dkv * 2 + 256
+        assert ds4x.index_and_attend_local_host_bytes(T, H, D, S, k_top, Hq, Dkv, L, 0, n) == plain
