@@ -48,6 +48,7 @@ def _bind(lib):
                                                i32, i32, f32, P, P]
     lib.ds4x_ref_index_and_attend_local.argtypes = [P, P, P, P, P, P, P, ctypes.c_int, i32, i32, i32, i32,
                                                     i32, i32, i32, i32, i32, i32, i32, f32, P, P, P]
+    lib.ds4x_ref_compress.argtypes = [P, P, P, ctypes.c_int, i32, i32, i32, P, P, i32, P, P, P]
     lib.ds4x_ref_decode.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, P, i32, i32, i32, i32, i32, i32,
                                     i32, i32, i32, f32, P, P, P, P, P]
     lib.ds4x_ref_n_visible.argtypes = [i64, i64, i64]
@@ -58,7 +59,7 @@ def _bind(lib):
     lib.ds4x_ref_encode16.restype = ctypes.c_uint16
     for f in ("ds4x_ref_indexer_score", "ds4x_ref_topk_ex", "ds4x_ref_sparse_attn",
               "ds4x_ref_index_and_attend", "ds4x_ref_decode", "ds4x_ref_local_pooled_attn",
-              "ds4x_ref_index_and_attend_local"):
+              "ds4x_ref_index_and_attend_local", "ds4x_ref_compress"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -179,6 +180,24 @@ class Oracle:
         assert rc == 0, rc
         return idx, out, lse
 
+    def compress(self, x, g, bias, dtype, ratio, fx=None, fg=None):
+        """x, g [T, D] raw bits of `dtype`, bias [ratio, D] float32, frontier fx, fg [f, D] (f < ratio,
+        None = empty). Returns (rows [(f+T)//ratio, D], new frontier x, new frontier g)."""
+        x, g = _c(x, np.uint16), _c(g, np.uint16)
+        bias = _c(bias, np.float32)
+        T, D = x.shape
+        f = 0 if fx is None else fx.shape[0]
+        fx = np.zeros((1, D), np.uint16) if fx is None else _c(fx, np.uint16)
+        fg = np.zeros((1, D), np.uint16) if fg is None else _c(fg, np.uint16)
+        n_out, rem = (f + T) // ratio, (f + T) % ratio
+        rows = np.empty((n_out, D), dtype=np.uint16)
+        fx_out = np.empty((rem, D), dtype=np.uint16)
+        fg_out = np.empty((rem, D), dtype=np.uint16)
+        rc = self.lib.ds4x_ref_compress(_ptr(x), _ptr(g), _ptr(bias), DTYPES[dtype], T, D, ratio, _ptr(fx), _ptr(fg),
+                                        f, _ptr(rows), _ptr(fx_out), _ptr(fg_out))
+        assert rc == 0, rc
+        return rows, fx_out, fg_out
+
     def decode(self, q, w, q_attn, k, kv, kv_dtype, S0, pos0, ratio, k_new, kv_new, k_top, scale):
         """The decode loop on copies of k / kv (capacity = their row count).
         Returns (indices, out bits, lse, positions, S per step, k after, kv after)."""
@@ -249,3 +268,7 @@ def local_pooled_attn(*a, **kw):
 
 def index_and_attend_local(*a, **kw):
     return default().index_and_attend_local(*a, **kw)
+
+
+def compress(*a, **kw):
+    return default().compress(*a, **kw)

@@ -30,6 +30,13 @@
  *    rule for joining the two sources; the reading here: the raw rows of the positions
  *    p - window + 1 .. p (none below 0) join the selected pooled rows in one softmax with
  *    the same query and scale, nothing de-duplicated.
+ *  - The compressor: one pooled row per `ratio` positions ("three merged oMLX PRs", section
+ *    "The three changes that merged", item 3: the skip path still advances the indexer
+ *    compressor and its cache), with the partial block carried between calls as state (the
+ *    ds4.c overview, disk-cache layout: "compressor frontier" tensors).  The pages give no
+ *    formula; the reading here: per channel, a softmax over the block's positions of a gate
+ *    logit plus a learned per-position bias weights the block's raw rows (equal gates give the
+ *    mean).  Gates, bias and raw rows are inputs (no trained weights exist).
  *  - The formula (which the pages leave unstated) is this library's definition:
  *    score[t,s] = sum_h w[t,h] * ReLU(q[t,h,:] . k[s,:]), row s visible iff
  *    (s+1)*ratio <= p+1, ties to the lower row index, indices ascending, attention with
@@ -44,7 +51,9 @@
  * brute-force of every step on tiny inputs; for local-plus-pooled attention a textbook
  * sliding-window attention in numpy, a numpy softmax over the union of both sources, the
  * log-sum-exp merge of the two one-source results, the exact mean for a zero query and a
- * one-row window.
+ * one-row window; for the compressor the exact rational mean under equal gates, a dominant gate
+ * giving its row, a numpy softmax pooling, and one call equal to any split into two calls with
+ * the frontier carried.
  */
 #include <math.h>
 #include <stdint.h>
@@ -418,6 +427,57 @@ int ds4x_ref_index_and_attend_local(const uint16_t* q, const uint16_t* w, const 
   ref_index_select(q, w, k, positions, T, H, D, S, ratio, k_top, indices);
   return ds4x_ref_local_pooled_attn(q_attn, kv, kv_local, kv_dtype, indices, positions, T, Hq,
                                     Dkv, S, k_top, local_pos0, L, window, scale, out, lse);
+}
+
+/* ---- the compressor ------------------------------------------------------------------ */
+
+/* Row v of the sequence made of the n_frontier held-over positions followed by the T new ones. */
+static const uint16_t* ref_seq_row(const uint16_t* held, const uint16_t* fresh, int32_t n_frontier,
+                                   int64_t v, int32_t D) {
+  return v < n_frontier ? held + v * D : fresh + (v - n_frontier) * D;
+}
+
+/* One compressed row per `ratio` consecutive positions.  The sequence is the n_frontier
+ * positions held over from the previous call (fx_in, fg_in) followed by the T new positions
+ * (x, g).  Block j covers sequence positions j*ratio .. j*ratio + ratio - 1 and gives, per
+ * channel d, with i the position inside the block:
+ *   rows[j,d] = sum_i a_i x_i[d],   a_i = exp(z_i) / sum_i' exp(z_i'),   z_i = g_i[d] + bias[i,d]
+ * (max-subtracted, in double, rounded once to dtype).  The (n_frontier + T) mod ratio positions
+ * after the last full block are copied to fx_out / fg_out: the new frontier. */
+int ds4x_ref_compress(const uint16_t* x, const uint16_t* g, const float* bias, int dtype,
+                      int32_t T, int32_t D, int32_t ratio, const uint16_t* fx_in,
+                      const uint16_t* fg_in, int32_t n_frontier, uint16_t* rows,
+                      uint16_t* fx_out, uint16_t* fg_out) {
+  if (T < 0 || D < 1 || ratio < 1 || n_frontier < 0 || n_frontier >= ratio) return -1;
+  const int64_t n = (int64_t)n_frontier + T;
+  const int64_t n_out = n / ratio;
+  double* z = (double*)malloc(sizeof(double) * (size_t)ratio);
+  for (int64_t j = 0; j < n_out; ++j) {
+    for (int32_t d = 0; d < D; ++d) {
+      double m = -INFINITY;
+      for (int32_t i = 0; i < ratio; ++i) {
+        const int64_t v = j * ratio + i;
+        z[i] = ref_to_double(ref_seq_row(fg_in, g, n_frontier, v, D)[d], dtype) +
+               (double)bias[(int64_t)i * D + d];
+        if (z[i] > m) m = z[i];
+      }
+      double sum = 0.0, acc = 0.0;
+      for (int32_t i = 0; i < ratio; ++i) {
+        const int64_t v = j * ratio + i;
+        const double a = exp(z[i] - m);
+        sum += a;
+        acc += a * ref_to_double(ref_seq_row(fx_in, x, n_frontier, v, D)[d], dtype);
+      }
+      rows[j * D + d] = ref_from_double(acc / sum, dtype);
+    }
+  }
+  for (int64_t v = n_out * ratio; v < n; ++v) {
+    const int64_t i = v - n_out * ratio;
+    memcpy(fx_out + i * D, ref_seq_row(fx_in, x, n_frontier, v, D), sizeof(uint16_t) * (size_t)D);
+    memcpy(fg_out + i * D, ref_seq_row(fg_in, g, n_frontier, v, D), sizeof(uint16_t) * (size_t)D);
+  }
+  free(z);
+  return 0;
 }
 
 /* ---- the decode loop ------------------------------------------------------------------ */

@@ -20,7 +20,10 @@ Independent facts used:
   * for local-plus-pooled attention: a textbook float64 causal sliding-window attention, a
     float64 softmax over the union of both row sources, the log-sum-exp merge identity of two
     one-source results, the exact rational mean for a zero query, a one-row window giving that
-    row, and the pooled result whenever no raw row is in reach.
+    row, and the pooled result whenever no raw row is in reach;
+  * for the compressor: the exact rational mean of each block under equal gates, a dominant gate
+    selecting its position's row, a float64 numpy gated pooling, and the equality of one call with
+    any two calls that carry the frontier.
 """
 from __future__ import annotations
 
@@ -571,6 +574,80 @@ def check_index_and_attend_local_composes(o):
     assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
 
 
+# ----------------------------------------------------------------------------- compressor
+def _softmax_pool_numpy(seq_x, seq_g, bias, ratio, dtype):
+    """Textbook float64 gated pooling of whole blocks of the sequence rows."""
+    xf, gf = _bits_val(seq_x, dtype), _bits_val(seq_g, dtype)
+    n_out = xf.shape[0] // ratio
+    out = np.empty((n_out, xf.shape[1]))
+    for j in range(n_out):
+        z = gf[j * ratio:(j + 1) * ratio] + bias.astype(np.float64)      # [ratio, D]
+        a = np.exp(z - z.max(axis=0))
+        out[j] = (a * xf[j * ratio:(j + 1) * ratio]).sum(axis=0) / a.sum(axis=0)
+    return out
+
+
+def check_compress_equal_gates_is_mean(o):
+    # equal gates: every block row is the exact rational mean of its positions, rounded once;
+    # a 3-position frontier at ratio 4 puts the first block across the call boundary
+    rng = np.random.default_rng(21)
+    ratio, D, T, f = 4, 24, 13, 3
+    xs = synth.to_bf16_bits(rng.standard_normal((f + T, D)))
+    g = np.full((f + T, D), synth.to_bf16_bits(np.array([0.75]))[0], dtype=np.uint16)
+    bias = np.zeros((ratio, D), np.float32)
+    rows, fx, fg = o.compress(xs[f:], g[f:], bias, "bf16", ratio, xs[:f], g[:f])
+    assert rows.shape == (4, D) and fx.shape == (0, D)
+    xv = _bits_val(xs, "bf16")
+    for j in range(4):
+        for d in range(D):
+            mean = sum(Fraction(float(v)) for v in xv[j * ratio:(j + 1) * ratio, d]) / ratio
+            assert Fraction(float(_bits_val(rows[j:j + 1, d], "bf16")[0])) == _rne_fraction(mean, 7, 8), (j, d)
+
+
+def check_compress_dominant_gate_selects_row(o):
+    # one position's gate 100 above the others: its weight is 1 to far below rounding
+    rng = np.random.default_rng(22)
+    ratio, D, T = 8, 16, 40
+    x = synth.to_f16_bits(rng.standard_normal((T, D)))
+    gv = np.zeros((T, D))
+    pick = rng.integers(0, ratio, size=(T // ratio, D))
+    for j in range(T // ratio):
+        gv[j * ratio + pick[j], np.arange(D)] = 100.0
+    rows, _, _ = o.compress(x, synth.to_f16_bits(gv), np.zeros((ratio, D), np.float32), "f16", ratio)
+    for j in range(T // ratio):
+        assert np.array_equal(rows[j], x[j * ratio + pick[j], np.arange(D)]), j
+
+
+def check_compress_vs_numpy(o):
+    rng = np.random.default_rng(23)
+    for dtype, ratio, D, T, f in (("bf16", 4, 32, 29, 2), ("f16", 16, 8, 50, 15), ("bf16", 128, 4, 300, 0)):
+        xs = synth.to_bits(rng.standard_normal((f + T, D)), dtype)
+        gs = synth.to_bits(2 * rng.standard_normal((f + T, D)), dtype)
+        bias = rng.standard_normal((ratio, D)).astype(np.float32)
+        rows, fx, fg = o.compress(xs[f:], gs[f:], bias, dtype, ratio, xs[:f] if f else None, gs[:f] if f else None)
+        ref = _softmax_pool_numpy(xs, gs, bias, ratio, dtype)
+        got = _bits_val(rows, dtype)
+        ulp = 2.0 ** (-8 if dtype == "bf16" else -11)
+        assert np.all(np.abs(got - ref) <= ulp * np.abs(ref) + 1e-7), (dtype, ratio, np.abs(got - ref).max())
+        rem = (f + T) % ratio
+        assert np.array_equal(fx, xs[f + T - rem:]) and np.array_equal(fg, gs[f + T - rem:])
+
+
+def check_compress_split_calls_equal_one(o):
+    # compressing a sequence in one call equals any split into two calls with the frontier carried
+    rng = np.random.default_rng(24)
+    ratio, D, N = 4, 12, 37
+    xs = synth.to_bf16_bits(rng.standard_normal((N, D)))
+    gs = synth.to_bf16_bits(rng.standard_normal((N, D)))
+    bias = rng.standard_normal((ratio, D)).astype(np.float32)
+    whole, wfx, wfg = o.compress(xs, gs, bias, "bf16", ratio)
+    for cut in (0, 1, 3, 4, 5, 18, 36, 37):
+        r1, fx, fg = o.compress(xs[:cut], gs[:cut], bias, "bf16", ratio)
+        r2, fx2, fg2 = o.compress(xs[cut:], gs[cut:], bias, "bf16", ratio, fx, fg)
+        assert np.array_equal(np.concatenate([r1, r2]), whole), cut
+        assert np.array_equal(fx2, wfx) and np.array_equal(fg2, wfg), cut
+
+
 ALL_CHECKS = [
     check_f16_decode_exhaustive, check_bf16_decode_exhaustive, check_encode_rne,
     check_visibility, check_golden_example, check_scores_int64_closed_form,
@@ -580,4 +657,6 @@ ALL_CHECKS = [
     check_decode_schedule, check_decode_steps_brute_force, check_local_only_vs_textbook,
     check_local_pooled_union_vs_textbook, check_local_pooled_lse_merge, check_local_zero_query_is_mean,
     check_local_window_off_is_sparse_attn, check_index_and_attend_local_composes,
+    check_compress_equal_gates_is_mean, check_compress_dominant_gate_selects_row, check_compress_vs_numpy,
+    check_compress_split_calls_equal_one,
 ]

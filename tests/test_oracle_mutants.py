@@ -48,6 +48,16 @@ MUTANTS = {
     "window_rows_from_pooled_kv": ("ref_decode_n(kv_local + (int64_t)wrows[j] * Dkv",
                                    "ref_decode_n(kv + (int64_t)wrows[j] * Dkv"),
     "window_of_first_token": ("ref_window_rows(positions[t], window", "ref_window_rows(positions[0], window"),
+    "compress_bias_reversed": ("(double)bias[(int64_t)i * D + d];", "(double)bias[(int64_t)(ratio - 1 - i) * D + d];"),
+    "compress_bias_dropped": ("(double)bias[(int64_t)i * D + d];", "0.0;"),
+    "compress_frontier_ignored": ("return v < n_frontier ? held + v * D : fresh + (v - n_frontier) * D;",
+                                  "return fresh + (v < n_frontier ? 0 : v - n_frontier) * D;"),
+    "compress_not_normalised": ("rows[j * D + d] = ref_from_double(acc / sum, dtype);",
+                                "rows[j * D + d] = ref_from_double(acc, dtype);"),
+    "compress_gate_of_next_position": ("const int64_t v = j * ratio + i;\n        z[i]",
+                                       "const int64_t v = j * ratio + (i + 1) % ratio;\n        z[i]"),
+    "compress_frontier_shifted": ("memcpy(fx_out + i * D, ref_seq_row(fx_in, x, n_frontier, v, D),",
+                                  "memcpy(fx_out + i * D, ref_seq_row(fx_in, x, n_frontier, v + 1 < n ? v + 1 : v, D),"),
     "w_index_transposed": ("ref_decode_n(w + (int64_t)t * H, H, REF_F16, wd);\n      int64_t n",
                            "ref_decode_n(w + (int64_t)t, H, REF_F16, wd);\n      int64_t n"),
 }
