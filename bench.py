@@ -56,6 +56,7 @@ def parse():
     ap.add_argument("--host-chunks", type=int, default=0,
                     help="token sub-chunks of the host-buffer call in the e2e leg (0: the library's choice)")
     ap.add_argument("--no-decode", action="store_true", help="skip the 1M-context decode measurement")
+    ap.add_argument("--no-compress", action="store_true", help="skip the compressor measurement")
     ap.add_argument("--decode-steps", type=int, default=256, help="decode steps per timed call (decode_1m)")
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
@@ -361,6 +362,44 @@ def measure_decode(ds4x, torch, dev, stream, seed: int, reps: int = 3, n_steps: 
     }
 
 
+def measure_compress(ds4x, torch, dev, stream, seed: int, reps: int = 20):
+    """The compressor on a 2048-token prefill chunk (k rows: fp16 D=128; kv rows: bf16 D=512; ratio 4
+    and 128, a 3-position frontier held over) and on a 64k-token batch of kv rows (HBM bandwidth).
+    Device time per call, L2 flushed before each; bytes = every input byte once + the outputs."""
+    flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+    cases = [("k_8k_r4", "f16", 128, 4, 2048, 3), ("kv_8k_r4", "bf16", 512, 4, 2048, 3),
+             ("kv_8k_r128", "bf16", 512, 128, 2048, 3), ("kv_64k_r4", "bf16", 512, 4, 65536, 3)]
+    out = {}
+    for name, dt, D, ratio, T, f in cases:
+        x, g, fx, fg, bias = synth.compress_inputs(seed, f"bench_{name}", T, D, ratio, dt, f)
+        tdt = torch.bfloat16 if dt == "bf16" else torch.float16
+
+        def d16(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(tdt)
+        dx, dg, dfx, dfg = d16(x), d16(g), d16(fx), d16(fg)
+        db = torch.from_numpy(bias).to(dev)
+        n_out, rem = (f + T) // ratio, (f + T) % ratio
+        rows = torch.empty((n_out, D), dtype=tdt, device=dev)
+        fxo = torch.empty((max(rem, 1), D), dtype=tdt, device=dev)
+        fgo = torch.empty((max(rem, 1), D), dtype=tdt, device=dev)
+        ts = []
+        for i in range(reps + 3):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ds4x.compress(dx, dg, db, ratio, dfx, dfg, rows=rows, frontier_x_out=fxo, frontier_g_out=fgo,
+                          stream=stream)
+            e1.record(stream)
+            if i >= 3:
+                ts.append((e0, e1))
+        torch.cuda.synchronize()
+        us = float(np.median([a.elapsed_time(b) for a, b in ts])) * 1e3
+        nbytes = 2 * (f + T) * D * 2 + ratio * D * 4 + n_out * D * 2 + 2 * rem * D * 2
+        out[name] = {"T": T, "D": D, "ratio": ratio, "dtype": dt, "us": us, "bytes": nbytes,
+                     "gbs": nbytes / (us * 1e-6) / 1e9}
+    return out
+
+
 def decode_main(args, ds4x, torch, dev, rank, world):
     """--workload decode_1m: the decode loop is the step (one call = decode_steps tokens)."""
     stream = torch.cuda.current_stream()
@@ -590,6 +629,12 @@ def main():
     if rank == 0 and not args.no_decode and wl.name != "decode_1m":
         dec = measure_decode(ds4x, torch, dev, stream, args.seed)
 
+    comp = None
+    if rank == 0 and not args.no_compress:
+        comp = measure_compress(ds4x, torch, dev, stream, args.seed)
+        for v in comp.values():
+            v["hbm_frac"] = v["gbs"] / peaks["hbm_gbs"]
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         v, cores, desc = cpu_baseline(wl, inp)
@@ -606,7 +651,7 @@ def main():
             "roofline": roof, "stage_ms": stages, "stage_rates": others,
             "staged_ms_per_step": float(stage_ms.sum(axis=1).mean()),
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
-            "clocks": sampler.summary(), "decode": dec,
+            "clocks": sampler.summary(), "decode": dec, "compress": comp,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

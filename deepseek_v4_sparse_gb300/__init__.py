@@ -25,6 +25,7 @@ OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_TIMEOUT = 0, -1, 
 F16, BF16 = 0, 1
 MAX_KTOP = 1024
 MAX_WINDOW = 1024
+MAX_RATIO = 65536
 EXPORTS = (
     "ds4x_indexer_score", "ds4x_topk", "ds4x_topk_workspace_bytes", "ds4x_sparse_attn",
     "ds4x_index_and_attend", "ds4x_workspace_bytes", "ds4x_status_string",
@@ -32,7 +33,7 @@ EXPORTS = (
     "ds4x_topk_static_scratch", "ds4x_decode", "ds4x_decode_workspace_bytes",
     "ds4x_index_and_attend_host", "ds4x_index_and_attend_host_bytes",
     "ds4x_local_pooled_attn", "ds4x_index_and_attend_local", "ds4x_workspace_bytes_local",
-    "ds4x_index_and_attend_local_host", "ds4x_index_and_attend_local_host_bytes",
+    "ds4x_index_and_attend_local_host", "ds4x_index_and_attend_local_host_bytes", "ds4x_compress",
 )
 
 _lock = threading.Lock()
@@ -79,6 +80,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                                          sz, P]
         lib.ds4x_index_and_attend_local_host_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, i32]
         lib.ds4x_index_and_attend_local_host_bytes.restype = sz
+        lib.ds4x_compress.argtypes = [P, P, P, ctypes.c_int, i32, i32, i32, P, P, i32, P, P, P, P]
         lib.ds4x_decode.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, P, i32, i32, i32, i32, i32, i32, i32,
                                     i32, i32, f32, P, P, P, P, P, sz, ctypes.POINTER(i32), P]
         lib.ds4x_decode_workspace_bytes.argtypes = [i32, i32]
@@ -90,7 +92,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.ds4x_selftest_bounded_wait.argtypes = [i64, P]
         for f in ("ds4x_indexer_score", "ds4x_topk", "ds4x_sparse_attn", "ds4x_index_and_attend", "ds4x_decode",
                   "ds4x_index_and_attend_host", "ds4x_local_pooled_attn", "ds4x_index_and_attend_local",
-                  "ds4x_index_and_attend_local_host",
+                  "ds4x_index_and_attend_local_host", "ds4x_compress",
                   "ds4x_last_launch_count", "ds4x_device_status", "ds4x_selftest_bounded_wait"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
@@ -390,6 +392,30 @@ def index_and_attend_local_host(q, w, k, positions, q_attn, kv, kv_local, ratio:
         _host_ptr(indices), _host_ptr(out), _host_ptr(lse), n_chunks, _ptr(device_buffer), dbytes, _stream(stream))
     _check("ds4x_index_and_attend_local_host", rc)
     return indices, out, lse
+
+
+# ------------------------------------------------------------------------------- compressor
+def compress(x, g, bias, ratio: int, frontier_x=None, frontier_g=None, rows=None, frontier_x_out=None,
+             frontier_g_out=None, stream=None):
+    """One gated-pooled row per `ratio` positions of the sequence frontier + (x, g).
+    x, g [T, D] and the frontier [f, D] (f < ratio) fp16 or bf16; bias [ratio, D] fp32.
+    Returns (rows [(f+T)//ratio, D], new frontier x, new frontier g [(f+T)%ratio, D])."""
+    torch = _torch()
+    dt = _kv_dtype(x)
+    T, D = x.shape
+    f = 0 if frontier_x is None else int(frontier_x.shape[0])
+    n_out, rem = (f + T) // ratio, (f + T) % ratio
+    if rows is None:
+        rows = torch.empty((n_out, D), dtype=x.dtype, device=x.device)
+    if frontier_x_out is None:
+        frontier_x_out = torch.empty((rem, D), dtype=x.dtype, device=x.device)
+    if frontier_g_out is None:
+        frontier_g_out = torch.empty((rem, D), dtype=x.dtype, device=x.device)
+    rc = load().ds4x_compress(_ptr(x), _ptr(g), _ptr(bias), dt, T, D, ratio, _ptr(frontier_x), _ptr(frontier_g), f,
+                              _ptr(rows) if n_out else None, _ptr(frontier_x_out) if rem else None,
+                              _ptr(frontier_g_out) if rem else None, _stream(stream))
+    _check("ds4x_compress", rc)
+    return rows, frontier_x_out, frontier_g_out
 
 
 def decode_workspace_bytes(capacity: int, k_top: int = 512) -> int:

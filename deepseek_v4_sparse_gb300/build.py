@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libds4x.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["ds4x_api.cu", "score_tcgen05.cu", "topk_stream.cu", "sparse_mqa.cu", "decode.cu"]
+SOURCES = ["ds4x_api.cu", "score_tcgen05.cu", "topk_stream.cu", "sparse_mqa.cu", "decode.cu", "compress.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "-I", os.path.join(ROOT, "include")]

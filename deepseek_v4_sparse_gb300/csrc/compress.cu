@@ -1,0 +1,273 @@
+// compress.cu — the compressor: one pooled row per `ratio` positions, the partial block carried.
+//
+//   rows[j,d] = sum_i a_i x_i[d],   a_i = softmax_i(g_i[d] + bias[i,d]),   i over block j's positions
+//
+// Source: "How I turned one oversized DeepSeek optimization into three merged oMLX PRs", section
+// "The three changes that merged", item 3 (the skip path still advances the indexer compressor and
+// its cache; one pooled row per `ratio` positions) and the ds4.c overview, disk-cache layout (the
+// "compressor frontier" tensors kept with the compressed rows).  The pages give no formula: the
+// gated pooling above is this library's definition (equal gates give the block mean).
+//
+// Streaming and HBM-bound: a thread owns 8 channels (16-byte loads of x and g) of one block and one
+// slice of the block's positions.  Positions go in batches of four (eight 16-byte loads in flight,
+// one running-max rescale per batch, weights by ex2.approx on log2-scaled gates); the slices of a
+// block are merged through shared memory.
+// Sequence position v is frontier row v (v < n_frontier) or new row v - n_frontier.  One extra CTA
+// copies the new frontier (the positions after the last full block).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "ds4x_internal.h"
+#include "ds4x_ptx.cuh"
+
+namespace ds4x {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kBatch = 4;  // positions loaded before their running-max update
+
+struct CompressParams {
+  const uint16_t* x;   // [T, D]
+  const uint16_t* g;   // [T, D]
+  const float* bias;   // [ratio, D]
+  const uint16_t* fx;  // [nf, D] frontier rows in
+  const uint16_t* fg;
+  uint16_t* rows;      // [n_out, D]
+  uint16_t* fx_out;    // [rem, D] frontier rows out
+  uint16_t* fg_out;
+  int nf, T, D, ratio, n_out, rem;
+  int cg;     // 8-channel groups per CTA slab
+  int slabs;  // slabs per block (D / 8 / cg)
+  int ns;     // position slices per block
+  int bpc;    // blocks per CTA
+  int main_ctas;  // CTAs of blocks (one more copies the frontier)
+};
+
+template <bool kBf16>
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if constexpr (kBf16) {
+      const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
+      f[2 * k] = __low2float(h);
+      f[2 * k + 1] = __high2float(h);
+    } else {
+      const __half2 h = *reinterpret_cast<const __half2*>(&w[k]);
+      f[2 * k] = __low2float(h);
+      f[2 * k + 1] = __high2float(h);
+    }
+  }
+}
+
+template <bool kBf16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (kBf16) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+
+__device__ __forceinline__ const uint4* seq_row(const uint16_t* held, const uint16_t* fresh, int nf, int64_t v,
+                                                int D) {
+  return reinterpret_cast<const uint4*>(v < nf ? held + v * D : fresh + (v - nf) * D);
+}
+
+__device__ __forceinline__ uint4 ldg16(const uint4* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// 2^x with the hardware approximation (MUFU.EX2; flushes subnormal results to zero); 2^-inf = 0.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// z = (g + bias) log2(e) for the 8 channels of one position
+template <bool kBf16>
+__device__ __forceinline__ void gate8(const uint4& ug, const float* bias_row, float (&z)[8]) {
+  unpack8<kBf16>(ug, z);
+  const float4 b0 = __ldg(reinterpret_cast<const float4*>(bias_row));
+  const float4 b1 = __ldg(reinterpret_cast<const float4*>(bias_row) + 1);
+  const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+  for (int k = 0; k < 8; ++k) z[k] = (z[k] + bb[k]) * 1.4426950408889634f;
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kThreads) compress_kernel(const CompressParams p) {
+  __shared__ float part[kThreads][24];  // a slice's (m, l, acc) of its 8 channels
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x;
+  if ((int)blockIdx.x >= p.main_ctas) {
+    // ------------------------------------------------ the new frontier: rem positions of x and g
+    const int per_row = p.D / 8;
+    for (int idx = tid; idx < p.rem * per_row; idx += blockDim.x) {
+      const int i = idx / per_row, c = idx - i * per_row;
+      const int64_t v = (int64_t)p.n_out * p.ratio + i;
+      reinterpret_cast<uint4*>(p.fx_out + (int64_t)i * p.D)[c] = seq_row(p.fx, p.x, p.nf, v, p.D)[c];
+      reinterpret_cast<uint4*>(p.fg_out + (int64_t)i * p.D)[c] = seq_row(p.fg, p.g, p.nf, v, p.D)[c];
+    }
+    return;
+  }
+  const int c = tid % p.cg;
+  const int s = (tid / p.cg) % p.ns;
+  const int b = tid / (p.cg * p.ns);
+  const int slab = blockIdx.x % p.slabs;
+  const int64_t j = (int64_t)(blockIdx.x / p.slabs) * p.bpc + b;
+  const int grp = slab * p.cg + c;  // 8-channel group within the row
+  const bool active = b < p.bpc && j < p.n_out;
+  // running max (log2 units), sum and weighted sum of the 8 channels
+  float m[8], l[8], acc[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    m[k] = -INFINITY;
+    l[k] = 0.f;
+    acc[k] = 0.f;
+  }
+  if (active) {
+    const int i0 = (int)((int64_t)s * p.ratio / p.ns), i1 = (int)((int64_t)(s + 1) * p.ratio / p.ns);
+    for (int i = i0; i < i1; i += kBatch) {
+      const int nb = min(kBatch, i1 - i);
+      uint4 ux[kBatch], ug[kBatch];
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        if (q < nb) {
+          const int64_t v = j * p.ratio + i + q;
+          ux[q] = ldg16(seq_row(p.fx, p.x, p.nf, v, p.D) + grp);
+          ug[q] = ldg16(seq_row(p.fg, p.g, p.nf, v, p.D) + grp);
+        }
+      }
+      // the batch's max raises the running max once; then its weights
+      float bm[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) bm[k] = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        if (q < nb) {
+          float z[8];
+          gate8<kBf16>(ug[q], p.bias + (int64_t)(i + q) * p.D + grp * 8, z);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) bm[k] = fmaxf(bm[k], z[k]);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float mn = fmaxf(m[k], bm[k]);
+        const float sc = ex2_approx(m[k] - mn);  // 0 while m is still -inf
+        l[k] *= sc;
+        acc[k] *= sc;
+        m[k] = mn;
+      }
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        if (q < nb) {
+          float z[8], xv[8];
+          gate8<kBf16>(ug[q], p.bias + (int64_t)(i + q) * p.D + grp * 8, z);
+          unpack8<kBf16>(ux[q], xv);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float a = ex2_approx(z[k] - m[k]);
+            l[k] += a;
+            acc[k] = fmaf(a, xv[k], acc[k]);
+          }
+        }
+      }
+    }
+  }
+  if (p.ns > 1) {
+    // merge the slices of each (block, channel group) as a tree in shared memory:
+    // M = max m_s, L = sum l_s 2^(m_s - M), the same for acc
+    for (int half = p.ns / 2; half >= 1; half /= 2) {
+      if (s >= half && s < 2 * half) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          part[tid][k] = m[k];
+          part[tid][8 + k] = l[k];
+          part[tid][16 + k] = acc[k];
+        }
+      }
+      __syncthreads();
+      if (s < half) {
+        const int o = tid + half * p.cg;  // slice s + half of the same (block, channel group)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float mo = part[o][k];
+          const float mn = fmaxf(m[k], mo);
+          if (mn == -INFINITY) continue;
+          const float sa = ex2_approx(m[k] - mn), sb = ex2_approx(mo - mn);
+          l[k] = l[k] * sa + part[o][8 + k] * sb;
+          acc[k] = acc[k] * sa + part[o][16 + k] * sb;
+          m[k] = mn;
+        }
+      }
+      __syncthreads();
+    }
+    if (s != 0) return;
+  }
+  if (!active) return;
+  uint4 o;
+  o.x = pack2<kBf16>(acc[0] / l[0], acc[1] / l[1]);
+  o.y = pack2<kBf16>(acc[2] / l[2], acc[3] / l[3]);
+  o.z = pack2<kBf16>(acc[4] / l[4], acc[5] / l[5]);
+  o.w = pack2<kBf16>(acc[6] / l[6], acc[7] / l[7]);
+  reinterpret_cast<uint4*>(p.rows + j * p.D)[grp] = o;
+}
+
+}  // namespace
+
+// Launch shape: ns position slices, a slab of cg 8-channel groups (the largest divisor of D/8 with
+// cg * ns <= kThreads), bpc blocks per CTA filling kThreads.
+int launch_compress(const CompressArgs& a, cudaStream_t stream) {
+  CompressParams p;
+  p.x = static_cast<const uint16_t*>(a.x);
+  p.g = static_cast<const uint16_t*>(a.g);
+  p.bias = a.bias;
+  p.fx = static_cast<const uint16_t*>(a.fx);
+  p.fg = static_cast<const uint16_t*>(a.fg);
+  p.rows = static_cast<uint16_t*>(a.rows);
+  p.fx_out = static_cast<uint16_t*>(a.fx_out);
+  p.fg_out = static_cast<uint16_t*>(a.fg_out);
+  p.nf = a.n_frontier;
+  p.T = a.T;
+  p.D = a.D;
+  p.ratio = a.ratio;
+  const int64_t n = (int64_t)a.n_frontier + a.T;
+  p.n_out = (int)(n / a.ratio);
+  p.rem = (int)(n % a.ratio);
+  if (p.n_out == 0 && p.rem == 0) return DS4X_OK;
+  const int groups = a.D / 8;
+  // position slices: as many as it takes for about four CTAs of work per SM (a power of two, at
+  // most 32 and at most ratio / kBatch), so a ratio-128 block of a 2048-token chunk spreads out
+  // while a long batch of blocks streams its positions in one thread
+  const int64_t want = 4ll * device_sm_count() * kThreads;
+  int ns = 1;
+  while (2 * ns <= a.ratio / kBatch && 2 * ns <= 32 && (int64_t)p.n_out * groups * ns < want) ns *= 2;
+  int cg = groups < kThreads / ns ? groups : kThreads / ns;
+  while (groups % cg) --cg;
+  p.cg = cg;
+  p.slabs = groups / cg;
+  p.ns = ns;
+  p.bpc = kThreads / (cg * ns);
+  p.main_ctas = (int)((p.n_out + p.bpc - 1) / p.bpc) * p.slabs;
+  const int grid = p.main_ctas + (p.rem > 0 ? 1 : 0);
+  const cudaError_t e = a.bf16 ? launch_pdl(compress_kernel<true>, dim3(grid), dim3(kThreads), 0, stream, p)
+                               : launch_pdl(compress_kernel<false>, dim3(grid), dim3(kThreads), 0, stream, p);
+  if (e != cudaSuccess) return DS4X_ERR_CUDA;
+  count_launch();
+  return DS4X_OK;
+}
+
+}  // namespace ds4x

@@ -491,6 +491,27 @@ int ds4x_index_and_attend_local_host(const void* q, const void* w, const void* k
                    lse, n_chunks, device_buffer, device_bytes, stream, window_of(kv_local, local_pos0, L, window));
 }
 
+int ds4x_compress(const void* x, const void* g, const float* bias, ds4x_dtype dtype, int32_t T, int32_t D,
+                  int32_t ratio, const void* frontier_x, const void* frontier_g, int32_t n_frontier, void* rows,
+                  void* frontier_x_out, void* frontier_g_out, void* stream) {
+  CallScope scope;
+  if (T < 0 || D < 8 || D % 8 != 0 || ratio < 1 || ratio > DS4X_MAX_RATIO || n_frontier < 0 || n_frontier >= ratio)
+    return DS4X_ERR_INVALID;
+  if (dtype != DS4X_F16 && dtype != DS4X_BF16) return DS4X_ERR_INVALID;
+  const int64_t n = (int64_t)n_frontier + T;
+  const int64_t n_out = n / ratio, rem = n % ratio;
+  if (T > 0 && (!x || !g || !aligned16(x) || !aligned16(g))) return DS4X_ERR_INVALID;
+  if (n_frontier > 0 && (!frontier_x || !frontier_g || !aligned16(frontier_x) || !aligned16(frontier_g)))
+    return DS4X_ERR_INVALID;
+  if (n_out > 0 && (!rows || !bias || !aligned16(rows) || !aligned16(bias))) return DS4X_ERR_INVALID;
+  if (rem > 0 && (!frontier_x_out || !frontier_g_out || !aligned16(frontier_x_out) || !aligned16(frontier_g_out)))
+    return DS4X_ERR_INVALID;
+  if (n_out == 0 && rem == 0) return scope.done(DS4X_OK);
+  CompressArgs a{x, g, bias, frontier_x, frontier_g, rows, frontier_x_out, frontier_g_out,
+                 dtype == DS4X_BF16 ? 1 : 0, T, D, ratio, n_frontier};
+  return scope.done(launch_compress(a, static_cast<cudaStream_t>(stream)));
+}
+
 int ds4x_device_status(void* stream, int clear) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* p = device_status_ptr();

@@ -94,6 +94,20 @@ bool attn_shape_supported(int Hq, int Dkv);
 // Scratch the split mode wants for T tokens on the current device (0: no split at this T).
 size_t attn_partial_bytes(int T, int k_top, int window);
 
+struct CompressArgs {
+  const void* x;       // [T, D] raw rows
+  const void* g;       // [T, D] gate logits
+  const float* bias;   // [ratio, D]
+  const void* fx;      // [n_frontier, D] held-over raw rows
+  const void* fg;      // [n_frontier, D] held-over gate logits
+  void* rows;          // [(n_frontier + T) / ratio, D]
+  void* fx_out;        // [(n_frontier + T) % ratio, D]
+  void* fg_out;
+  int bf16;
+  int T, D, ratio, n_frontier;
+};
+int launch_compress(const CompressArgs& a, cudaStream_t stream);
+
 // The fused path (score -> top-k -> attention, Hq = 64, Dkv = 512) on validated arguments, and
 // the workspace it needs: [scores T x S fp32 | top-k scratch | split-attention scratch].
 size_t fused_workspace_bytes(int T, int S, int k_top, int window = 0);

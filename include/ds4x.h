@@ -261,6 +261,32 @@ size_t ds4x_index_and_attend_local_host_bytes(int32_t T, int32_t H, int32_t D, i
                                               int32_t window, int32_t n_chunks);
 
 /* ---------------------------------------------------------------------------
+ * ds4x_compress — the compressor: one pooled row per `ratio` positions, with the partial block
+ * carried from call to call as the "frontier" ([S] item 3: the skip path still advances the
+ * indexer compressor and its cache; the ds4.c overview keeps "compressor frontier" tensors with
+ * the compressed rows).  The pages give no formula; this library's definition:
+ *
+ *   the sequence is the n_frontier held-over positions (frontier_x, frontier_g) followed by the
+ *   T new positions (x, g); block j = sequence positions j*ratio .. j*ratio + ratio - 1, and
+ *     rows[j, d] = sum_i a_i x_i[d],   a_i = exp(z_i) / sum_i' exp(z_i'),   z_i = g_i[d] + bias[i, d]
+ *   (i = position inside the block; softmax in fp32, rows rounded to `dtype`, equal gates give the
+ *   mean).  The (n_frontier + T) % ratio positions after the last full block are copied to
+ *   frontier_x_out / frontier_g_out: the next call's frontier.
+ *
+ *   x, g [T, D] and frontier_x, frontier_g [n_frontier, D] of `dtype` (raw rows and gate logits,
+ *   the outputs of the compressor's projections); bias [ratio, D] fp32 (learned per-position
+ *   weights); rows [(n_frontier + T) / ratio, D] of `dtype` (e.g. the next rows of k or kv);
+ *   frontier_*_out [(n_frontier + T) % ratio, D].  D % 8 == 0, 1 <= ratio <= DS4X_MAX_RATIO,
+ *   0 <= n_frontier < ratio.  The outputs must not overlap the inputs (keep two frontier buffers
+ *   and swap them between calls).  One launch; HBM-bound (every input byte read once).
+ * ------------------------------------------------------------------------- */
+#define DS4X_MAX_RATIO 65536
+int ds4x_compress(const void* x, const void* g, const float* bias, ds4x_dtype dtype, int32_t T,
+                  int32_t D, int32_t ratio, const void* frontier_x, const void* frontier_g,
+                  int32_t n_frontier, void* rows, void* frontier_x_out, void* frontier_g_out,
+                  void* stream);
+
+/* ---------------------------------------------------------------------------
  * ds4x_decode — the decode loop: n_steps query tokens at consecutive positions
  * pos0, pos0+1, ..., one fused step (ds4x_index_and_attend with T = 1) each, with the
  * compressed rows appended as the positions complete them ([K]: decode at long context;

@@ -266,3 +266,15 @@ def custom_inputs(seed: int, tag: str, T: int, H: int, D: int, rows: int, Hq: in
     q_attn = _bits(seed, wl, "q_attn", T * Hq * Dkv, (-2, 2), kv_dtype).reshape(T, Hq, Dkv)
     kv = _bits(seed, wl, "kv", rows * Dkv, (-2, 2), kv_dtype).reshape(rows, Dkv)
     return Inputs(wl, q, w, k, np.asarray(positions, dtype=np.int32), q_attn, kv)
+
+
+def compress_inputs(seed: int, tag: str, T: int, D: int, ratio: int, dtype: str, n_frontier: int = 0):
+    """Compressor inputs: raw rows x and gate logits g [T, D] (N(0,1), dtype bits), a held-over
+    frontier fx, fg [n_frontier, D] drawn the same way, and the per-position bias [ratio, D]
+    (N(0,1), float32)."""
+    x = normal_bits(seed, f"{tag}/x", T * D, dtype).reshape(T, D)
+    g = normal_bits(seed, f"{tag}/g", T * D, dtype).reshape(T, D)
+    fx = normal_bits(seed, f"{tag}/fx", n_frontier * D, dtype).reshape(n_frontier, D)
+    fg = normal_bits(seed, f"{tag}/fg", n_frontier * D, dtype).reshape(n_frontier, D)
+    bias = normal(seed, f"{tag}/bias", ratio * D).astype(np.float32).reshape(ratio, D)
+    return x, g, fx, fg, bias

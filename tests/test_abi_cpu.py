@@ -210,3 +210,29 @@ def test_local_workspace_and_staging_sizes(lib):
         # the window's rows are staged once, beside k and kv
         assert L * Dkv * 2 <= local - plain <= L * Dkv * 2 + 256
         assert ds4x.index_and_attend_local_host_bytes(T, H, D, S, k_top, Hq, Dkv, L, 0, n) == plain
+
+
+def _compress(lib, T=16, D=128, ratio=4, nf=0, x=0x10000, fx=0x10000, rows=0x10000, fxo=0x10000, bias=0x10000,
+              dtype=0):
+    A = 0x10000
+    return lib.ds4x_compress(_p(x) if x else None, _p(A), _p(bias) if bias else None, dtype, T, D, ratio,
+                             _p(fx) if fx else None, _p(A), nf, _p(rows) if rows else None, _p(fxo) if fxo else None,
+                             _p(A), None)
+
+
+def test_compress_arguments_rejected_without_launch(lib):
+    assert _compress(lib, D=100) == ds4x.ERR_INVALID             # rows of whole 16-byte units
+    assert _compress(lib, D=0) == ds4x.ERR_INVALID
+    assert _compress(lib, ratio=0) == ds4x.ERR_INVALID
+    assert _compress(lib, ratio=ds4x.MAX_RATIO + 1) == ds4x.ERR_INVALID
+    assert _compress(lib, nf=4) == ds4x.ERR_INVALID              # a frontier is shorter than a block
+    assert _compress(lib, nf=-1) == ds4x.ERR_INVALID
+    assert _compress(lib, T=-1) == ds4x.ERR_INVALID
+    assert _compress(lib, dtype=9) == ds4x.ERR_INVALID
+    assert _compress(lib, x=0) == ds4x.ERR_INVALID               # new positions but no rows
+    assert _compress(lib, x=0x10002) == ds4x.ERR_INVALID         # misaligned
+    assert _compress(lib, nf=2, fx=0) == ds4x.ERR_INVALID        # a frontier but no buffer
+    assert _compress(lib, rows=0) == ds4x.ERR_INVALID            # 4 blocks complete but nowhere to write
+    assert _compress(lib, bias=0) == ds4x.ERR_INVALID
+    assert _compress(lib, T=6, fxo=0) == ds4x.ERR_INVALID        # 2 positions left over, no frontier out
+    assert _compress(lib, T=0) == ds4x.OK                        # nothing to do, nothing launched
