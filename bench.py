@@ -69,6 +69,20 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(torch, dist, x: float, world: int, dev) -> float:
+    """The largest of every rank's x (the slowest rank sets a step's time); x itself at N = 1."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, units_per_rank: int, ms: float) -> float:
+    """Whole-job units per second: every rank processes its own units in `ms` (max over ranks)."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 def workload_config(wl: synth.Workload, l2_note: str) -> dict:
     return {
         "workload": f"{wl.name}: {wl.T} query tokens at positions {wl.pos0}..{wl.pos0 + wl.T - 1}, "
@@ -402,6 +416,7 @@ def measure_compress(ds4x, torch, dev, stream, seed: int, reps: int = 20):
 
 def decode_main(args, ds4x, torch, dev, rank, world):
     """--workload decode_1m: the decode loop is the step (one call = decode_steps tokens)."""
+    import torch.distributed as dist
     stream = torch.cuda.current_stream()
     sampler = ClockSampler(dev.index or 0)
     with sampler:
@@ -418,10 +433,13 @@ def decode_main(args, ds4x, torch, dev, rank, world):
             "algorithmic": step_bytes, "traffic": None}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["peak_source"] = f"{peaks['source']} (burst)"
+    # the slowest rank's time per decode step; each rank decodes its own token stream
+    us_step = max_over_ranks(torch, dist, dec["us_per_step"], world, dev)
     if rank == 0:
         step_ms = 1e3 * dec["steps"] / dec["value"]
         line = {
-            "metric": METRIC, "value": world * dec["value"], "unit": "decode tokens/s", "n_gpus": world,
+            "metric": METRIC, "value": job_throughput(world, 1, us_step / 1e3), "unit": "decode tokens/s",
+            "n_gpus": world,
             "steps": max(1, args.steps), "warmup": max(3, args.warmup), "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16+bf16 (fp32 accumulate)",
             "data": "synthetic", "config": {"workload": dec["workload"], "l2": dec["l2"]},
@@ -543,11 +561,7 @@ def main():
         barrier()
     fused_ms = [a.elapsed_time(b) for a, b in fused_ev]
     stage_ms = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in stage_ev])
-    step_ms = float(np.mean(fused_ms))
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(torch, dist, float(np.mean(fused_ms)), world, dev)
     assert ds4x.device_status() == ds4x.OK, "a bounded device wait timed out during the timed region"
 
     # ------------------------------------------- end to end through the C ABI (host buffers)
@@ -586,12 +600,8 @@ def main():
             e2e_step()
         e1.record(stream)
         barrier()
-        e_ms = e0.elapsed_time(e1) / e_steps
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * T / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+        e_ms = max_over_ranks(torch, dist, e0.elapsed_time(e1) / e_steps, world, dev)
+        e2e = {"value": job_throughput(world, T, e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms,
                "call": ("ds4x_index_and_attend_local_host" if win else "ds4x_index_and_attend_host") +
                        " (page-locked host buffers; copies in, work and copies out "
@@ -642,7 +652,7 @@ def main():
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": world * T / (step_ms / 1e3), "unit": UNIT, "n_gpus": world,
+            "metric": METRIC, "value": job_throughput(world, T, step_ms), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16+bf16 (fp32 accumulate)",
             "data": "synthetic",
