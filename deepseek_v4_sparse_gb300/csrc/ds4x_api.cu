@@ -147,17 +147,20 @@ using namespace ds4x;
 
 namespace {
 // ------------------------------------------------------------- the host-buffer fused path
-// Device staging of ds4x_index_and_attend_host: [k | kv | fused workspace of one sub-chunk |
-// two slots of one sub-chunk's per-token inputs and outputs], every part 256-byte aligned.
+// Device staging of ds4x_index_and_attend_host: [k | kv | window rows | w, positions and lse of every
+// token | fused workspace of one sub-chunk | kHostSlots slots of one sub-chunk's q, q_attn, indices
+// and out], every part 256-byte aligned.  The small per-token arrays move in one copy each; the
+// large ones by sub-chunk, rotating over the slots.
+constexpr int kHostSlots = 3;
 struct HostLayout {
-  int n = 0, tc = 0;                                 // sub-chunks, tokens per sub-chunk
-  size_t k = 0, kv = 0, kvl = 0, ws = 0, ws_bytes = 0, slot0 = 0, slot = 0, total = 0;
-  size_t q = 0, w = 0, pos = 0, qa = 0, idx = 0, out = 0, lse = 0;  // offsets within a slot
+  int n = 0, tc = 0, ns = 0;                         // sub-chunks, tokens per sub-chunk, slots in use
+  size_t k = 0, kv = 0, kvl = 0, w = 0, pos = 0, lse = 0, ws = 0, ws_bytes = 0, slot0 = 0, slot = 0, total = 0;
+  size_t q = 0, qa = 0, idx = 0, out = 0;            // offsets within a slot
 };
 
-int default_host_chunks(int T) {  // sub-chunks of about 512 tokens (a few CTA waves each)
-  const int n = T / 512;
-  return n < 1 ? 1 : n > 8 ? 8 : n;
+int default_host_chunks(int T) {  // sub-chunks of about 256 tokens
+  const int n = T / 256;
+  return n < 1 ? 1 : n > 16 ? 16 : n;
 }
 
 HostLayout host_layout(int T, int H, int D, int S, int k_top, int Hq, int Dkv, int n_chunks, int Lrows = 0,
@@ -167,6 +170,7 @@ HostLayout host_layout(int T, int H, int D, int S, int k_top, int Hq, int Dkv, i
   L.n = n_chunks > 0 ? (n_chunks < T ? n_chunks : T) : default_host_chunks(T);
   L.tc = (T + L.n - 1) / L.n;
   L.n = (T + L.tc - 1) / L.tc;  // no empty sub-chunk
+  L.ns = L.n < kHostSlots ? L.n : kHostSlots;
   const size_t tc = (size_t)L.tc, e16 = 2;
   size_t o = 0;
   L.k = o;
@@ -175,27 +179,27 @@ HostLayout host_layout(int T, int H, int D, int S, int k_top, int Hq, int Dkv, i
   o += round256((size_t)S * Dkv * e16);
   L.kvl = o;
   o += win ? round256((size_t)Lrows * Dkv * e16) : 0;
+  L.w = o;
+  o += round256((size_t)T * H * e16);
+  L.pos = o;
+  o += round256((size_t)T * sizeof(int32_t));
+  L.lse = o;
+  o += round256((size_t)T * Hq * sizeof(float));
   L.ws = o;
   L.ws_bytes = fused_workspace_bytes(L.tc, S, k_top, win ? window : 0);
   o += round256(L.ws_bytes);
   size_t s = 0;
   L.q = s;
   s += round256(tc * H * D * e16);
-  L.w = s;
-  s += round256(tc * H * e16);
-  L.pos = s;
-  s += round256(tc * sizeof(int32_t));
   L.qa = s;
   s += round256(tc * Hq * Dkv * e16);
   L.idx = s;
   s += round256(tc * k_top * sizeof(int32_t));
   L.out = s;
   s += round256(tc * Hq * Dkv * e16);
-  L.lse = s;
-  s += round256(tc * Hq * sizeof(float));
   L.slot = s;
   L.slot0 = o;
-  L.total = o + 2 * s;
+  L.total = o + (size_t)L.ns * s;
   return L;
 }
 
@@ -205,7 +209,8 @@ struct HostPipe {
   std::mutex m;
   bool ready = false;
   cudaStream_t in = nullptr, out = nullptr;
-  cudaEvent_t start = nullptr, in_done[2] = {}, work_done[2] = {}, out_done[2] = {};
+  cudaEvent_t start = nullptr, fin = nullptr, in_done[kHostSlots] = {}, work_done[kHostSlots] = {},
+              out_done[kHostSlots] = {};
 };
 HostPipe g_host_pipe[kMaxDevices];
 
@@ -214,7 +219,8 @@ cudaError_t host_pipe_init(HostPipe& hp) {
   cudaError_t e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming);
-  for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.fin, cudaEventDisableTiming);
+  for (int i = 0; i < kHostSlots && e == cudaSuccess; ++i) {
     e = cudaEventCreateWithFlags(&hp.in_done[i], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.work_done[i], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.out_done[i], cudaEventDisableTiming);
@@ -419,41 +425,42 @@ int host_path(const void* q, const void* w, const void* k, const int32_t* positi
     DS4X_CK(cudaMemcpyAsync(base + L.kvl, lw.kv_local, (size_t)lw.L * Dkv * 2, h2d, hp.in));
     dlw.kv_local = base + L.kvl;
   }
-  const size_t qt = (size_t)H * D * 2, wt = (size_t)H * 2, at = (size_t)Hq * Dkv * 2;
-  const size_t it = (size_t)k_top * sizeof(int32_t), lt = (size_t)Hq * sizeof(float);
+  // every token's w and position, once
+  DS4X_CK(cudaMemcpyAsync(base + L.w, w, (size_t)T * H * 2, h2d, hp.in));
+  DS4X_CK(cudaMemcpyAsync(base + L.pos, positions, (size_t)T * sizeof(int32_t), h2d, hp.in));
+  const size_t qt = (size_t)H * D * 2, at = (size_t)Hq * Dkv * 2, it = (size_t)k_top * sizeof(int32_t);
+  float* lse_dev = reinterpret_cast<float*>(base + L.lse);
   for (int j = 0; j < L.n; ++j) {
-    const int b = j & 1;
+    const int b = j % L.ns;
     const size_t t0 = (size_t)j * L.tc;
     const int tn = (int)((size_t)T - t0 < (size_t)L.tc ? (size_t)T - t0 : (size_t)L.tc);
     uint8_t* sl = base + L.slot0 + b * L.slot;
-    // inputs of sub-chunk j, once sub-chunk j-2 (same slot) has been computed
-    if (j >= 2) DS4X_CK(cudaStreamWaitEvent(hp.in, hp.work_done[b], 0));
+    // inputs of sub-chunk j, once sub-chunk j - ns (same slot) has been computed
+    if (j >= L.ns) DS4X_CK(cudaStreamWaitEvent(hp.in, hp.work_done[b], 0));
     DS4X_CK(cudaMemcpyAsync(sl + L.q, static_cast<const uint8_t*>(q) + t0 * qt, tn * qt, h2d, hp.in));
-    DS4X_CK(cudaMemcpyAsync(sl + L.w, static_cast<const uint8_t*>(w) + t0 * wt, tn * wt, h2d, hp.in));
-    DS4X_CK(cudaMemcpyAsync(sl + L.pos, positions + t0, tn * sizeof(int32_t), h2d, hp.in));
     DS4X_CK(cudaMemcpyAsync(sl + L.qa, static_cast<const uint8_t*>(q_attn) + t0 * at, tn * at, h2d, hp.in));
     DS4X_CK(cudaEventRecord(hp.in_done[b], hp.in));
-    // the work, once the inputs are in and sub-chunk j-2's outputs are out of the slot
+    // the work, once the inputs are in and sub-chunk j - ns's outputs are out of the slot
     DS4X_CK(cudaStreamWaitEvent(st, hp.in_done[b], 0));
-    if (j >= 2) DS4X_CK(cudaStreamWaitEvent(st, hp.out_done[b], 0));
-    const int rc = run_index_and_attend(sl + L.q, sl + L.w, S > 0 ? base + L.k : nullptr,
-                                        reinterpret_cast<const int32_t*>(sl + L.pos), sl + L.qa,
+    if (j >= L.ns) DS4X_CK(cudaStreamWaitEvent(st, hp.out_done[b], 0));
+    const int rc = run_index_and_attend(sl + L.q, base + L.w + t0 * H * 2, S > 0 ? base + L.k : nullptr,
+                                        reinterpret_cast<const int32_t*>(base + L.pos) + t0, sl + L.qa,
                                         S > 0 ? base + L.kv : nullptr, kv_dtype == DS4X_BF16 ? 1 : 0, tn, H, D, S,
                                         ratio, k_top, scale, reinterpret_cast<int32_t*>(sl + L.idx), sl + L.out,
-                                        lse ? reinterpret_cast<float*>(sl + L.lse) : nullptr, base + L.ws,
-                                        L.ws_bytes, st, dlw);
+                                        lse ? lse_dev + t0 * Hq : nullptr, base + L.ws, L.ws_bytes, st, dlw);
     if (rc != DS4X_OK) return rc;
     DS4X_CK(cudaEventRecord(hp.work_done[b], st));
     // outputs of sub-chunk j
     DS4X_CK(cudaStreamWaitEvent(hp.out, hp.work_done[b], 0));
     DS4X_CK(cudaMemcpyAsync(indices + t0 * k_top, sl + L.idx, tn * it, d2h, hp.out));
     DS4X_CK(cudaMemcpyAsync(static_cast<uint8_t*>(out) + t0 * at, sl + L.out, tn * at, d2h, hp.out));
-    if (lse) DS4X_CK(cudaMemcpyAsync(lse + t0 * Hq, sl + L.lse, tn * lt, d2h, hp.out));
     DS4X_CK(cudaEventRecord(hp.out_done[b], hp.out));
   }
+  // every token's lse, once, after the last sub-chunk's work (the copy stream waited for it)
+  if (lse) DS4X_CK(cudaMemcpyAsync(lse, lse_dev, (size_t)T * Hq * sizeof(float), d2h, hp.out));
   // later work on the caller's stream (a synchronisation included) sees the outputs
-  DS4X_CK(cudaStreamWaitEvent(st, hp.out_done[(L.n - 1) & 1], 0));
-  if (L.n > 1) DS4X_CK(cudaStreamWaitEvent(st, hp.out_done[L.n & 1], 0));
+  DS4X_CK(cudaEventRecord(hp.fin, hp.out));
+  DS4X_CK(cudaStreamWaitEvent(st, hp.fin, 0));
 #undef DS4X_CK
   return scope.done(DS4X_OK);
 }

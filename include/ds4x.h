@@ -175,19 +175,21 @@ size_t ds4x_workspace_bytes(int32_t T, int32_t S, int32_t k_top);
 /* ---------------------------------------------------------------------------
  * ds4x_index_and_attend_host — ds4x_index_and_attend on HOST buffers: the inputs are copied
  *   to the device, the path runs, the outputs are copied back, and the copies overlap the
- *   work.  The tokens are cut into n_chunks sub-chunks (0: the library chooses); sub-chunk j
- *   is copied in on an internal stream while sub-chunk j-1 is computed on `stream` and
- *   sub-chunk j-2's outputs are copied out on a second internal stream, so that both copy
- *   directions and the kernels run at once.  The shared rows k and kv are copied once, first.
- *   Results are those of ds4x_index_and_attend on each sub-chunk (the same per token).
+ *   work.  The tokens are cut into n_chunks sub-chunks (0: the library chooses, about 256
+ *   tokens each); the sub-chunks' q and q_attn are copied in on an internal stream, computed on
+ *   `stream` and their indices and out copied back on a second internal stream, rotating over
+ *   three device staging slots, so that both copy directions and the kernels run at once.  The
+ *   shared rows k and kv and every token's w and position are copied once, first; every
+ *   token's lse is copied back once, last.  Results are those of ds4x_index_and_attend on each
+ *   sub-chunk (the same per token).
  *
  *   q, w, positions, q_attn, k, kv: host memory, layouts as in ds4x_index_and_attend.
  *   indices, out, lse (lse may be NULL): host memory, written by the call.
  *   Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for the copies to
  *   run asynchronously and overlap; pageable memory gives the same results, serialised.
  *   device_buffer: device memory the call owns for its duration, 16-byte aligned, at least
- *   ds4x_index_and_attend_host_bytes(...) bytes (staging for k, kv, two sub-chunks of
- *   per-token inputs and outputs, and the fused workspace).
+ *   ds4x_index_and_attend_host_bytes(...) bytes (staging for k, kv, every token's w, position
+ *   and lse, three sub-chunks of q, q_attn, indices and out, and the fused workspace).
  *   Ordering: the copies start after all work enqueued on `stream` before the call; on return
  *   everything is enqueued and `stream` waits for the last copy out, so a synchronisation of
  *   `stream` (or any work enqueued on it later) sees the outputs in host memory.  The host

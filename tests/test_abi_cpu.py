@@ -147,16 +147,17 @@ def test_host_path_arguments_rejected_without_launch(lib):
 
 def test_host_path_staging_sizes(lib):
     T, H, D, S, k_top, Hq, Dkv = 2048, 64, 128, 2048, 512, 64, 512
-    per_token = H * D * 2 + H * 2 + 4 + Hq * Dkv * 2 + k_top * 4 + Hq * Dkv * 2 + Hq * 4
-    shared = S * D * 2 + S * Dkv * 2
-    for n in (1, 3, 4, 8):
+    per_token_slot = H * D * 2 + Hq * Dkv * 2 + k_top * 4 + Hq * Dkv * 2       # q, q_attn, indices, out
+    shared = S * D * 2 + S * Dkv * 2 + T * (H * 2 + 4 + Hq * 4)                # k, kv; w, positions, lse of all
+    for n in (1, 3, 4, 8, 16):
         tc = -(-T // n)
+        slots = min(n, 3)
         b = ds4x.index_and_attend_host_bytes(T, H, D, S, k_top, Hq, Dkv, n)
-        # k and kv, the fused workspace of one sub-chunk, two slots of one sub-chunk's tokens
-        low = shared + ds4x.workspace_bytes(tc, S, k_top) + 2 * tc * per_token
-        assert low <= b <= low + 20 * 256
+        # the shared parts, the fused workspace of one sub-chunk, up to three slots of one sub-chunk
+        low = shared + ds4x.workspace_bytes(tc, S, k_top) + slots * tc * per_token_slot
+        assert low <= b <= low + 20 * 256, (n, b - low)
     assert ds4x.index_and_attend_host_bytes(T, H, D, S, k_top, Hq, Dkv, 0) == \
-        ds4x.index_and_attend_host_bytes(T, H, D, S, k_top, Hq, Dkv, 4)      # default: sub-chunks of ~512 tokens
+        ds4x.index_and_attend_host_bytes(T, H, D, S, k_top, Hq, Dkv, 8)      # default: sub-chunks of ~256 tokens
     assert ds4x.index_and_attend_host_bytes(0, H, D, S, k_top, Hq, Dkv, 0) == 0
     assert ds4x.index_and_attend_host_bytes(T, H, D, S, k_top, Hq, Dkv, -1) == 0
 
