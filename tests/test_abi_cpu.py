@@ -237,3 +237,15 @@ def test_compress_arguments_rejected_without_launch(lib):
     assert _compress(lib, bias=0) == ds4x.ERR_INVALID
     assert _compress(lib, T=6, fxo=0) == ds4x.ERR_INVALID        # 2 positions left over, no frontier out
     assert _compress(lib, T=0) == ds4x.OK                        # nothing to do, nothing launched
+
+
+def test_plain_c_caller(lib, tmp_path):
+    # the header compiles as C11 and a C program links the library and gets the host-side answers
+    exe = tmp_path / "c_abi_check"
+    pkg = os.path.dirname(ds4x.LIB_PATH)
+    subprocess.check_call(["gcc", "-std=c11", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                           os.path.join(ROOT, "tests", "c_abi_check.c"), "-o", str(exe), ds4x.LIB_PATH,
+                           "-Wl,-rpath," + pkg])
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert "c abi ok" in r.stdout
