@@ -50,6 +50,8 @@ struct ScoreArgs {
   int T, H, D, S, ratio;
   int skip_k_top;     // >0: tokens with n_vis <= skip_k_top need no scores (fused path)
   int write_masked;   // 1: write -inf on masked rows, including whole masked tiles
+  uint32_t* zero_words = nullptr;  // fused path: words the kernel zeroes once the previous kernel is done
+  int n_zero = 0;                  // (the top-k's barrier counters, so no memset sits between the launches)
 };
 int launch_score(const ScoreArgs& a, cudaStream_t stream);
 bool score_shape_supported(int H, int D);
@@ -63,6 +65,7 @@ struct TopkArgs {
   int32_t* counts;
   void* workspace;
   size_t workspace_bytes;
+  int counters_zeroed = 0;  // 1: the workspace's barrier counters were zeroed by the kernel before (fused path)
 };
 size_t topk_workspace_bytes(int T, int S, int k_top);
 int launch_topk(const TopkArgs& a, cudaStream_t stream);

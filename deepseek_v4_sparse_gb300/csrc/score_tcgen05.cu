@@ -93,6 +93,8 @@ struct Params {
   int skip_k_top;
   int write_masked;
   int* status;
+  uint32_t* zero_words;  // zeroed by CTA 0 once the previous kernel is done
+  int n_zero;
 };
 
 __device__ __forceinline__ int n_visible(const Params& p, int t) {
@@ -208,6 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();  // everything above touched only this CTA's own resources
   pdl_trigger();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < p.n_zero; i += blockDim.x) p.zero_words[i] = 0u;
 
   const long long beg = (long long)blockIdx.x * p.total_items / gridDim.x;
   const long long end = (long long)(blockIdx.x + 1) * p.total_items / gridDim.x;
@@ -522,6 +526,8 @@ int launch_impl(const ScoreArgs& a, cudaStream_t stream) {
   p.skip_k_top = a.skip_k_top;
   p.write_masked = a.write_masked;
   p.status = device_status_ptr();
+  p.zero_words = a.zero_words;
+  p.n_zero = a.zero_words ? a.n_zero : 0;
   const int sms = device_sm_count();
   const int grid = (int)(p.total_items < sms ? p.total_items : sms);
   const cudaError_t e = launch_pdl(score_kernel<H, D, TN>, dim3(grid), dim3(kThreads), (size_t)C::SMEM, stream, tq, tk, p);

@@ -1119,6 +1119,7 @@ __device__ bool token_barrier(uint32_t* counter, uint32_t target, int* status, i
 }
 
 __global__ void __launch_bounds__(kThreads) long_coop_kernel(const KParams p) {
+  pdl_wait();  // returns at once unless launched as a programmatic dependent of the scorer
   extern __shared__ uint8_t smem_raw[];
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
   uint32_t* sbm = reinterpret_cast<uint32_t*>(smem_raw + sizeof(Shared));  // whole-row fallback only
@@ -1296,6 +1297,9 @@ __global__ void __launch_bounds__(kThreads) long_coop_kernel(const KParams p) {
     }
   }
   if (!token_barrier(counter, 4u * P, p.status, 63)) return;
+  // the next kernel may start its prologue now: every slice has passed its last barrier, so early
+  // CTAs of that kernel can no longer keep one of these from being resident
+  pdl_trigger();
   if (__ldcg(&ctl->whole)) return;
 
   // phase 5: this slice's selected rows, in ascending order, after those of the slices before it
@@ -1389,19 +1393,25 @@ bool long_coop_fits(int T, int P, size_t smem) {
   return (long long)nb * device_sm_count() >= (long long)T * P;
 }
 
-cudaError_t launch_long_coop(KParams& p, cudaStream_t st, size_t smem) {
-  cudaError_t e = cudaMemsetAsync(p.gbar, 0, (size_t)p.T * sizeof(uint32_t), st);
+// counters_zeroed: the kernel before it on the stream zeroed the barrier counters (the fused path's
+// scorer does), so no memset separates the two launches and this one may start early (programmatic
+// dependent launch: its CTAs wait in pdl_wait until the scorer's results are visible).
+cudaError_t launch_long_coop(KParams& p, cudaStream_t st, size_t smem, bool counters_zeroed) {
+  cudaError_t e = cudaSuccess;
+  if (!counters_zeroed) e = cudaMemsetAsync(p.gbar, 0, (size_t)p.T * sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.nslice, p.T);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = counters_zeroed ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, long_coop_kernel, p);
   count_launch();
   return e;
@@ -1471,8 +1481,9 @@ int launch_topk(const TopkArgs& a, cudaStream_t stream) {
     if (a.workspace == nullptr || a.workspace_bytes < need) return DS4X_ERR_WORKSPACE;
     p.gbar = static_cast<uint32_t*>(a.workspace);
     p.long_ws = static_cast<uint8_t*>(a.workspace) + long_counters_bytes(a.T);
-    const cudaError_t e = long_coop_fits(a.T, p.nslice, msmem) ? launch_long_coop(p, stream, msmem)
-                                                             : launch_long(p, stream, msmem);
+    const cudaError_t e = long_coop_fits(a.T, p.nslice, msmem)
+                              ? launch_long_coop(p, stream, msmem, a.counters_zeroed != 0)
+                              : launch_long(p, stream, msmem);
     if (e != cudaSuccess) return DS4X_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? DS4X_OK : DS4X_ERR_CUDA;
@@ -1557,7 +1568,7 @@ extern "C" int ds4x_topk_static_scratch(const float* scores, int64_t ld_scores, 
     // nothing left in the array by an earlier call is ever read
     p.gbar = static_cast<uint32_t*>(scratch);
     p.long_ws = static_cast<uint8_t*>(scratch) + long_counters_bytes(T);
-    e = long_coop_fits(T, p.nslice, msmem) ? launch_long_coop(p, st, msmem) : launch_long(p, st, msmem);
+    e = long_coop_fits(T, p.nslice, msmem) ? launch_long_coop(p, st, msmem, false) : launch_long(p, st, msmem);
   }
   return e == cudaSuccess ? DS4X_OK : DS4X_ERR_CUDA;
 }
