@@ -455,7 +455,7 @@ def check_local_only_vs_textbook(o):
     qa = synth.to_bf16_bits(rng.standard_normal((T, Hq, Dkv)))
     ind = np.full((T, 4), -1, dtype=np.int32)
     scale = 0.3
-    out, lse = o.local_pooled_attn(qa, X[:2], X[lp0:lp0 + L], "bf16", ind, pos, 2, lp0, W, scale)
+    out, lse = o.local_pooled_attn(qa, X, X[lp0:lp0 + L], "bf16", ind, pos, 2, lp0, W, scale)
     Xf = _bits_val(X, "bf16")
     for t, p in enumerate(pos):
         rows = [a for a in range(max(0, p - W + 1, lp0), min(p, lp0 + L - 1) + 1)]

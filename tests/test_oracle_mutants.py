@@ -5,6 +5,8 @@ tie-break, a transposed operand, ...). They are compiled from a textual edit of
 oracle/ds4x_oracle.c into a temporary library; the oracle source itself is untouched.
 """
 import os
+import subprocess
+import sys
 
 import pytest
 
@@ -63,6 +65,21 @@ MUTANTS = {
 }
 
 
+# Each mutant's pins run in a child process: a planted slip may also read out of bounds, and a
+# child that dies by a signal has caught it just as a failing pin would, without taking pytest down.
+_RUNNER = """
+import sys
+sys.path[:0] = [{root!r}, {tests!r}]
+import oracle, oracle_pins
+o = oracle.Oracle({lib!r})
+for check in oracle_pins.ALL_CHECKS:
+    try:
+        check(o)
+    except (AssertionError, ValueError, IndexError):
+        print("FAILED", check.__name__, flush=True)
+"""
+
+
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_mutant_is_caught(name, tmp_path):
     old, new = MUTANTS[name]
@@ -71,11 +88,10 @@ def test_mutant_is_caught(name, tmp_path):
     mutated = tmp_path / "mutant.c"
     mutated.write_text(src.replace(old, new, 1))
     lib = oracle.build(force=True, src=str(mutated), out=str(tmp_path / "libmutant.so"))
-    o = oracle.Oracle(lib)
-    failed = []
-    for check in oracle_pins.ALL_CHECKS:
-        try:
-            check(o)
-        except (AssertionError, ValueError, IndexError):
-            failed.append(check.__name__)
-    assert failed, f"no pin catches the planted mistake {name}"
+    tests = os.path.dirname(os.path.abspath(__file__))
+    code = _RUNNER.format(root=os.path.dirname(tests), tests=tests, lib=lib)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
+    died = r.returncode < 0
+    failed = [l.split()[1] for l in r.stdout.splitlines() if l.startswith("FAILED")]
+    assert r.returncode == 0 or died, r.stderr[-2000:]
+    assert failed or died, f"no pin catches the planted mistake {name}"
