@@ -160,23 +160,51 @@ namespace {
 // large ones by sub-chunk, rotating over the slots.
 constexpr int kHostSlots = 3;
 struct HostLayout {
-  int n = 0, tc = 0, ns = 0;                         // sub-chunks, tokens per sub-chunk, slots in use
+  int n = 0, tc = 0, ns = 0;                         // sub-chunks, tokens a slot holds, slots in use
+  int T = 0, ramp = 0, mid = 0;                      // tokens of the short first and last sub-chunks; of the others
+  // sub-chunk j: its first token and its token count.  With a ramp, the first and last sub-chunks
+  // are short (the first copy in and the last copy out overlap nothing) and the others even.
+  void chunk(int j, size_t& t0, int& tn) const {
+    if (ramp == 0) {
+      t0 = (size_t)j * tc;
+      tn = (int)((size_t)T - t0 < (size_t)tc ? (size_t)T - t0 : (size_t)tc);
+    } else if (j == 0) {
+      t0 = 0;
+      tn = ramp;
+    } else if (j == n - 1) {
+      t0 = (size_t)T - ramp;
+      tn = ramp;
+    } else {
+      t0 = (size_t)ramp + (size_t)(j - 1) * mid;
+      const size_t end = (size_t)T - ramp, e = t0 + mid < end ? t0 + mid : end;
+      tn = (int)(e - t0);
+    }
+  }
   size_t k = 0, kv = 0, kvl = 0, w = 0, pos = 0, lse = 0, ws = 0, ws_bytes = 0, slot0 = 0, slot = 0, total = 0;
   size_t q = 0, qa = 0, idx = 0, out = 0;            // offsets within a slot
 };
 
-int default_host_chunks(int T) {  // sub-chunks of about 256 tokens
-  const int n = T / 256;
-  return n < 1 ? 1 : n > 16 ? 16 : n;
+int default_host_chunks(int T) {  // sub-chunks of about 512 tokens (plus the short first and last)
+  const int n = T / 512;
+  return n < 1 ? 1 : n > 8 ? 8 : n;
 }
 
 HostLayout host_layout(int T, int H, int D, int S, int k_top, int Hq, int Dkv, int n_chunks, int Lrows = 0,
                        int window = 0) {
   const bool win = window > 0 && Lrows > 0;
   HostLayout L;
+  L.T = T;
   L.n = n_chunks > 0 ? (n_chunks < T ? n_chunks : T) : default_host_chunks(T);
   L.tc = (T + L.n - 1) / L.n;
   L.n = (T + L.tc - 1) / L.tc;  // no empty sub-chunk
+  if (L.n >= 4 && L.tc >= 8) {
+    // a quarter-size first and last sub-chunk, the rest in even sub-chunks of at most tc tokens
+    L.ramp = L.tc / 4;
+    const int middle = T - 2 * L.ramp;
+    const int nm = (middle + L.tc - 1) / L.tc;
+    L.mid = (middle + nm - 1) / nm;
+    L.n = nm + 2;
+  }
   L.ns = L.n < kHostSlots ? L.n : kHostSlots;
   const size_t tc = (size_t)L.tc, e16 = 2;
   size_t o = 0;
@@ -439,8 +467,9 @@ int host_path(const void* q, const void* w, const void* k, const int32_t* positi
   float* lse_dev = reinterpret_cast<float*>(base + L.lse);
   for (int j = 0; j < L.n; ++j) {
     const int b = j % L.ns;
-    const size_t t0 = (size_t)j * L.tc;
-    const int tn = (int)((size_t)T - t0 < (size_t)L.tc ? (size_t)T - t0 : (size_t)L.tc);
+    size_t t0;
+    int tn;
+    L.chunk(j, t0, tn);
     uint8_t* sl = base + L.slot0 + b * L.slot;
     // inputs of sub-chunk j, once sub-chunk j - ns (same slot) has been computed
     if (j >= L.ns) DS4X_CK(cudaStreamWaitEvent(hp.in, hp.work_done[b], 0));

@@ -175,8 +175,9 @@ size_t ds4x_workspace_bytes(int32_t T, int32_t S, int32_t k_top);
 /* ---------------------------------------------------------------------------
  * ds4x_index_and_attend_host — ds4x_index_and_attend on HOST buffers: the inputs are copied
  *   to the device, the path runs, the outputs are copied back, and the copies overlap the
- *   work.  The tokens are cut into n_chunks sub-chunks (0: the library chooses, about 256
- *   tokens each); the sub-chunks' q and q_attn are copied in on an internal stream, computed on
+ *   work.  The tokens are cut into about n_chunks sub-chunks (0: the library chooses, about 512
+ *   tokens each; from four on, a quarter-size first and last sub-chunk are added, since the first
+ *   copy in and the last copy out overlap nothing); the sub-chunks' q and q_attn are copied in on an internal stream, computed on
  *   `stream` and their indices and out copied back on a second internal stream, rotating over
  *   three device staging slots, so that both copy directions and the kernels run at once.  The
  *   shared rows k and kv and every token's w and position are copied once, first; every

@@ -157,7 +157,7 @@ def test_host_path_staging_sizes(lib):
         low = shared + ds4x.workspace_bytes(tc, S, k_top) + slots * tc * per_token_slot
         assert low <= b <= low + 20 * 256, (n, b - low)
     assert ds4x.index_and_attend_host_bytes(T, H, D, S, k_top, Hq, Dkv, 0) == \
-        ds4x.index_and_attend_host_bytes(T, H, D, S, k_top, Hq, Dkv, 8)      # default: sub-chunks of ~256 tokens
+        ds4x.index_and_attend_host_bytes(T, H, D, S, k_top, Hq, Dkv, 4)      # default: sub-chunks of ~512 tokens
     assert ds4x.index_and_attend_host_bytes(0, H, D, S, k_top, Hq, Dkv, 0) == 0
     assert ds4x.index_and_attend_host_bytes(T, H, D, S, k_top, Hq, Dkv, -1) == 0
 
