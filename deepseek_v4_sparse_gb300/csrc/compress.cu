@@ -8,8 +8,9 @@
 // "compressor frontier" tensors kept with the compressed rows).  The pages give no formula: the
 // gated pooling above is this library's definition (equal gates give the block mean).
 //
-// Streaming and HBM-bound: a thread owns 8 channels (16-byte loads of x and g) of one block and one
-// slice of the block's positions.  Positions go in batches of four (eight 16-byte loads in flight,
+// Streaming and HBM-bound: a thread owns 8 channels (16-byte loads of x and g), or 4 (8-byte loads,
+// more threads) when the blocks alone would not fill the GPU, of one block and one slice of the
+// block's positions.  Positions go in batches of four (eight 16-byte loads in flight,
 // one running-max rescale per batch, weights by ex2.approx on log2-scaled gates); the slices of a
 // block are merged through shared memory.
 // Sequence position v is frontier row v (v < n_frontier) or new row v - n_frontier.  One extra CTA
@@ -39,18 +40,42 @@ struct CompressParams {
   uint16_t* fx_out;    // [rem, D] frontier rows out
   uint16_t* fg_out;
   int nf, T, D, ratio, n_out, rem;
-  int cg;     // 8-channel groups per CTA slab
-  int slabs;  // slabs per block (D / 8 / cg)
+  int cg;     // channel groups (of 4 or 8 channels) per CTA slab
+  int slabs;  // slabs per block (D / channels a group / cg)
   int ns;     // position slices per block
   int bpc;    // blocks per CTA
   int main_ctas;  // CTAs of blocks (one more copies the frontier)
 };
 
-template <bool kBf16>
-__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+// CPT channels a thread: their 16-bit values move as one vector (16 bytes for 8, 8 for 4)
+template <int CPT>
+struct Vec;
+template <>
+struct Vec<8> {
+  using T = uint4;
+  static constexpr int kWords = 4;
+};
+template <>
+struct Vec<4> {
+  using T = uint2;
+  static constexpr int kWords = 2;
+};
+
+template <int CPT>
+__device__ __forceinline__ void words_of(const typename Vec<CPT>::T& u, uint32_t (&w)[CPT / 2]) {
+  if constexpr (CPT == 8) {
+    w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+  } else {
+    w[0] = u.x; w[1] = u.y;
+  }
+}
+
+template <bool kBf16, int CPT>
+__device__ __forceinline__ void unpack(const typename Vec<CPT>::T& u, float (&f)[CPT]) {
+  uint32_t w[CPT / 2];
+  words_of<CPT>(u, w);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < CPT / 2; ++k) {
     if constexpr (kBf16) {
       const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
       f[2 * k] = __low2float(h);
@@ -74,16 +99,19 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   }
 }
 
-__device__ __forceinline__ const uint4* seq_row(const uint16_t* held, const uint16_t* fresh, int nf, int64_t v,
-                                                int D) {
-  return reinterpret_cast<const uint4*>(v < nf ? held + v * D : fresh + (v - nf) * D);
+__device__ __forceinline__ const uint16_t* seq_row(const uint16_t* held, const uint16_t* fresh, int nf, int64_t v,
+                                                   int D) {
+  return v < nf ? held + v * D : fresh + (v - nf) * D;
 }
 
-__device__ __forceinline__ uint4 ldg16(const uint4* p) {
+__device__ __forceinline__ uint4 ldg_vec(const uint4* p) {
   uint4 r;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint2 ldg_vec(const uint2* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
   return r;
 }
 
@@ -94,20 +122,24 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// z = (g + bias) log2(e) for the 8 channels of one position
-template <bool kBf16>
-__device__ __forceinline__ void gate8(const uint4& ug, const float* bias_row, float (&z)[8]) {
-  unpack8<kBf16>(ug, z);
-  const float4 b0 = __ldg(reinterpret_cast<const float4*>(bias_row));
-  const float4 b1 = __ldg(reinterpret_cast<const float4*>(bias_row) + 1);
-  const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+// z = (g + bias) log2(e) for the CPT channels of one position
+template <bool kBf16, int CPT>
+__device__ __forceinline__ void gate(const typename Vec<CPT>::T& ug, const float* bias_row, float (&z)[CPT]) {
+  unpack<kBf16, CPT>(ug, z);
 #pragma unroll
-  for (int k = 0; k < 8; ++k) z[k] = (z[k] + bb[k]) * 1.4426950408889634f;
+  for (int k4 = 0; k4 < CPT / 4; ++k4) {
+    const float4 b = __ldg(reinterpret_cast<const float4*>(bias_row) + k4);
+    z[4 * k4] = (z[4 * k4] + b.x) * 1.4426950408889634f;
+    z[4 * k4 + 1] = (z[4 * k4 + 1] + b.y) * 1.4426950408889634f;
+    z[4 * k4 + 2] = (z[4 * k4 + 2] + b.z) * 1.4426950408889634f;
+    z[4 * k4 + 3] = (z[4 * k4 + 3] + b.w) * 1.4426950408889634f;
+  }
 }
 
-template <bool kBf16>
-__global__ void __launch_bounds__(kThreads) compress_kernel(const CompressParams p) {
-  __shared__ float part[kThreads][24];  // a slice's (m, l, acc) of its 8 channels
+template <bool kBf16, int CPT>
+__global__ void __launch_bounds__(kThreads, CPT == 4 ? 3 : 1) compress_kernel(const CompressParams p) {
+  using V = typename Vec<CPT>::T;
+  __shared__ float part[kThreads][3 * CPT];  // a slice's (m, l, acc) of its CPT channels
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x;
@@ -117,8 +149,10 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressParams
     for (int idx = tid; idx < p.rem * per_row; idx += blockDim.x) {
       const int i = idx / per_row, c = idx - i * per_row;
       const int64_t v = (int64_t)p.n_out * p.ratio + i;
-      reinterpret_cast<uint4*>(p.fx_out + (int64_t)i * p.D)[c] = seq_row(p.fx, p.x, p.nf, v, p.D)[c];
-      reinterpret_cast<uint4*>(p.fg_out + (int64_t)i * p.D)[c] = seq_row(p.fg, p.g, p.nf, v, p.D)[c];
+      reinterpret_cast<uint4*>(p.fx_out + (int64_t)i * p.D)[c] =
+          reinterpret_cast<const uint4*>(seq_row(p.fx, p.x, p.nf, v, p.D))[c];
+      reinterpret_cast<uint4*>(p.fg_out + (int64_t)i * p.D)[c] =
+          reinterpret_cast<const uint4*>(seq_row(p.fg, p.g, p.nf, v, p.D))[c];
     }
     return;
   }
@@ -127,12 +161,12 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressParams
   const int b = tid / (p.cg * p.ns);
   const int slab = blockIdx.x % p.slabs;
   const int64_t j = (int64_t)(blockIdx.x / p.slabs) * p.bpc + b;
-  const int grp = slab * p.cg + c;  // 8-channel group within the row
+  const int grp = slab * p.cg + c;  // CPT-channel group within the row
   const bool active = b < p.bpc && j < p.n_out;
-  // running max (log2 units), sum and weighted sum of the 8 channels
-  float m[8], l[8], acc[8];
+  // running max (log2 units), sum and weighted sum of the CPT channels
+  float m[CPT], l[CPT], acc[CPT];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
+  for (int k = 0; k < CPT; ++k) {
     m[k] = -INFINITY;
     l[k] = 0.f;
     acc[k] = 0.f;
@@ -141,30 +175,30 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressParams
     const int i0 = (int)((int64_t)s * p.ratio / p.ns), i1 = (int)((int64_t)(s + 1) * p.ratio / p.ns);
     for (int i = i0; i < i1; i += kBatch) {
       const int nb = min(kBatch, i1 - i);
-      uint4 ux[kBatch], ug[kBatch];
+      V ux[kBatch], ug[kBatch];
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) {
         if (q < nb) {
           const int64_t v = j * p.ratio + i + q;
-          ux[q] = ldg16(seq_row(p.fx, p.x, p.nf, v, p.D) + grp);
-          ug[q] = ldg16(seq_row(p.fg, p.g, p.nf, v, p.D) + grp);
+          ux[q] = ldg_vec(reinterpret_cast<const V*>(seq_row(p.fx, p.x, p.nf, v, p.D)) + grp);
+          ug[q] = ldg_vec(reinterpret_cast<const V*>(seq_row(p.fg, p.g, p.nf, v, p.D)) + grp);
         }
       }
       // the batch's max raises the running max once; then its weights
-      float bm[8];
+      float bm[CPT];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) bm[k] = -INFINITY;
+      for (int k = 0; k < CPT; ++k) bm[k] = -INFINITY;
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) {
         if (q < nb) {
-          float z[8];
-          gate8<kBf16>(ug[q], p.bias + (int64_t)(i + q) * p.D + grp * 8, z);
+          float z[CPT];
+          gate<kBf16, CPT>(ug[q], p.bias + (int64_t)(i + q) * p.D + grp * CPT, z);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) bm[k] = fmaxf(bm[k], z[k]);
+          for (int k = 0; k < CPT; ++k) bm[k] = fmaxf(bm[k], z[k]);
         }
       }
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < CPT; ++k) {
         const float mn = fmaxf(m[k], bm[k]);
         const float sc = ex2_approx(m[k] - mn);  // 0 while m is still -inf
         l[k] *= sc;
@@ -174,11 +208,11 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressParams
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) {
         if (q < nb) {
-          float z[8], xv[8];
-          gate8<kBf16>(ug[q], p.bias + (int64_t)(i + q) * p.D + grp * 8, z);
-          unpack8<kBf16>(ux[q], xv);
+          float z[CPT], xv[CPT];
+          gate<kBf16, CPT>(ug[q], p.bias + (int64_t)(i + q) * p.D + grp * CPT, z);
+          unpack<kBf16, CPT>(ux[q], xv);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
+          for (int k = 0; k < CPT; ++k) {
             const float a = ex2_approx(z[k] - m[k]);
             l[k] += a;
             acc[k] = fmaf(a, xv[k], acc[k]);
@@ -193,23 +227,23 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressParams
     for (int half = p.ns / 2; half >= 1; half /= 2) {
       if (s >= half && s < 2 * half) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < CPT; ++k) {
           part[tid][k] = m[k];
-          part[tid][8 + k] = l[k];
-          part[tid][16 + k] = acc[k];
+          part[tid][CPT + k] = l[k];
+          part[tid][2 * CPT + k] = acc[k];
         }
       }
       __syncthreads();
       if (s < half) {
         const int o = tid + half * p.cg;  // slice s + half of the same (block, channel group)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < CPT; ++k) {
           const float mo = part[o][k];
           const float mn = fmaxf(m[k], mo);
           if (mn == -INFINITY) continue;
           const float sa = ex2_approx(m[k] - mn), sb = ex2_approx(mo - mn);
-          l[k] = l[k] * sa + part[o][8 + k] * sb;
-          acc[k] = acc[k] * sa + part[o][16 + k] * sb;
+          l[k] = l[k] * sa + part[o][CPT + k] * sb;
+          acc[k] = acc[k] * sa + part[o][2 * CPT + k] * sb;
           m[k] = mn;
         }
       }
@@ -218,18 +252,22 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressParams
     if (s != 0) return;
   }
   if (!active) return;
-  uint4 o;
-  o.x = pack2<kBf16>(acc[0] / l[0], acc[1] / l[1]);
-  o.y = pack2<kBf16>(acc[2] / l[2], acc[3] / l[3]);
-  o.z = pack2<kBf16>(acc[4] / l[4], acc[5] / l[5]);
-  o.w = pack2<kBf16>(acc[6] / l[6], acc[7] / l[7]);
-  reinterpret_cast<uint4*>(p.rows + j * p.D)[grp] = o;
+  uint32_t w[CPT / 2];
+#pragma unroll
+  for (int k = 0; k < CPT / 2; ++k) w[k] = pack2<kBf16>(acc[2 * k] / l[2 * k], acc[2 * k + 1] / l[2 * k + 1]);
+  V o;
+  if constexpr (CPT == 8) {
+    o = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {
+    o = make_uint2(w[0], w[1]);
+  }
+  reinterpret_cast<V*>(p.rows + j * p.D)[grp] = o;
 }
 
 }  // namespace
 
-// Launch shape: ns position slices, a slab of cg 8-channel groups (the largest divisor of D/8 with
-// cg * ns <= kThreads), bpc blocks per CTA filling kThreads.
+// Launch shape: channels a thread, ns position slices, a slab of cg channel groups (the largest
+// divisor of the row's groups with cg * ns <= kThreads), bpc blocks per CTA filling kThreads.
 int launch_compress(const CompressArgs& a, cudaStream_t stream) {
   CompressParams p;
   p.x = static_cast<const uint16_t*>(a.x);
@@ -248,11 +286,14 @@ int launch_compress(const CompressArgs& a, cudaStream_t stream) {
   p.n_out = (int)(n / a.ratio);
   p.rem = (int)(n % a.ratio);
   if (p.n_out == 0 && p.rem == 0) return DS4X_OK;
-  const int groups = a.D / 8;
+  // 8 channels a thread (16-byte loads) when the blocks alone give about four CTAs of work per SM,
+  // else 4 (more threads, fewer registers: three CTAs per SM) and position slices as needed
+  const int64_t want = 4ll * device_sm_count() * kThreads;
+  const int CPT = (int64_t)p.n_out * (a.D / 8) >= want ? 8 : 4;
+  const int groups = a.D / CPT;
   // position slices: as many as it takes for about four CTAs of work per SM (a power of two, at
   // most 32 and at most ratio / kBatch), so a ratio-128 block of a 2048-token chunk spreads out
   // while a long batch of blocks streams its positions in one thread
-  const int64_t want = 4ll * device_sm_count() * kThreads;
   int ns = 1;
   while (2 * ns <= a.ratio / kBatch && 2 * ns <= 32 && (int64_t)p.n_out * groups * ns < want) ns *= 2;
   int cg = groups < kThreads / ns ? groups : kThreads / ns;
@@ -263,8 +304,13 @@ int launch_compress(const CompressArgs& a, cudaStream_t stream) {
   p.bpc = kThreads / (cg * ns);
   p.main_ctas = (int)((p.n_out + p.bpc - 1) / p.bpc) * p.slabs;
   const int grid = p.main_ctas + (p.rem > 0 ? 1 : 0);
-  const cudaError_t e = a.bf16 ? launch_pdl(compress_kernel<true>, dim3(grid), dim3(kThreads), 0, stream, p)
-                               : launch_pdl(compress_kernel<false>, dim3(grid), dim3(kThreads), 0, stream, p);
+  cudaError_t e;
+  if (CPT == 8)
+    e = a.bf16 ? launch_pdl(compress_kernel<true, 8>, dim3(grid), dim3(kThreads), 0, stream, p)
+               : launch_pdl(compress_kernel<false, 8>, dim3(grid), dim3(kThreads), 0, stream, p);
+  else
+    e = a.bf16 ? launch_pdl(compress_kernel<true, 4>, dim3(grid), dim3(kThreads), 0, stream, p)
+               : launch_pdl(compress_kernel<false, 4>, dim3(grid), dim3(kThreads), 0, stream, p);
   if (e != cudaSuccess) return DS4X_ERR_CUDA;
   count_launch();
   return DS4X_OK;

@@ -95,3 +95,15 @@ def test_compress_split_calls_equal_one_bit_for_bit(ratio):
         parts.append(r)
     assert np.array_equal(np.concatenate(parts), whole)
     assert np.array_equal(fx, wfx) and np.array_equal(fg, wfg)
+
+
+def test_compress_streaming_batch_full_size():
+    # the benchmark's bandwidth case: a 64k-token batch of kv rows at ratio 4 with a 3-position frontier
+    D, ratio, T, f = 512, 4, 65536, 3
+    x, g, fx, fg, bias = synth.compress_inputs(0, "bench_kv_64k_r4", T, D, ratio, "bf16", f)
+    rows, fxo, fgo = _gpu(x, g, fx, fg, bias, ratio, "bf16")
+    rrows, rfx, rfg = oracle.compress(x, g, bias, "bf16", ratio, fx, fg)
+    assert rows.shape == rrows.shape == ((T + f) // ratio, D)
+    check_rows(rows, rrows, "bf16")
+    assert np.array_equal(fxo, rfx) and np.array_equal(fgo, rfg)
+

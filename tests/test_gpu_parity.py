@@ -272,7 +272,7 @@ def test_long_row_topk_exact(case):
 
 
 # --------------------------------------- full-size workloads in the benchmark's launch shape
-@pytest.mark.parametrize("name", ["prefill_8k", "prefill_64k"])
+@pytest.mark.parametrize("name", ["prefill_8k", "prefill_32k", "prefill_64k"])
 def test_full_size_sampled(name):
     wl = synth.WORKLOADS[name]
     inp = synth.make_inputs(wl, seed=0)
@@ -317,3 +317,23 @@ def test_pooled_ratio128_all_rows():
     assert all(np.array_equal(gidx[t, :nv[t]], np.arange(nv[t])) for t in range(T))
     ref_out, ref_lse = oracle.sparse_attn(inp.q_attn, inp.kv, wl.kv_dtype, gidx, wl.S, wl.scale)
     check_attn(host16(fout), ref_out, wl.kv_dtype, flse.cpu().numpy(), ref_lse)
+
+
+def test_pooled_ratio128_full_chunk_sampled():
+    # the benchmark's ratio-128 workload at its full size: every token takes the shortcut; sampled
+    # tokens' attention against the oracle, every token's indices against the closed form
+    wl = synth.WORKLOADS["pooled_64k_r128"]
+    inp = synth.make_inputs(wl, seed=0)
+    d = to_device(inp)
+    fidx, fout, flse = ds4x.index_and_attend(d["q"], d["w"], d["k"], d["positions"], d["q_attn"], d["kv"],
+                                             wl.ratio, wl.k_top, S=wl.S, scale=wl.scale)
+    torch.cuda.synchronize()
+    assert ds4x.device_status() == ds4x.OK
+    gidx = fidx.cpu().numpy()
+    nv = np.minimum(wl.S, (inp.positions.astype(np.int64) + 1) // wl.ratio)
+    want = np.where(np.arange(wl.k_top)[None, :] < nv[:, None], np.arange(wl.k_top)[None, :], -1)
+    assert np.array_equal(gidx, want)
+    sample = np.array([0, 1, 700, 1400, wl.T - 1])
+    ref_out, ref_lse = oracle.sparse_attn(inp.q_attn[sample], inp.kv, wl.kv_dtype, gidx[sample], wl.S, wl.scale)
+    check_attn(host16(fout)[sample], ref_out, wl.kv_dtype, flse.cpu().numpy()[sample], ref_lse)
+
