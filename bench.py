@@ -271,7 +271,8 @@ def run_reference(args, wl):
 
 
 # ---------------------------------------------------------------------------- decode loop
-def measure_decode(ds4x, torch, dev, stream, seed: int, reps: int = 3, n_steps: int = 256, warm: int = 1):
+def measure_decode(ds4x, torch, dev, stream, seed: int, reps: int = 3, n_steps: int = 256, warm: int = 1,
+                   window: int = 0):
     """The 1M-context decode: n_steps single-token steps from position 1048575 over 262144
     resident rows, a row appended every 4 positions (63 over 256 steps), each step
     score -> top-512 -> sparse MQA.  One timed unit is a whole ds4x_decode call (appends
@@ -293,12 +294,26 @@ def measure_decode(ds4x, torch, dev, stream, seed: int, reps: int = 3, n_steps: 
     idx = torch.empty((n_steps, wl.k_top), dtype=torch.int32, device=dev)
     out = torch.empty_like(qa)
     lse = torch.empty((n_steps, wl.Hq), dtype=torch.float32, device=dev)
-    ws = torch.empty((ds4x.decode_workspace_bytes(cap, wl.k_top),), dtype=torch.uint8, device=dev)
+    ws = torch.empty((ds4x.decode_local_workspace_bytes(cap, wl.k_top, window),), dtype=torch.uint8, device=dev)
     flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+    if window > 0:
+        # raw rows of every position up to the last step: the window's history and the steps' own
+        raw_cap = wl.pos0 + n_steps
+        kv_raw = torch.zeros((raw_cap, wl.Dkv), dtype=kvt, device=dev)
+        kv_raw[wl.pos0 - window:wl.pos0] = dev16(synth.local_rows(seed, "bench_decode_raw", window, wl.Dkv, "normal",
+                                                                  wl.kv_dtype), kvt)
+        kv_raw_new = dev16(synth.local_rows(seed, "bench_decode_raw_new", n_steps, wl.Dkv, "normal", wl.kv_dtype), kvt)
+
+    def launch(st):
+        if window > 0:
+            return ds4x.decode_local(q, w, qa, k, kv, S0, wl.pos0, wl.ratio, kv_raw, kv_raw_new, window, k_new=k_new,
+                                     kv_new=kv_new, k_top=wl.k_top, scale=wl.scale, positions=pos, indices=idx,
+                                     out=out, lse=lse, workspace=ws, stream=st)
+        return ds4x.decode(q, w, qa, k, kv, S0, wl.pos0, wl.ratio, k_new=k_new, kv_new=kv_new, k_top=wl.k_top,
+                           scale=wl.scale, positions=pos, indices=idx, out=out, lse=lse, workspace=ws, stream=st)
 
     def call():
-        r = ds4x.decode(q, w, qa, k, kv, S0, wl.pos0, wl.ratio, k_new=k_new, kv_new=kv_new, k_top=wl.k_top,
-                        scale=wl.scale, positions=pos, indices=idx, out=out, lse=lse, workspace=ws, stream=stream)
+        r = launch(stream)
         return r[4], ds4x.last_launch_count()
 
     for _ in range(max(1, warm)):
@@ -323,9 +338,7 @@ def measure_decode(ds4x, torch, dev, stream, seed: int, reps: int = 3, n_steps: 
         side.wait_stream(stream)
         with torch.cuda.stream(side):
             with torch.cuda.graph(g, stream=side):
-                ds4x.decode(q, w, qa, k, kv, S0, wl.pos0, wl.ratio, k_new=k_new, kv_new=kv_new, k_top=wl.k_top,
-                            scale=wl.scale, positions=pos, indices=idx, out=out, lse=lse, workspace=ws,
-                            stream=side)
+                launch(side)
         stream.wait_stream(side)
         gt = []
         for _ in range(reps):
@@ -341,6 +354,16 @@ def measure_decode(ds4x, torch, dev, stream, seed: int, reps: int = 3, n_steps: 
     except RuntimeError as e:  # capture refused: report the host-issued number only
         graph_ms = None
         print(f"decode graph capture unavailable: {e}", file=sys.stderr)
+    if window > 0:
+        return {
+            "workload": f"decode_1m with a {window}-position raw window: {n_steps} steps of 1 query token at positions "
+                        f"{wl.pos0}..{wl.pos0 + n_steps - 1}, each attending to its top-{wl.k_top} pooled rows and "
+                        f"the raw rows of its last {window} positions (ds4x_decode_local)",
+            "value": n_steps / (ms / 1e3), "unit": "decode tokens/s", "us_per_step": 1e3 * ms / n_steps,
+            "graph_value": None if graph_ms is None else n_steps / (graph_ms / 1e3),
+            "graph_us_per_step": None if graph_ms is None else 1e3 * graph_ms / n_steps,
+            "steps": n_steps, "gpu_launches_per_call": int(launches),
+        }
     # per-kernel split of the last step (T = 1 over S_final rows), each stage timed alone
     S = s_final
     sc = torch.empty((1, S), dtype=torch.float32, device=dev)
@@ -640,9 +663,10 @@ def main():
         "attn_gather_gbs": alg["attn_gather_bytes"] / (st_mean[2] / 1e3) / 1e9,
     }
 
-    dec = None
+    dec = dec_local = None
     if rank == 0 and not args.no_decode and wl.name != "decode_1m":
         dec = measure_decode(ds4x, torch, dev, stream, args.seed)
+        dec_local = measure_decode(ds4x, torch, dev, stream, args.seed, window=128)
 
     comp = None
     if rank == 0 and not args.no_compress:
@@ -666,7 +690,7 @@ def main():
             "roofline": roof, "stage_ms": stages, "stage_rates": others,
             "staged_ms_per_step": float(stage_ms.sum(axis=1).mean()),
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
-            "clocks": sampler.summary(), "decode": dec, "compress": comp,
+            "clocks": sampler.summary(), "decode": dec, "decode_local": dec_local, "compress": comp,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -34,6 +34,7 @@ EXPORTS = (
     "ds4x_index_and_attend_host", "ds4x_index_and_attend_host_bytes",
     "ds4x_local_pooled_attn", "ds4x_index_and_attend_local", "ds4x_workspace_bytes_local",
     "ds4x_index_and_attend_local_host", "ds4x_index_and_attend_local_host_bytes", "ds4x_compress",
+    "ds4x_decode_local", "ds4x_decode_local_workspace_bytes",
 )
 
 _lock = threading.Lock()
@@ -83,6 +84,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.ds4x_compress.argtypes = [P, P, P, ctypes.c_int, i32, i32, i32, P, P, i32, P, P, P, P]
         lib.ds4x_decode.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, P, i32, i32, i32, i32, i32, i32, i32,
                                     i32, i32, f32, P, P, P, P, P, sz, ctypes.POINTER(i32), P]
+        lib.ds4x_decode_local.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, P, i32, i32, i32, i32, i32, i32,
+                                          i32, i32, i32, f32, P, i32, P, i32, P, P, P, P, P, sz, ctypes.POINTER(i32), P]
+        lib.ds4x_decode_local_workspace_bytes.argtypes = [i32, i32, i32]
+        lib.ds4x_decode_local_workspace_bytes.restype = sz
         lib.ds4x_decode_workspace_bytes.argtypes = [i32, i32]
         lib.ds4x_decode_workspace_bytes.restype = sz
         lib.ds4x_status_string.argtypes = [ctypes.c_int]
@@ -92,7 +97,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.ds4x_selftest_bounded_wait.argtypes = [i64, P]
         for f in ("ds4x_indexer_score", "ds4x_topk", "ds4x_sparse_attn", "ds4x_index_and_attend", "ds4x_decode",
                   "ds4x_index_and_attend_host", "ds4x_local_pooled_attn", "ds4x_index_and_attend_local",
-                  "ds4x_index_and_attend_local_host", "ds4x_compress",
+                  "ds4x_index_and_attend_local_host", "ds4x_compress", "ds4x_decode_local",
                   "ds4x_last_launch_count", "ds4x_device_status", "ds4x_selftest_bounded_wait"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
@@ -454,6 +459,49 @@ def decode(q, w, q_attn, k, kv, S0: int, pos0: int, ratio: int, k_new=None, kv_n
                             _ptr(indices), _ptr(out), _ptr(lse), _ptr(workspace),
                             workspace.numel() * workspace.element_size(), ctypes.byref(s_final), _stream(stream))
     _check("ds4x_decode", rc)
+    return indices, out, lse, positions, int(s_final.value)
+
+
+def decode_local_workspace_bytes(capacity: int, k_top: int = 512, window: int = 128) -> int:
+    return int(load().ds4x_decode_local_workspace_bytes(capacity, k_top, window))
+
+
+def decode_local(q, w, q_attn, k, kv, S0: int, pos0: int, ratio: int, kv_raw, kv_raw_new, window: int,
+                 k_new=None, kv_new=None, k_top: int = 512, scale: float | None = None, positions=None,
+                 indices=None, out=None, lse=None, workspace=None, want_lse: bool = True, stream=None):
+    """decode() with local-plus-pooled attention: kv_raw [raw_capacity, 512] holds the raw row of
+    each position (rows below pos0 are the window's history), kv_raw_new [n_steps, 512] the steps'
+    own raw rows, written at rows pos0.. by the call. Returns (indices, out, lse, positions, S_final)."""
+    torch = _torch()
+    dt = _kv_dtype(kv)
+    n_steps, H, D = q.shape
+    _, Hq, Dkv = q_attn.shape
+    capacity = k.shape[0]
+    if kv.shape[0] != capacity:
+        raise ValueError("k and kv must have the same capacity")
+    if kv_raw.dtype != kv.dtype or kv_raw_new.dtype != kv.dtype:
+        raise ValueError("kv_raw and kv_raw_new must have kv's dtype")
+    n_new = 0 if k_new is None else k_new.shape[0]
+    scale = 1.0 / math.sqrt(Dkv) if scale is None else scale
+    dev = q.device
+    if positions is None:
+        positions = torch.empty((n_steps,), dtype=torch.int32, device=dev)
+    if indices is None:
+        indices = torch.empty((n_steps, k_top), dtype=torch.int32, device=dev)
+    if out is None:
+        out = torch.empty_like(q_attn)
+    if lse is None and want_lse:
+        lse = torch.empty((n_steps, Hq), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty((max(decode_local_workspace_bytes(capacity, k_top, window), 16),), dtype=torch.uint8,
+                                device=dev)
+    s_final = ctypes.c_int32(0)
+    rc = load().ds4x_decode_local(_ptr(q), _ptr(w), _ptr(q_attn), _ptr(k), _ptr(kv), dt, capacity, S0, _ptr(k_new),
+                                  _ptr(kv_new), n_new, pos0, n_steps, H, D, ratio, k_top, Hq, Dkv, scale, _ptr(kv_raw),
+                                  kv_raw.shape[0], _ptr(kv_raw_new), window, _ptr(positions), _ptr(indices),
+                                  _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  ctypes.byref(s_final), _stream(stream))
+    _check("ds4x_decode_local", rc)
     return indices, out, lse, positions, int(s_final.value)
 
 

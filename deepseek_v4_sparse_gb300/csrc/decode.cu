@@ -58,33 +58,43 @@ size_t ds4x_decode_workspace_bytes(int32_t capacity, int32_t k_top) {
   return fused_workspace_bytes(1, capacity, k_top);
 }
 
-int ds4x_decode(const void* q, const void* w, const void* q_attn, void* k, void* kv, ds4x_dtype kv_dtype,
+}  // extern "C"
+
+namespace {
+// The decode loop, with or without the raw window (raw: kv_raw rows are positions 0, 1, ...; the
+// n_steps rows of kv_raw_new land at rows pos0 .. pos0 + n_steps - 1 before the first step, and
+// step i attends to the raw rows of positions p - window + 1 .. p, p = pos0 + i).
+int decode_impl(const void* q, const void* w, const void* q_attn, void* k, void* kv, ds4x_dtype kv_dtype,
                 int32_t capacity, int32_t S0, const void* k_new, const void* kv_new, int32_t n_new, int32_t pos0,
                 int32_t n_steps, int32_t H, int32_t D, int32_t ratio, int32_t k_top, int32_t Hq, int32_t Dkv,
                 float scale, int32_t* positions, int32_t* indices, void* out, float* lse, void* workspace,
-                size_t workspace_bytes, int32_t* S_final, void* stream) {
+                size_t workspace_bytes, int32_t* S_final, void* stream, void* kv_raw, int32_t raw_capacity,
+                const void* kv_raw_new, int32_t window) {
   call_begin();
   if (n_steps < 0 || capacity < 1 || S0 < 0 || S0 > capacity || n_new < 0 || H <= 0 || D <= 0 || Hq <= 0 ||
-      Dkv <= 0 || ratio < 1 || k_top < 1 || pos0 < 0)
+      Dkv <= 0 || ratio < 1 || k_top < 1 || pos0 < 0 || window < 0)
     return DS4X_ERR_INVALID;
   if ((int64_t)pos0 + n_steps > INT32_MAX) return DS4X_ERR_INVALID;
   if (kv_dtype != DS4X_F16 && kv_dtype != DS4X_BF16) return DS4X_ERR_INVALID;
-  if (k_top > DS4X_MAX_KTOP) return DS4X_ERR_UNSUPPORTED;
+  if (k_top > DS4X_MAX_KTOP || window > DS4X_MAX_WINDOW) return DS4X_ERR_UNSUPPORTED;
   if (!score_shape_supported(H, D) || !attn_shape_supported(Hq, Dkv)) return DS4X_ERR_UNSUPPORTED;
+  const bool win = window > 0;
+  if (win && (int64_t)pos0 + n_steps > raw_capacity) return DS4X_ERR_INVALID;  // every step's raw row has a place
   if (n_steps == 0) {
     if (S_final) *S_final = S0;
     return call_end(DS4X_OK);
   }
   if (!q || !w || !q_attn || !k || !kv || !positions || !indices || !out || !workspace ||
-      (n_new > 0 && (!k_new || !kv_new)))
+      (n_new > 0 && (!k_new || !kv_new)) || (win && (!kv_raw || !kv_raw_new)))
     return DS4X_ERR_INVALID;
   if (!aligned16(q) || !aligned16(w) || !aligned16(q_attn) || !aligned16(k) || !aligned16(kv) ||
       !aligned16(positions) || !aligned16(indices) || !aligned16(out) || (lse && !aligned16(lse)) ||
-      !aligned16(workspace) || (k_new && !aligned16(k_new)) || (kv_new && !aligned16(kv_new)))
+      !aligned16(workspace) || (k_new && !aligned16(k_new)) || (kv_new && !aligned16(kv_new)) ||
+      (win && (!aligned16(kv_raw) || !aligned16(kv_raw_new))))
     return DS4X_ERR_INVALID;
   // per-step tensors must stay 16-byte aligned: w rows are H fp16, index rows k_top int32
   if ((H * 2) % 16 != 0 || (k_top * 4) % 16 != 0) return DS4X_ERR_UNSUPPORTED;
-  if (workspace_bytes < ds4x_decode_workspace_bytes(capacity, k_top)) return DS4X_ERR_WORKSPACE;
+  if (workspace_bytes < fused_workspace_bytes(1, capacity, k_top, window)) return DS4X_ERR_WORKSPACE;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_pdl(fill_positions_kernel, dim3((n_steps + 255) / 256), dim3(256), 0, st, positions, pos0, n_steps) !=
@@ -92,6 +102,21 @@ int ds4x_decode(const void* q, const void* w, const void* q_attn, void* k, void*
     return DS4X_ERR_CUDA;
   count_launch();
   const int k16 = D * 2 / 16, kv16 = Dkv * 2 / 16;
+  LocalWindow lw;
+  if (win) {
+    // every step's raw row into place at once: a step's window never reaches past its own position
+    const int total = n_steps * kv16;
+    const int blocks = (total + 255) / 256 < 256 ? (total + 255) / 256 : 256;
+    if (launch_pdl(append_rows_kernel, dim3(blocks), dim3(256), 0, st, static_cast<uint4*>(kv_raw) + (int64_t)pos0 * kv16,
+                   static_cast<const uint4*>(kv_raw_new), kv16, static_cast<uint4*>(nullptr),
+                   static_cast<const uint4*>(nullptr), 0, n_steps) != cudaSuccess)
+      return DS4X_ERR_CUDA;
+    count_launch();
+    lw.kv_local = kv_raw;
+    lw.local_pos0 = 0;
+    lw.L = pos0 + n_steps;
+    lw.window = window;
+  }
   const int bf16 = kv_dtype == DS4X_BF16 ? 1 : 0;
   int S = S0, appended = 0;
   for (int i = 0; i < n_steps; ++i) {
@@ -115,11 +140,40 @@ int ds4x_decode(const void* q, const void* w, const void* q_attn, void* k, void*
         static_cast<const uint16_t*>(q) + (int64_t)i * H * D, static_cast<const uint16_t*>(w) + (int64_t)i * H, k,
         positions + i, static_cast<const uint16_t*>(q_attn) + (int64_t)i * Hq * Dkv, kv, bf16, 1, H, D, S, ratio,
         k_top, scale, indices + (int64_t)i * k_top, static_cast<uint16_t*>(out) + (int64_t)i * Hq * Dkv,
-        lse ? lse + (int64_t)i * Hq : nullptr, workspace, workspace_bytes, st);
+        lse ? lse + (int64_t)i * Hq : nullptr, workspace, workspace_bytes, st, lw);
     if (rc != DS4X_OK) return rc;
   }
   if (S_final) *S_final = S;
   return call_end(DS4X_OK);
+}
+}  // namespace
+
+extern "C" {
+
+int ds4x_decode(const void* q, const void* w, const void* q_attn, void* k, void* kv, ds4x_dtype kv_dtype,
+                int32_t capacity, int32_t S0, const void* k_new, const void* kv_new, int32_t n_new, int32_t pos0,
+                int32_t n_steps, int32_t H, int32_t D, int32_t ratio, int32_t k_top, int32_t Hq, int32_t Dkv,
+                float scale, int32_t* positions, int32_t* indices, void* out, float* lse, void* workspace,
+                size_t workspace_bytes, int32_t* S_final, void* stream) {
+  return decode_impl(q, w, q_attn, k, kv, kv_dtype, capacity, S0, k_new, kv_new, n_new, pos0, n_steps, H, D, ratio,
+                     k_top, Hq, Dkv, scale, positions, indices, out, lse, workspace, workspace_bytes, S_final, stream,
+                     nullptr, 0, nullptr, 0);
+}
+
+size_t ds4x_decode_local_workspace_bytes(int32_t capacity, int32_t k_top, int32_t window) {
+  if (capacity <= 0 || k_top <= 0 || window < 0 || window > DS4X_MAX_WINDOW) return 0;
+  return fused_workspace_bytes(1, capacity, k_top, window);
+}
+
+int ds4x_decode_local(const void* q, const void* w, const void* q_attn, void* k, void* kv, ds4x_dtype kv_dtype,
+                      int32_t capacity, int32_t S0, const void* k_new, const void* kv_new, int32_t n_new,
+                      int32_t pos0, int32_t n_steps, int32_t H, int32_t D, int32_t ratio, int32_t k_top, int32_t Hq,
+                      int32_t Dkv, float scale, void* kv_raw, int32_t raw_capacity, const void* kv_raw_new,
+                      int32_t window, int32_t* positions, int32_t* indices, void* out, float* lse, void* workspace,
+                      size_t workspace_bytes, int32_t* S_final, void* stream) {
+  return decode_impl(q, w, q_attn, k, kv, kv_dtype, capacity, S0, k_new, kv_new, n_new, pos0, n_steps, H, D, ratio,
+                     k_top, Hq, Dkv, scale, positions, indices, out, lse, workspace, workspace_bytes, S_final, stream,
+                     kv_raw, raw_capacity, kv_raw_new, window);
 }
 
 }  // extern "C"

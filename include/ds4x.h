@@ -320,6 +320,28 @@ int ds4x_decode(const void* q, const void* w, const void* q_attn, void* k, void*
                 float* lse, void* workspace, size_t workspace_bytes, int32_t* S_final, void* stream);
 size_t ds4x_decode_workspace_bytes(int32_t capacity, int32_t k_top);
 
+/* ---------------------------------------------------------------------------
+ * ds4x_decode_local — ds4x_decode with local-plus-pooled attention: each step also attends to the
+ * raw rows of its last `window` positions (see ds4x_local_pooled_attn), the decode form of [A]'s
+ * local-plus-pooled kernel.
+ *
+ *   kv_raw [raw_capacity, Dkv] of kv_dtype: row a holds the raw row of position a; rows below
+ *   pos0 (the window's history) are the caller's, rows pos0 .. pos0 + n_steps - 1 are written
+ *   by the call from kv_raw_new [n_steps, Dkv] (step i's own raw row) before the first step.
+ *   raw_capacity >= pos0 + n_steps.  Step i (position p) attends to its selected pooled rows and
+ *   to kv_raw rows max(0, p - window + 1) .. p in one softmax; window = 0 is ds4x_decode.
+ *   workspace: at least ds4x_decode_local_workspace_bytes(capacity, k_top, window) bytes.
+ *   Everything else as ds4x_decode.
+ * ------------------------------------------------------------------------- */
+int ds4x_decode_local(const void* q, const void* w, const void* q_attn, void* k, void* kv,
+                      ds4x_dtype kv_dtype, int32_t capacity, int32_t S0, const void* k_new,
+                      const void* kv_new, int32_t n_new, int32_t pos0, int32_t n_steps, int32_t H,
+                      int32_t D, int32_t ratio, int32_t k_top, int32_t Hq, int32_t Dkv, float scale,
+                      void* kv_raw, int32_t raw_capacity, const void* kv_raw_new, int32_t window,
+                      int32_t* positions, int32_t* indices, void* out, float* lse, void* workspace,
+                      size_t workspace_bytes, int32_t* S_final, void* stream);
+size_t ds4x_decode_local_workspace_bytes(int32_t capacity, int32_t k_top, int32_t window);
+
 /* Human-readable name of a ds4x_status value (static storage, never NULL). */
 const char* ds4x_status_string(int status);
 

@@ -51,6 +51,8 @@ def _bind(lib):
     lib.ds4x_ref_compress.argtypes = [P, P, P, ctypes.c_int, i32, i32, i32, P, P, i32, P, P, P]
     lib.ds4x_ref_decode.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, P, i32, i32, i32, i32, i32, i32,
                                     i32, i32, i32, f32, P, P, P, P, P]
+    lib.ds4x_ref_decode_local.argtypes = [P, P, P, P, P, ctypes.c_int, i32, i32, P, P, i32, i32, i32, i32, i32,
+                                          i32, i32, i32, i32, f32, P, i32, P, i32, P, P, P, P, P]
     lib.ds4x_ref_n_visible.argtypes = [i64, i64, i64]
     lib.ds4x_ref_n_visible.restype = i64
     lib.ds4x_ref_decode16.argtypes = [ctypes.c_uint16, ctypes.c_int]
@@ -59,7 +61,7 @@ def _bind(lib):
     lib.ds4x_ref_encode16.restype = ctypes.c_uint16
     for f in ("ds4x_ref_indexer_score", "ds4x_ref_topk_ex", "ds4x_ref_sparse_attn",
               "ds4x_ref_index_and_attend", "ds4x_ref_decode", "ds4x_ref_local_pooled_attn",
-              "ds4x_ref_index_and_attend_local", "ds4x_ref_compress"):
+              "ds4x_ref_index_and_attend_local", "ds4x_ref_compress", "ds4x_ref_decode_local"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -220,6 +222,32 @@ class Oracle:
         assert rc == 0, rc
         return idx, out, lse, pos, s_steps, k, kv
 
+    def decode_local(self, q, w, q_attn, k, kv, kv_dtype, S0, pos0, ratio, k_new, kv_new, k_top, scale, kv_raw,
+                     kv_raw_new, window):
+        """decode() with the raw window, on copies of k / kv / kv_raw. Returns (indices, out bits, lse,
+        positions, S per step, k after, kv after, kv_raw after)."""
+        q, w, q_attn = _c(q, np.uint16), _c(w, np.uint16), _c(q_attn, np.uint16)
+        k, kv = np.array(k, dtype=np.uint16, copy=True), np.array(kv, dtype=np.uint16, copy=True)
+        kv_raw = np.array(kv_raw, dtype=np.uint16, copy=True)
+        kv_raw_new = _c(kv_raw_new, np.uint16)
+        n_new = 0 if k_new is None else k_new.shape[0]
+        k_new = None if k_new is None else _c(k_new, np.uint16)
+        kv_new = None if kv_new is None else _c(kv_new, np.uint16)
+        n_steps, H, D = q.shape
+        _, Hq, Dkv = q_attn.shape
+        idx = np.empty((n_steps, k_top), dtype=np.int32)
+        out = np.empty((n_steps, Hq, Dkv), dtype=np.uint16)
+        lse = np.empty((n_steps, Hq), dtype=np.float32)
+        pos = np.empty((n_steps,), dtype=np.int32)
+        s_steps = np.empty((n_steps,), dtype=np.int32)
+        rc = self.lib.ds4x_ref_decode_local(_ptr(q), _ptr(w), _ptr(q_attn), _ptr(k), _ptr(kv), DTYPES[kv_dtype],
+                                            k.shape[0], S0, _ptr(k_new), _ptr(kv_new), n_new, pos0, n_steps, H, D,
+                                            ratio, k_top, Hq, Dkv, scale, _ptr(kv_raw), kv_raw.shape[0],
+                                            _ptr(kv_raw_new), window, _ptr(pos), _ptr(idx), _ptr(out), _ptr(lse),
+                                            _ptr(s_steps))
+        assert rc == 0, rc
+        return idx, out, lse, pos, s_steps, k, kv, kv_raw
+
 
 def default() -> Oracle:
     """The oracle built from ds4x_oracle.c (compiled on first use)."""
@@ -272,3 +300,7 @@ def index_and_attend_local(*a, **kw):
 
 def compress(*a, **kw):
     return default().compress(*a, **kw)
+
+
+def decode_local(*a, **kw):
+    return default().decode_local(*a, **kw)

@@ -514,3 +514,42 @@ int ds4x_ref_decode(const uint16_t* q, const uint16_t* w, const uint16_t* q_attn
   }
   return 0;
 }
+
+/* The decode loop with local-plus-pooled attention: as ds4x_ref_decode, and before the first step
+ * the n_steps raw rows kv_raw_new land at rows pos0 .. pos0 + n_steps - 1 of kv_raw (row a = the
+ * raw row of position a; rows below pos0 are the caller's history); step i (position p) is
+ * ds4x_ref_index_and_attend_local over kv_raw with the window.  kv_raw holds raw_capacity rows
+ * (>= pos0 + n_steps) and is updated in place. */
+int ds4x_ref_decode_local(const uint16_t* q, const uint16_t* w, const uint16_t* q_attn, uint16_t* k,
+                          uint16_t* kv, int kv_dtype, int32_t capacity, int32_t S0,
+                          const uint16_t* k_new, const uint16_t* kv_new, int32_t n_new, int32_t pos0,
+                          int32_t n_steps, int32_t H, int32_t D, int32_t ratio, int32_t k_top,
+                          int32_t Hq, int32_t Dkv, float scale, uint16_t* kv_raw,
+                          int32_t raw_capacity, const uint16_t* kv_raw_new, int32_t window,
+                          int32_t* positions, int32_t* indices, uint16_t* out, float* lse,
+                          int32_t* S_steps) {
+  if (n_steps < 0 || capacity < 1 || S0 < 0 || S0 > capacity || n_new < 0 || ratio < 1 || pos0 < 0 ||
+      window < 0 || (int64_t)pos0 + n_steps > raw_capacity)
+    return -1;
+  memcpy(kv_raw + (int64_t)pos0 * Dkv, kv_raw_new, sizeof(uint16_t) * (size_t)n_steps * Dkv);
+  int32_t S = S0, a = 0;
+  for (int32_t i = 0; i < n_steps; ++i) {
+    const int64_t p = (int64_t)pos0 + i;
+    positions[i] = (int32_t)p;
+    while (S < capacity && a < n_new && (int64_t)S < (p + 1) / ratio) {
+      memcpy(k + (int64_t)S * D, k_new + (int64_t)a * D, sizeof(uint16_t) * (size_t)D);
+      memcpy(kv + (int64_t)S * Dkv, kv_new + (int64_t)a * Dkv, sizeof(uint16_t) * (size_t)Dkv);
+      ++S;
+      ++a;
+    }
+    S_steps[i] = S;
+    int rc = ds4x_ref_index_and_attend_local(q + (int64_t)i * H * D, w + (int64_t)i * H, k, positions + i,
+                                             q_attn + (int64_t)i * Hq * Dkv, kv, kv_raw, kv_dtype, 1, H, D, S,
+                                             ratio, k_top, Hq, Dkv, 0, pos0 + n_steps, window, scale,
+                                             indices + (int64_t)i * k_top, out + (int64_t)i * Hq * Dkv,
+                                             lse + (int64_t)i * Hq);
+    if (rc != 0) return rc;
+  }
+  return 0;
+}
+

@@ -648,6 +648,55 @@ def check_compress_split_calls_equal_one(o):
         assert np.array_equal(fx2, wfx) and np.array_equal(fg2, wfg), cut
 
 
+def _tiny_decode_local_case(seed=8):
+    c = _tiny_decode_case(seed)
+    rng = np.random.default_rng(seed + 100)
+    raw_cap = c["pos0"] + c["n_steps"] + 3
+    kv_raw = synth.to_bf16_bits(rng.standard_normal((raw_cap, c["kv"].shape[1])))   # history below pos0
+    kv_raw_new = synth.to_bf16_bits(rng.standard_normal((c["n_steps"], c["kv"].shape[1])))
+    c.update(kv_raw=kv_raw, kv_raw_new=kv_raw_new, window=5)
+    return c
+
+
+def check_decode_local_window_off(o):
+    # window 0: the plain decode loop, bit for bit
+    c = _tiny_decode_local_case()
+    a = o.decode(c["q"], c["w"], c["qa"], c["k"], c["kv"], "bf16", c["S0"], c["pos0"], c["ratio"], c["k_new"],
+                 c["kv_new"], c["k_top"], 0.25)
+    b = o.decode_local(c["q"], c["w"], c["qa"], c["k"], c["kv"], "bf16", c["S0"], c["pos0"], c["ratio"], c["k_new"],
+                       c["kv_new"], c["k_top"], 0.25, c["kv_raw"], c["kv_raw_new"], 0)
+    for x, y in zip(a[:5], b[:5]):
+        assert np.array_equal(x, y)
+
+
+def check_decode_local_steps_brute_force(o):
+    # each step against numpy: the definition score, sorted() ranking, and a textbook softmax over
+    # the selected pooled rows together with the raw rows of the step's last `window` positions
+    c = _tiny_decode_local_case()
+    scale, W = 0.25, c["window"]
+    idx, out, lse, pos, s_steps, _, _, raw_after = o.decode_local(
+        c["q"], c["w"], c["qa"], c["k"], c["kv"], "bf16", c["S0"], c["pos0"], c["ratio"], c["k_new"], c["kv_new"],
+        c["k_top"], scale, c["kv_raw"], c["kv_raw_new"], W)
+    p0, n = c["pos0"], c["n_steps"]
+    assert np.array_equal(raw_after[p0:p0 + n], c["kv_raw_new"])          # the steps' raw rows in place
+    assert np.array_equal(raw_after[:p0], c["kv_raw"][:p0])               # the history untouched
+    rows_k = np.concatenate([c["k"][:c["S0"]], c["k_new"]])
+    rows_kv = np.concatenate([c["kv"][:c["S0"]], c["kv_new"]])
+    kf, kvf, rawf = _f16_val(rows_k), _bits_val(rows_kv, "bf16"), _bits_val(raw_after, "bf16")
+    for i in range(n):
+        p = p0 + i
+        S = min(c["S0"] + c["n_new"], max(c["S0"], (p + 1) // c["ratio"]))
+        nv = min(S, (p + 1) // c["ratio"])
+        qf, wf = _f16_val(c["q"][i]), _f16_val(c["w"][i])
+        score = (wf[:, None] * np.maximum(qf @ kf[:nv].T, 0.0)).sum(axis=0).astype(np.float32)
+        ranked = sorted(sorted(range(nv), key=lambda s_: (-float(score[s_]), s_))[:c["k_top"]])
+        assert list(idx[i]) == ranked + [-1] * (c["k_top"] - len(ranked)), i
+        V = np.concatenate([kvf[ranked], rawf[max(0, p - W + 1):p + 1]])
+        ref, rlse = _softmax_rows(_bits_val(c["qa"][i], "bf16"), V, scale)
+        assert np.allclose(_bits_val(out[i], "bf16"), ref, rtol=2 ** -8, atol=1e-6), i
+        assert np.allclose(lse[i], rlse, rtol=1e-6, atol=1e-6), i
+
+
 ALL_CHECKS = [
     check_f16_decode_exhaustive, check_bf16_decode_exhaustive, check_encode_rne,
     check_visibility, check_golden_example, check_scores_int64_closed_form,
@@ -658,5 +707,5 @@ ALL_CHECKS = [
     check_local_pooled_union_vs_textbook, check_local_pooled_lse_merge, check_local_zero_query_is_mean,
     check_local_window_off_is_sparse_attn, check_index_and_attend_local_composes,
     check_compress_equal_gates_is_mean, check_compress_dominant_gate_selects_row, check_compress_vs_numpy,
-    check_compress_split_calls_equal_one,
+    check_compress_split_calls_equal_one, check_decode_local_window_off, check_decode_local_steps_brute_force,
 ]

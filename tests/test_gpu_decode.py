@@ -88,3 +88,36 @@ def test_split_attention_matches_oracle(T, k_top):
     ref_scores = oracle.indexer_score(inp.q, inp.w, inp.k, inp.positions, wl.ratio, S=wl.S)
     ref_idx, _ = oracle.topk(ref_scores, inp.positions, wl.S, wl.ratio, k_top)
     check_index_sets(gidx, ref_idx, ref_scores, inp.positions, wl.ratio, wl.S, k_top)
+
+
+# --------------------------------------------------- the decode loop with the raw window
+@pytest.mark.parametrize("S0,extra,n_steps,window", [(4096, 16, 24, 128), (2048, 4, 12, 100), (262144, 64, 6, 128)])
+def test_decode_local_vs_oracle(S0, extra, n_steps, window):
+    # each step attends to its selected pooled rows and the raw rows of its last `window` positions;
+    # the raw history below pos0 is the caller's, the steps' own raw rows are written by the call
+    wl, inp, pos0, k0, kv0, k_new, kv_new = _decode_case(S0, extra, n_steps, seed=3)
+    raw_cap = pos0 + n_steps + 5
+    hist = synth.local_rows(3, f"decode_raw_{S0}", window, wl.Dkv, "normal", wl.kv_dtype)
+    kv_raw = np.zeros((raw_cap, wl.Dkv), dtype=np.uint16)
+    kv_raw[pos0 - window:pos0] = hist                 # the window's history
+    kv_raw_new = synth.local_rows(4, f"decode_raw_new_{S0}", n_steps, wl.Dkv, "normal", wl.kv_dtype)
+    d_k, d_kv, d_raw = dev16(k0, "f16"), dev16(kv0, wl.kv_dtype), dev16(kv_raw, wl.kv_dtype)
+    idx, out, lse, pos, S_final = ds4x.decode_local(
+        dev16(inp.q, "f16"), dev16(inp.w, "f16"), dev16(inp.q_attn, wl.kv_dtype), d_k, d_kv, S0, pos0, wl.ratio,
+        d_raw, dev16(kv_raw_new, wl.kv_dtype), window, k_new=dev16(k_new, "f16"), kv_new=dev16(kv_new, wl.kv_dtype),
+        k_top=wl.k_top, scale=wl.scale)
+    torch.cuda.synchronize()
+    assert ds4x.device_status() == ds4x.OK
+    ridx, rout, rlse, rpos, rS, rk, rkv, rraw = oracle.decode_local(
+        inp.q, inp.w, inp.q_attn, k0, kv0, wl.kv_dtype, S0, pos0, wl.ratio, k_new, kv_new, wl.k_top, wl.scale,
+        kv_raw, kv_raw_new, window)
+    assert np.array_equal(pos.cpu().numpy(), rpos) and S_final == int(rS[-1])
+    assert np.array_equal(host16(d_raw), rraw)                   # the steps' raw rows, in place
+    gidx, gout, glse = idx.cpu().numpy(), host16(out), lse.cpu().numpy()
+    for i in range(n_steps):
+        S = int(rS[i])
+        ref_scores = oracle.indexer_score(inp.q[i:i + 1], inp.w[i:i + 1], rk, rpos[i:i + 1], wl.ratio, S=S)
+        check_index_sets(gidx[i:i + 1], ridx[i:i + 1], ref_scores, rpos[i:i + 1], wl.ratio, S, wl.k_top)
+        ref_out, ref_lse = oracle.local_pooled_attn(inp.q_attn[i:i + 1], rkv, rraw, wl.kv_dtype, gidx[i:i + 1],
+                                                    rpos[i:i + 1], S, 0, window, wl.scale)
+        check_attn(gout[i:i + 1], ref_out, wl.kv_dtype, glse[i:i + 1], ref_lse)

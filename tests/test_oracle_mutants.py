@@ -60,6 +60,9 @@ MUTANTS = {
                                        "const int64_t v = j * ratio + (i + 1) % ratio;\n        z[i]"),
     "compress_frontier_shifted": ("memcpy(fx_out + i * D, ref_seq_row(fx_in, x, n_frontier, v, D),",
                                   "memcpy(fx_out + i * D, ref_seq_row(fx_in, x, n_frontier, v + 1 < n ? v + 1 : v, D),"),
+    "decode_raw_rows_one_late": ("memcpy(kv_raw + (int64_t)pos0 * Dkv, kv_raw_new",
+                                 "memcpy(kv_raw + (int64_t)(pos0 + 1) * Dkv, kv_raw_new"),
+    "decode_window_misses_new_rows": ("Dkv, 0, pos0 + n_steps, window, scale,", "Dkv, 0, pos0, window, scale,"),
     "w_index_transposed": ("ref_decode_n(w + (int64_t)t * H, H, REF_F16, wd);\n      int64_t n",
                            "ref_decode_n(w + (int64_t)t, H, REF_F16, wd);\n      int64_t n"),
 }
