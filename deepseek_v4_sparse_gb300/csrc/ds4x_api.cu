@@ -271,7 +271,7 @@ const char* ds4x_status_string(int status) {
   switch (status) {
     case DS4X_OK: return "DS4X_OK";
     case DS4X_ERR_INVALID: return "DS4X_ERR_INVALID: invalid argument";
-    case DS4X_ERR_UNSUPPORTED: return "DS4X_ERR_UNSUPPORTED: shape not supported by this build";
+    case DS4X_ERR_UNSUPPORTED: return "DS4X_ERR_UNSUPPORTED: shape not supported by this library";
     case DS4X_ERR_CUDA: return "DS4X_ERR_CUDA: a CUDA call or kernel launch failed";
     case DS4X_ERR_WORKSPACE: return "DS4X_ERR_WORKSPACE: workspace too small";
     case DS4X_ERR_TIMEOUT: return "DS4X_ERR_TIMEOUT: a bounded device wait gave up";

@@ -55,7 +55,7 @@ typedef enum { DS4X_F16 = 0, DS4X_BF16 = 1 } ds4x_dtype;
 typedef enum {
   DS4X_OK = 0,
   DS4X_ERR_INVALID = -1,     /* null/misaligned pointer, negative size, bad ld, ...  */
-  DS4X_ERR_UNSUPPORTED = -2, /* a shape this build has no kernel for                 */
+  DS4X_ERR_UNSUPPORTED = -2, /* a shape this library has no kernel for               */
   DS4X_ERR_CUDA = -3,        /* a kernel launch or device query failed              */
   DS4X_ERR_WORKSPACE = -4,   /* workspace_bytes smaller than the *_workspace_bytes() */
   DS4X_ERR_TIMEOUT = -5      /* a bounded device-side wait gave up                  */

@@ -69,7 +69,7 @@ def test_invalid_arguments_rejected_without_launch(lib):
     assert lib.ds4x_topk(_p(A), 10, _p(A), 4, 10, 4, 0, _p(A), None, None, 0, None) == ds4x.ERR_INVALID
     assert lib.ds4x_topk(_p(A), 10, _p(A), 4, 10, 4, 4096, _p(A), None, None, 0, None) == ds4x.ERR_UNSUPPORTED
     assert lib.ds4x_topk(_p(A), 10, _p(A), 4, 10, 4, 512, None, None, None, 0, None) == ds4x.ERR_INVALID
-    # attention: shapes this build has no kernel for, bad dtype
+    # attention: shapes the library has no kernel for, bad dtype
     assert lib.ds4x_sparse_attn(_p(A), _p(A), 1, _p(A), 4, 32, 512, 10, 512, 0.1, _p(A), None, None) == ds4x.ERR_UNSUPPORTED
     assert lib.ds4x_sparse_attn(_p(A), _p(A), 1, _p(A), 4, 64, 256, 10, 512, 0.1, _p(A), None, None) == ds4x.ERR_UNSUPPORTED
     assert lib.ds4x_sparse_attn(_p(A), _p(A), 7, _p(A), 4, 64, 512, 10, 512, 0.1, _p(A), None, None) == ds4x.ERR_INVALID
