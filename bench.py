@@ -58,6 +58,9 @@ def parse():
     ap.add_argument("--no-decode", action="store_true", help="skip the 1M-context decode measurement")
     ap.add_argument("--no-compress", action="store_true", help="skip the compressor measurement")
     ap.add_argument("--decode-steps", type=int, default=256, help="decode steps per timed call (decode_1m)")
+    ap.add_argument("--extra-workloads", default="prefill_32k,prefill_64k",
+                    help="other prefill chunks measured into the line's 'workloads' object (comma list, '' = none)")
+    ap.add_argument("--extra-steps", type=int, default=20, help="timed steps of each extra workload")
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
 
@@ -83,7 +86,14 @@ def job_throughput(world: int, units_per_rank: int, ms: float) -> float:
     return world * units_per_rank / (ms / 1e3)
 
 
-def workload_config(wl: synth.Workload, l2_note: str) -> dict:
+L2_NOTE = "flushed before every timed step (256 MiB write)"
+
+
+def parallelism(world: int) -> str:
+    return f"dp{world} (independent chunks per GPU)" if world > 1 else "single GPU"
+
+
+def workload_config(wl: synth.Workload, l2_note: str = L2_NOTE, world: int = 1) -> dict:
     return {
         "workload": f"{wl.name}: {wl.T} query tokens at positions {wl.pos0}..{wl.pos0 + wl.T - 1}, "
                     f"ratio {wl.ratio} -> {wl.S} compressed rows; indexer q[{wl.T},{wl.H},{wl.D}] fp16, "
@@ -91,7 +101,7 @@ def workload_config(wl: synth.Workload, l2_note: str) -> dict:
                     f"{wl.Hq} heads x {wl.Dkv} over kv[{wl.S},{wl.Dkv}] {wl.kv_dtype}",
         "T": wl.T, "S": wl.S, "H": wl.H, "D": wl.D, "ratio": wl.ratio, "k_top": wl.k_top,
         "Hq": wl.Hq, "Dkv": wl.Dkv, "kv_dtype": wl.kv_dtype, "seed": 0,
-        "l2": l2_note,
+        "l2": l2_note, "parallelism": parallelism(world),
         **({"window": wl.window,
             "attention": f"local-plus-pooled: each token's top-{wl.k_top} pooled rows and the raw rows of its "
                          f"last {wl.window} positions in one softmax (kv_local[{wl.T + wl.window - 1},{wl.Dkv}])"}
@@ -262,12 +272,109 @@ def run_reference(args, wl):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(wl, "host run (no GPU)"),
+        "data": "synthetic", "config": workload_config(wl, world=world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"{per_step} random tokens of the {wl.T}-token chunk per step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------- stage rooflines
+def stage_roofline(wl: synth.Workload, st_mean, peaks: dict):
+    """Per-stage times, the dominant stage against its roofline, and every stage's rate."""
+    alg = algorithmic(wl)
+    stages = {"score_ms": float(st_mean[0]), "topk_ms": float(st_mean[1]), "attn_ms": float(st_mean[2])}
+    dom = int(np.argmax(st_mean))
+    if dom == 0:
+        ach = alg["score_flops"] / (st_mean[0] / 1e3) / 1e12
+        roof = {"kernel": "score_kernel (tcgen05)", "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "algorithmic": alg["score_flops"], "traffic": profiled_traffic("score", wl.name)}
+    elif dom == 1:
+        ach = alg["topk_bytes"] / (st_mean[1] / 1e3) / 1e9
+        roof = {"kernel": "top-k kernel", "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "algorithmic": alg["topk_bytes"], "traffic": profiled_traffic("topk", wl.name)}
+    else:
+        ach = alg["attn_flops"] / (st_mean[2] / 1e3) / 1e12
+        roof = {"kernel": "sparse_mqa_kernel (tcgen05)", "bound": "tensor", "achieved": ach,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "algorithmic": alg["attn_flops"],
+                "traffic": profiled_traffic("attn", wl.name)}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["peak_source"] = f"{peaks['source']} (burst)"
+    others = {
+        "score_tflops": alg["score_flops"] / (st_mean[0] / 1e3) / 1e12,
+        "score_frac": alg["score_flops"] / (st_mean[0] / 1e3) / 1e12 / peaks["bf16_tflops"],
+        "topk_gbs": alg["topk_bytes"] / (st_mean[1] / 1e3) / 1e9,
+        "topk_frac": alg["topk_bytes"] / (st_mean[1] / 1e3) / 1e9 / peaks["hbm_gbs"],
+        "attn_tflops": alg["attn_flops"] / (st_mean[2] / 1e3) / 1e12,
+        "attn_frac": alg["attn_flops"] / (st_mean[2] / 1e3) / 1e12 / peaks["bf16_tflops"],
+        "attn_gather_gbs": alg["attn_gather_bytes"] / (st_mean[2] / 1e3) / 1e9,
+    }
+    return stages, roof, others
+
+
+def measure_prefill(ds4x, torch, dev, stream, wl: synth.Workload, seed: int, steps: int, peaks: dict, flush,
+                    cpu: bool):
+    """One more prefill chunk on this GPU, timed like the headline workload (inputs resident, L2
+    flushed before every step, CUDA events on the launching stream): `steps` whole-path calls for
+    the throughput, `steps` staged calls for the per-stage times, and the oracle on a bounded
+    sample of the chunk's tokens on the host cores."""
+    inp = synth.make_inputs(wl, seed=seed)
+    kvt = torch.bfloat16 if wl.kv_dtype == "bf16" else torch.float16
+
+    def d16(a, dt):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(dt)
+    q, w, k = d16(inp.q, torch.float16), d16(inp.w, torch.float16), d16(inp.k, torch.float16)
+    qa, kv = d16(inp.q_attn, kvt), d16(inp.kv, kvt)
+    pos = torch.from_numpy(inp.positions.copy()).to(dev)
+    T, S, k_top = wl.T, wl.S, wl.k_top
+    scores = torch.empty((T, S), dtype=torch.float32, device=dev)
+    idx = torch.empty((T, k_top), dtype=torch.int32, device=dev)
+    out = torch.empty_like(qa)
+    lse = torch.empty((T, wl.Hq), dtype=torch.float32, device=dev)
+    ws = torch.empty((max(1, ds4x.workspace_bytes(T, S, k_top)),), dtype=torch.uint8, device=dev)
+    tws_n = ds4x.topk_workspace_bytes(T, S, k_top)
+    tws = torch.empty((tws_n,), dtype=torch.uint8, device=dev) if tws_n else None
+
+    def fused():
+        ds4x.index_and_attend(q, w, k, pos, qa, kv, wl.ratio, k_top, S=S, scale=wl.scale, indices=idx, out=out,
+                              lse=lse, workspace=ws, stream=stream)
+
+    def staged(ev):
+        ev[0].record(stream)
+        ds4x.indexer_score(q, w, k, pos, wl.ratio, scores=scores, S=S, stream=stream)
+        ev[1].record(stream)
+        ds4x.topk(scores, pos, S, wl.ratio, k_top, indices=idx, workspace=tws, stream=stream)
+        ev[2].record(stream)
+        ds4x.sparse_attn(qa, kv, idx, S=S, scale=wl.scale, out=out, lse=lse, stream=stream)
+        ev[3].record(stream)
+
+    for _ in range(3):
+        fused()
+        staged([torch.cuda.Event(enable_timing=True) for _ in range(4)])
+    torch.cuda.synchronize()
+    fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        fev[i][0].record(stream)
+        fused()
+        fev[i][1].record(stream)
+    for i in range(steps):
+        flush.zero_()
+        staged(sev[i])
+    torch.cuda.synchronize()
+    assert ds4x.device_status() == ds4x.OK, f"a bounded device wait timed out ({wl.name})"
+    ms = float(np.mean([a.elapsed_time(b) for a, b in fev]))
+    st = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in sev]).mean(axis=0)
+    stages, roof, rates = stage_roofline(wl, st, peaks)
+    res = {"config": workload_config(wl), "value": T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
+           "steps": steps, "warmup": 3, "roofline": roof, "stage_ms": stages, "stage_rates": rates,
+           "staged_ms_per_step": float(st.sum())}
+    if cpu:
+        v, cores, desc = cpu_baseline(wl, inp, target_s=5.0, first=16)
+        res["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+    return res
 
 
 # ---------------------------------------------------------------------------- decode loop
@@ -437,6 +544,22 @@ def measure_compress(ds4x, torch, dev, stream, seed: int, reps: int = 20):
     return out
 
 
+def decode_roofline(dec: dict, peaks: dict) -> dict:
+    """A decode step is bound by memory: every step reads all of k ([rows, 128] fp16) for the scores,
+    writes and reads one fp32 score per row, and gathers 512 kv rows; rows = the call's average S."""
+    wl = synth.WORKLOADS["decode_1m"]
+    rows = wl.S + dec["appended_rows"] / 2.0
+    step_bytes = 2.0 * wl.D * rows + 2 * 4.0 * rows + 2.0 * wl.Dkv * wl.k_top
+    roof = {"kernel": "decode step (score, top-k, attention launches)", "bound": "hbm",
+            "achieved": step_bytes / (dec["us_per_step"] * 1e-6) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "algorithmic": step_bytes, "traffic": None}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["peak_source"] = f"{peaks['source']} (burst)"
+    if dec.get("graph_us_per_step"):
+        roof["graph_frac"] = step_bytes / (dec["graph_us_per_step"] * 1e-6) / 1e9 / peaks["hbm_gbs"]
+    return roof
+
+
 def decode_main(args, ds4x, torch, dev, rank, world):
     """--workload decode_1m: the decode loop is the step (one call = decode_steps tokens)."""
     import torch.distributed as dist
@@ -446,16 +569,7 @@ def decode_main(args, ds4x, torch, dev, rank, world):
         dec = measure_decode(ds4x, torch, dev, stream, args.seed + rank, reps=max(1, args.steps),
                              n_steps=args.decode_steps, warm=max(3, args.warmup))
     peaks = load_peaks()
-    # a decode step is bound by memory: every step reads all of k ([rows, 128] fp16) for the scores,
-    # writes and reads one fp32 score per row, and gathers 512 kv rows; rows = the average S
-    wl = synth.WORKLOADS["decode_1m"]
-    rows = wl.S + dec["appended_rows"] / 2.0
-    step_bytes = 2.0 * wl.D * rows + 2 * 4.0 * rows + 2.0 * wl.Dkv * wl.k_top
-    roof = {"kernel": "decode step (score, top-k, attention launches)", "bound": "hbm",
-            "achieved": step_bytes / (dec["us_per_step"] * 1e-6) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "algorithmic": step_bytes, "traffic": None}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["peak_source"] = f"{peaks['source']} (burst)"
+    roof = decode_roofline(dec, peaks)
     # the slowest rank's time per decode step; each rank decodes its own token stream
     us_step = max_over_ranks(torch, dist, dec["us_per_step"], world, dev)
     if rank == 0:
@@ -636,37 +750,22 @@ def main():
                        "overlapped by sub-chunks of tokens)", "host_chunks": args.host_chunks}
 
     # ------------------------------------------------------------------ roofline
-    alg = algorithmic(wl)
     peaks = load_peaks()
     st_mean = stage_ms.mean(axis=0)
-    stages = {"score_ms": float(st_mean[0]), "topk_ms": float(st_mean[1]), "attn_ms": float(st_mean[2])}
-    dom = int(np.argmax(st_mean))
-    if dom == 0:
-        ach = alg["score_flops"] / (st_mean[0] / 1e3) / 1e12
-        roof = {"kernel": "score_kernel (tcgen05)", "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "algorithmic": alg["score_flops"], "traffic": profiled_traffic("score", wl.name)}
-    elif dom == 1:
-        ach = alg["topk_bytes"] / (st_mean[1] / 1e3) / 1e9
-        roof = {"kernel": "topk_row_kernel", "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "algorithmic": alg["topk_bytes"], "traffic": profiled_traffic("topk", wl.name)}
-    else:
-        ach = alg["attn_flops"] / (st_mean[2] / 1e3) / 1e12
-        roof = {"kernel": "sparse_mqa_kernel (tcgen05)", "bound": "tensor", "achieved": ach,
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "algorithmic": alg["attn_flops"],
-                "traffic": profiled_traffic("attn", wl.name)}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["peak_source"] = f"{peaks['source']} (burst)"
-    others = {
-        "score_tflops": alg["score_flops"] / (st_mean[0] / 1e3) / 1e12,
-        "topk_gbs": alg["topk_bytes"] / (st_mean[1] / 1e3) / 1e9,
-        "attn_tflops": alg["attn_flops"] / (st_mean[2] / 1e3) / 1e12,
-        "attn_gather_gbs": alg["attn_gather_bytes"] / (st_mean[2] / 1e3) / 1e9,
-    }
+    stages, roof, others = stage_roofline(wl, st_mean, peaks)
 
     dec = dec_local = None
     if rank == 0 and not args.no_decode and wl.name != "decode_1m":
         dec = measure_decode(ds4x, torch, dev, stream, args.seed)
+        dec["roofline"] = decode_roofline(dec, peaks)
         dec_local = measure_decode(ds4x, torch, dev, stream, args.seed, window=128)
+
+    extra = None
+    names = [n for n in args.extra_workloads.split(",") if n and n != wl.name]
+    if rank == 0 and names:
+        extra = {n: measure_prefill(ds4x, torch, dev, stream, synth.WORKLOADS[n], args.seed, args.extra_steps,
+                                    peaks, flush, cpu=not args.no_cpu_baseline and world == 1)
+                 for n in names}
 
     comp = None
     if rank == 0 and not args.no_compress:
@@ -685,12 +784,12 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16+bf16 (fp32 accumulate)",
             "data": "synthetic",
-            "config": dict(workload_config(wl, "flushed before every timed step (256 MiB write)"),
-                           parallelism=f"dp{world} (independent chunks per GPU)" if world > 1 else "single GPU"),
+            "config": workload_config(wl, world=world),
             "roofline": roof, "stage_ms": stages, "stage_rates": others,
             "staged_ms_per_step": float(stage_ms.sum(axis=1).mean()),
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
-            "clocks": sampler.summary(), "decode": dec, "decode_local": dec_local, "compress": comp,
+            "clocks": sampler.summary(), "workloads": extra, "decode": dec, "decode_local": dec_local,
+            "compress": comp,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -155,6 +155,13 @@ def _need(t, dtype, name):
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _need_positions(positions, T: int):
+    """positions must be int32 with at least one entry per token (the kernels read T of them)."""
+    _need(positions, _torch().int32, "positions")
+    if positions.numel() < T:
+        raise ValueError(f"positions holds {positions.numel()} entries for {T} tokens")
+
+
 # ------------------------------------------------------------------------------ entry points
 def workspace_bytes(T: int, S: int, k_top: int) -> int:
     return int(load().ds4x_workspace_bytes(T, S, k_top))
@@ -173,8 +180,8 @@ def indexer_score(q, w, k, positions, ratio: int, scores=None, S: int | None = N
     q [T,H,D] fp16, w [T,H] fp16, k [>=S, D] fp16, positions [T] int32 (CUDA tensors)."""
     torch = _torch()
     _need(q, torch.float16, "q"); _need(w, torch.float16, "w"); _need(k, torch.float16, "k")
-    _need(positions, torch.int32, "positions")
     T, H, D = q.shape
+    _need_positions(positions, T)
     S = k.shape[0] if S is None else S
     if scores is None:
         scores = torch.empty((T, S), dtype=torch.float32, device=q.device)
@@ -192,6 +199,7 @@ def topk(scores, positions, S: int, ratio: int, k_top: int = 512, indices=None, 
     torch = _torch()
     _need(scores, torch.float32, "scores")
     T, ld = scores.shape
+    _need_positions(positions, T)
     dev = scores.device
     if indices is None:
         indices = torch.empty((T, k_top), dtype=torch.int32, device=dev)
@@ -525,6 +533,7 @@ def topk_static_scratch(scores, positions, S: int, ratio: int, k_top: int = 512,
     torch = _torch()
     _need(scores, torch.float32, "scores")
     T, ld = scores.shape
+    _need_positions(positions, T)
     if indices is None:
         indices = torch.empty((T, k_top), dtype=torch.int32, device=scores.device)
     if counts is None:

@@ -88,6 +88,48 @@ int* device_status_ptr() {
 void count_launch(int n) { t_launches += n; }
 
 namespace {
+struct SmemAttr {
+  const void* func;
+  int bytes;
+};
+constexpr int kMaxAttrKernels = 64;
+std::mutex g_attr_mutex;
+SmemAttr g_attr[kMaxDevices][kMaxAttrKernels];
+int g_attr_count[kMaxDevices];
+}  // namespace
+
+EncodeTiledFn encode_tiled_fn() {
+  static const EncodeTiledFn fn = [] {  // a function-local static: initialised once, thread-safe
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<EncodeTiledFn>(ptr);
+    return static_cast<EncodeTiledFn>(nullptr);
+  }();
+  return fn;
+}
+
+cudaError_t ensure_dynamic_smem_raw(const void* func, int bytes) {
+  const int d = current_device();
+  std::lock_guard<std::mutex> lock(g_attr_mutex);
+  SmemAttr* tab = g_attr[d];
+  int i = 0;
+  while (i < g_attr_count[d] && tab[i].func != func) ++i;
+  if (i < g_attr_count[d] && tab[i].bytes >= bytes) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  if (i < g_attr_count[d]) {
+    tab[i].bytes = bytes;
+  } else if (i < kMaxAttrKernels) {  // a full table only means the attribute is set on every call
+    tab[i] = SmemAttr{func, bytes};
+    g_attr_count[d] = i + 1;
+  }
+  return cudaSuccess;
+}
+
+namespace {
 size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
 }  // namespace
 

@@ -1,5 +1,6 @@
 // ds4x_internal.h — declarations shared by the kernels' host launchers and the C ABI layer.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -39,6 +40,19 @@ int call_end(int rc);
 // Device address of the library's status word on the current device (bounded waits that give
 // up record DS4X_ERR_TIMEOUT there).
 int* device_status_ptr();
+// The driver's cuTensorMapEncodeTiled, looked up once per process (nullptr if the driver lacks it).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the current device.  The
+// attribute belongs to the device, so it is recorded per device (under a lock) and set again on
+// each device that launches the kernel for the first time.
+cudaError_t ensure_dynamic_smem_raw(const void* func, int bytes);
+template <typename... KArgs>
+inline cudaError_t ensure_dynamic_smem(void (*kernel)(KArgs...), int bytes) {
+  return ensure_dynamic_smem_raw(reinterpret_cast<const void*>(kernel), bytes);
+}
 
 struct ScoreArgs {
   const void* q;             // [T, H, D] fp16

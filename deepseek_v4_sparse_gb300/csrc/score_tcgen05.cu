@@ -467,28 +467,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
 
 // 2-D fp16 tensor [rows, cols] (cols contiguous), box = 64 columns x box_rows rows, 128B swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  EncodeTiledFn fn = encode_fn();
+  EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
@@ -502,13 +484,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 template <int H, int D, int TN>
 int launch_impl(const ScoreArgs& a, cudaStream_t stream) {
   using C = Cfg<H, D, TN>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(score_kernel<H, D, TN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
-        cudaSuccess)
-      return DS4X_ERR_CUDA;
-    attr_set = true;
-  }
+  if (ensure_dynamic_smem(score_kernel<H, D, TN>, C::SMEM) != cudaSuccess) return DS4X_ERR_CUDA;
   CUtensorMap tq, tk;
   if (!make_map(&tq, a.q, (uint64_t)a.T * H, D, TN) || !make_map(&tk, a.k, (uint64_t)a.S, D, kTileS))
     return DS4X_ERR_CUDA;

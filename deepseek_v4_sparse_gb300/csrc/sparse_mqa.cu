@@ -775,37 +775,13 @@ size_t partial_bytes_for(int T, int nsplit) {
   return (size_t)T * nsplit * ((size_t)kHq * kDkv * 4 + 2 * kHq * 4);
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
 
 template <bool kBf16>
 int launch_impl(const AttnArgs& a, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(sparse_mqa_kernel<kBf16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(sparse_mqa_kernel<kBf16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
-            cudaSuccess)
-      return DS4X_ERR_CUDA;
-    attr_set = true;
-  }
-  EncodeTiledFn fn = encode_fn();
+  if (ensure_dynamic_smem(sparse_mqa_kernel<kBf16, false>, kSmem) != cudaSuccess ||
+      ensure_dynamic_smem(sparse_mqa_kernel<kBf16, true>, kSmem) != cudaSuccess)
+    return DS4X_ERR_CUDA;
+  EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return DS4X_ERR_CUDA;
   CUtensorMap tq;
   cuuint64_t dims[2] = {(cuuint64_t)kDkv, (cuuint64_t)a.T * kHq};

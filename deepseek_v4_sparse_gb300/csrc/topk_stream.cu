@@ -1530,22 +1530,23 @@ extern "C" int ds4x_topk_static_scratch(const float* scores, int64_t ld_scores, 
                                         int32_t T, int32_t S, int32_t ratio, int32_t k_top, int32_t* indices,
                                         int32_t* counts, void* stream) {
   using namespace ds4x;
-  if (T < 0 || S < 0 || ratio < 1 || ld_scores < S) return DS4X_ERR_INVALID;
-  if (k_top < 1 || k_top > DS4X_MAX_KTOP) return k_top < 1 ? DS4X_ERR_INVALID : DS4X_ERR_UNSUPPORTED;
-  if (T == 0) return DS4X_OK;
-  if (!scores || !positions || !indices) return DS4X_ERR_INVALID;
+  call_begin();  // launch accounting for ds4x_last_launch_count
+  if (T < 0 || S < 0 || ratio < 1 || ld_scores < S) return call_end(DS4X_ERR_INVALID);
+  if (k_top < 1 || k_top > DS4X_MAX_KTOP) return call_end(k_top < 1 ? DS4X_ERR_INVALID : DS4X_ERR_UNSUPPORTED);
+  if (T == 0) return call_end(DS4X_OK);
+  if (!scores || !positions || !indices) return call_end(DS4X_ERR_INVALID);
   const uintptr_t mis = (reinterpret_cast<uintptr_t>(scores) | reinterpret_cast<uintptr_t>(positions) |
                          reinterpret_cast<uintptr_t>(indices) | reinterpret_cast<uintptr_t>(counts)) & 15u;
-  if (mis) return DS4X_ERR_INVALID;
+  if (mis) return call_end(DS4X_ERR_INVALID);
   // the candidate lists must fit the fixed array
-  if (topk_workspace_bytes(T, S, k_top) > (size_t)DS4X_TOPK_STATIC_SCRATCH_BYTES) return DS4X_ERR_WORKSPACE;
+  if (topk_workspace_bytes(T, S, k_top) > (size_t)DS4X_TOPK_STATIC_SCRATCH_BYTES) return call_end(DS4X_ERR_WORKSPACE);
   void* scratch = static_scratch_address();
-  if (scratch == nullptr) return DS4X_ERR_CUDA;
+  if (scratch == nullptr) return call_end(DS4X_ERR_CUDA);
   const size_t smem = row_kernel_smem(S);
   const size_t msmem = bitmap_smem(S);
-  if (smem > 220 * 1024 || msmem > 220 * 1024) return DS4X_ERR_UNSUPPORTED;
+  if (smem > 220 * 1024 || msmem > 220 * 1024) return call_end(DS4X_ERR_UNSUPPORTED);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (set_smem_attrs(smem, msmem) != cudaSuccess) return DS4X_ERR_CUDA;
+  if (set_smem_attrs(smem, msmem) != cudaSuccess) return call_end(DS4X_ERR_CUDA);
   KParams p;
   p.scores = scores;
   p.ld = ld_scores;
@@ -1563,6 +1564,7 @@ extern "C" int ds4x_topk_static_scratch(const float* scores, int64_t ld_scores, 
   cudaError_t e;
   if (p.nslice <= 1) {
     e = launch_one_cta_per_token(p, smem, st);
+    count_launch();
   } else {
     // the first launch zeroes every counter, histogram and bitmap the later ones read, so
     // nothing left in the array by an earlier call is ever read
@@ -1570,5 +1572,5 @@ extern "C" int ds4x_topk_static_scratch(const float* scores, int64_t ld_scores, 
     p.long_ws = static_cast<uint8_t*>(scratch) + long_counters_bytes(T);
     e = long_coop_fits(T, p.nslice, msmem) ? launch_long_coop(p, st, msmem, false) : launch_long(p, st, msmem);
   }
-  return e == cudaSuccess ? DS4X_OK : DS4X_ERR_CUDA;
+  return call_end(e == cudaSuccess ? DS4X_OK : DS4X_ERR_CUDA);
 }

@@ -118,7 +118,10 @@ size_t ds4x_topk_workspace_bytes(int32_t T, int32_t S, int32_t k_top);
  *   over many CTAs) live instead in a fixed array of DS4X_TOPK_STATIC_SCRATCH_BYTES compiled
  *   into the library; every GPU that loads the library holds that array until the process exits.
  *   - Calls needing more than that (ds4x_topk_workspace_bytes(T, S, k_top) > the maximum) return
- *     DS4X_ERR_WORKSPACE and launch nothing.
+ *     DS4X_ERR_WORKSPACE and launch nothing.  The split mode is used only while T is below the
+ *     GPU's SM count and rows are longer than 8192, so the need is 0 for T >= SM count: e.g. at
+ *     262144-row rows, T = 1..35 fits, T = 36..(SM count - 1) is refused and larger T runs one CTA
+ *     per token without any scratch.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
  *     that device current); make that first call before any stream capture.
  *   - Allocates nothing (no cudaMalloc, cudaFree or allocating library routine).

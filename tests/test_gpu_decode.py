@@ -67,6 +67,41 @@ def test_decode_full_size_first_steps():
     assert list(rS) == [262144] * 4 + [262145] * 2
 
 
+def test_decode_full_size_whole_call_sampled():
+    # the 1M-context decode as the benchmark runs it: 256 steps over 262144 resident rows with 64
+    # staged rows.  Rows per step follow the append rule (the oracle's decode loop is pinned to
+    # the same closed form); steps on both sides of three appends and the call's last step are
+    # compared with the oracle on the rows present at that step.
+    S0, extra, n_steps = 262144, 64, 256
+    wl, inp, pos0, k0, kv0, k_new, kv_new = _decode_case(S0, extra, n_steps, seed=5)
+    d_k, d_kv = dev16(k0, "f16"), dev16(kv0, wl.kv_dtype)
+    idx, out, lse, pos, S_final = ds4x.decode(
+        dev16(inp.q, "f16"), dev16(inp.w, "f16"), dev16(inp.q_attn, wl.kv_dtype), d_k, d_kv, S0, pos0, wl.ratio,
+        k_new=dev16(k_new, "f16"), kv_new=dev16(kv_new, wl.kv_dtype), k_top=wl.k_top, scale=wl.scale)
+    torch.cuda.synchronize()
+    assert ds4x.device_status() == ds4x.OK
+    cap = k0.shape[0]
+    rpos = pos0 + np.arange(n_steps, dtype=np.int64)
+    rS = np.minimum(np.minimum(S0 + extra, cap), np.maximum(S0, (rpos + 1) // wl.ratio))
+    assert np.array_equal(pos.cpu().numpy(), rpos.astype(np.int32)) and S_final == int(rS[-1]) == S0 + 63
+    # the rows after the call: the staged rows appended in order, the rest untouched
+    n_app = int(rS[-1]) - S0
+    rk, rkv = k0.copy(), kv0.copy()
+    rk[S0:S0 + n_app], rkv[S0:S0 + n_app] = k_new[:n_app], kv_new[:n_app]
+    assert np.array_equal(host16(d_k), rk) and np.array_equal(host16(d_kv), rkv)
+    gidx, gout, glse = idx.cpu().numpy(), host16(out), lse.cpu().numpy()
+    steps = [0, 3, 4, 127, 128, 255]
+    assert [int(rS[i]) for i in steps] == [262144, 262144, 262145, 262175, 262176, 262207]
+    for i in steps:
+        S = int(rS[i])
+        p_i = rpos[i:i + 1].astype(np.int32)
+        ref_scores = oracle.indexer_score(inp.q[i:i + 1], inp.w[i:i + 1], rk, p_i, wl.ratio, S=S)
+        ref_idx, _ = oracle.topk(ref_scores, p_i, S, wl.ratio, wl.k_top)
+        check_index_sets(gidx[i:i + 1], ref_idx, ref_scores, p_i, wl.ratio, S, wl.k_top)
+        ref_out, ref_lse = oracle.sparse_attn(inp.q_attn[i:i + 1], rkv, wl.kv_dtype, gidx[i:i + 1], S, wl.scale)
+        check_attn(gout[i:i + 1], ref_out, wl.kv_dtype, glse[i:i + 1], ref_lse)
+
+
 @pytest.mark.parametrize("T,k_top", [(1, 512), (16, 512), (50, 512), (76, 512), (1, 300)])
 def test_split_attention_matches_oracle(T, k_top):
     # few tokens: the fused path splits each token's attention over CTAs (uneven splits at

@@ -298,6 +298,41 @@ def test_full_size_sampled(name):
     assert np.all(allidx[:, 0] >= 0) and np.all(allidx[:, -1] < nv)
 
 
+def test_scores_full_64k_rows_elementwise():
+    # the 64k chunk's scorer in its wide-tile launch (4 tokens x 64 heads a tile) over all 16384
+    # rows, element by element against the oracle: the last 20 tokens of the chunk (five token
+    # groups, each seeing 15868..16384 rows, so the masked tails differ)
+    wl = synth.WORKLOADS["prefill_64k"]
+    T = 20
+    inp = synth.make_inputs(wl, seed=0, T=T, pos0=wl.pos0 + wl.T - T)
+    d = to_device(inp)
+    scores = ds4x.indexer_score(d["q"], d["w"], d["k"], d["positions"], wl.ratio, S=wl.S)
+    torch.cuda.synchronize()
+    assert ds4x.device_status() == ds4x.OK
+    ref = oracle.indexer_score(inp.q, inp.w, inp.k, inp.positions, wl.ratio, S=wl.S)
+    check_scores(scores.cpu().numpy(), ref, inp.positions, wl.ratio, wl.S, exact=False)
+
+
+def test_scores_decode_rows_elementwise():
+    # the decode step's scorer (one token: the narrow tile) over a 1M-context row of 262181
+    # compressed rows, element by element against the oracle: a token that sees every row, the
+    # decode loop's first position (the last 37 rows masked) and one far back (a long masked tail)
+    wl = synth.WORKLOADS["decode_1m"]
+    S = 262144 + 37
+    pos = np.array([4 * S + 10, wl.pos0, 4 * 200000 - 1], dtype=np.int32)
+    inp = synth.make_inputs(wl, seed=2, T=3, S=S, rows=S)
+    d = to_device(inp)
+    got = []
+    for t in range(3):     # one call per token: each takes the narrow, single-token tile
+        pt = torch.from_numpy(pos[t:t + 1].copy()).cuda()
+        got.append(ds4x.indexer_score(d["q"][t:t + 1], d["w"][t:t + 1], d["k"], pt, wl.ratio, S=S))
+    torch.cuda.synchronize()
+    assert ds4x.device_status() == ds4x.OK
+    ref = oracle.indexer_score(inp.q, inp.w, inp.k, pos, wl.ratio, S=S)
+    check_scores(torch.cat(got).cpu().numpy(), ref, pos, wl.ratio, S, exact=False)
+    assert [n_vis(p, wl.ratio, S) for p in pos] == [S, 262144, 200000]
+
+
 def test_pooled_ratio128_all_rows():
     # the ratio-128 layer kind: a token at the end of a 64k chunk sees at most 512 pooled rows, so
     # the fused path skips scoring and attends every visible row (sequential indices)

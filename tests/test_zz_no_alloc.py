@@ -4,9 +4,9 @@ Some callers of this library may not allocate device memory while they run — a
 process that handed all of HBM to its KV cache at start-up, or a plugin inside a host framework
 that owns the allocator — so they cannot give ds4x_topk the workspace its split mode needs.
 The allocation-free variant keeps that scratch in a fixed array inside the library. These tests
-call it through the C ABI and require the same indices and counts as ds4x_topk (top-k results
-are compared bit for bit everywhere in this suite), on two calls in a row, since every call
-reuses the same array.
+call it through the C ABI and require the same indices and counts as ds4x_topk and as the CPU
+oracle's top-k on the same fp32 scores (top-k results are compared bit for bit everywhere in this
+suite), on two calls in a row, since every call reuses the same array.
 """
 import ctypes
 
@@ -15,6 +15,7 @@ import pytest
 import torch
 
 import deepseek_v4_sparse_gb300 as ds4x
+import oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -55,6 +56,10 @@ def workspace_topk(scores, positions, S, ratio, k_top):
 @pytest.mark.parametrize("T,S,ratio", [(1, 262144 + 37, 4), (3, 70000, 1), (200, 4096, 4)])
 def test_matches_workspace_entry_on_two_calls(lib, T, S, ratio):
     rng = np.random.default_rng(T * 1000 + S)
+    # the first two cases split each row over many CTAs (the mode whose scratch is the fixed
+    # array): one cooperative launch, or three launches where it cannot be resident at once
+    split = ds4x.topk_workspace_bytes(T, S, 512) > 0
+    assert split == (T < 100), "the cases are chosen to cover both modes"
     for call in range(2):
         scores = rng.standard_normal((T, S)).astype(np.float32)
         if call == 1:
@@ -64,10 +69,15 @@ def test_matches_workspace_entry_on_two_calls(lib, T, S, ratio):
         d_scores = torch.from_numpy(scores).cuda()
         d_pos = torch.from_numpy(pos).cuda()
         a_idx, a_cnt = static_topk(lib, d_scores, d_pos, S, ratio, 512)
+        launches = ds4x.last_launch_count()
+        assert launches in ((1, 3) if split else (1,)), f"call {call}: {launches} launches"
         b_idx, b_cnt = workspace_topk(d_scores, d_pos, S, ratio, 512)
         torch.cuda.synchronize()
         assert torch.equal(a_idx, b_idx), f"call {call}: indices differ from ds4x_topk"
         assert torch.equal(a_cnt, b_cnt), f"call {call}: counts differ from ds4x_topk"
+        r_idx, r_cnt = oracle.topk(scores, pos, S, ratio, 512)
+        assert np.array_equal(a_idx.cpu().numpy(), r_idx), f"call {call}: indices differ from the oracle"
+        assert np.array_equal(a_cnt.cpu().numpy(), r_cnt), f"call {call}: counts differ from the oracle"
     assert ds4x.device_status() == ds4x.OK
 
 
