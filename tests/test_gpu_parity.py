@@ -246,6 +246,33 @@ def test_topk_one_cta_rounds_exact(S, pad):
     assert np.array_equal(cnt.cpu().numpy(), ref_cnt)
 
 
+@pytest.mark.parametrize("S", [2048, 8192, 12000, 16384])
+@pytest.mark.parametrize("k_top", [300, 512, 1024])
+def test_topk_many_tokens_exact(S, k_top):
+    # at least one token per SM, so every row takes the one-token-per-CTA kernels (a warp per token up
+    # to 2048 rows; eight warps per token, one segment each, up to 16384): N(0,1) rows, small
+    # integers (long runs of ties), a row whose best scores all sit in one segment, a row of equal
+    # scores, and visible counts from just above k_top to the whole row
+    T = 160
+    rng = np.random.default_rng(S * 7 + k_top)
+    sc = rng.standard_normal((T, S)).astype(np.float32)
+    sc[1::4] = rng.integers(-3, 4, size=sc[1::4].shape).astype(np.float32)
+    seg = S // 8
+    sc[2::4, 3 * seg:4 * seg] += 50.0
+    sc[3] = 1.5
+    nv = rng.integers(k_top + 1, S + 1, size=T)
+    nv[:8] = [S, S, S, S, k_top + 1, k_top + 2, min(S, 2048), S - 1]
+    pos = (4 * nv - 1).astype(np.int32)
+    assert ds4x.topk_workspace_bytes(T, S, k_top) == 0
+    idx, cnt = ds4x.topk(torch.from_numpy(sc).cuda(), torch.from_numpy(pos).cuda(), S, 4, k_top)
+    torch.cuda.synchronize()
+    assert ds4x.device_status() == ds4x.OK
+    ref_idx, ref_cnt = oracle.topk(sc, pos, S, 4, k_top)
+    assert np.array_equal(cnt.cpu().numpy(), ref_cnt)
+    bad = np.nonzero(np.any(idx.cpu().numpy() != ref_idx, axis=1))[0]
+    assert bad.size == 0, f"tokens {bad[:8]} differ from the oracle"
+
+
 @pytest.mark.parametrize("case", ["boundary_overflow", "all_equal", "few_tokens"])
 def test_long_row_topk_exact(case):
     # long rows over many CTAs: a boundary bin with more rows than the candidate buffer (the last
