@@ -340,6 +340,16 @@ __device__ __forceinline__ uint32_t bin_of(uint32_t key, uint32_t kmin, uint32_t
   return __umulhi(key - kmin, mult);
 }
 
+// The multiplier of nb bins over `range` keys (range > nb): about nb * 2^32 / range, computed in
+// fp32 (a few instructions where the 64-bit integer quotient is a long routine) and lowered by a
+// relative 2^-20, well above the fp32 quotient's error (under 2^-22), so that it never exceeds
+// the exact quotient: bin = umulhi(key - min, mult) then stays below nb.  Any multiplier keeps the
+// bins monotone in the key, and every CTA computes the same value from the same range.
+__device__ __forceinline__ uint32_t bin_mult(uint64_t range, uint32_t nb) {
+  const float q = (float)nb * 4294967296.0f / (float)range;
+  return (uint32_t)(q * 0.999999f);
+}
+
 // Block-wide min and max of 32-bit keys.
 __device__ __forceinline__ void block_minmax32(uint32_t mn, uint32_t mx, Shared& sh, uint32_t* omin, uint32_t* omax) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -364,51 +374,49 @@ __device__ __forceinline__ void block_minmax32(uint32_t mn, uint32_t mx, Shared&
   *omax = b;
 }
 
-// One pass over a row staged in shared memory: thread t visits the 4-element vectors t, t+256, ...
-// (16-byte shared loads) and calls f(j, keys[4], valid4) with j = the vector's first element.
-template <class F>
-__device__ __forceinline__ void smem_row_pass(const float* srow, int n, F&& f) {
-  const int nv = (n + 3) >> 2;
-  for (int v = threadIdx.x; v < nv; v += kThreads) {
-    const float4 x = reinterpret_cast<const float4*>(srow)[v];
-    const int j = 4 * v;
-    const uint32_t k4[4] = {ordered_key(x.x), ordered_key(x.y), ordered_key(x.z), ordered_key(x.w)};
-    const bool v4[4] = {j < n, j + 1 < n, j + 2 < n, j + 3 < n};
-    f(j, k4, v4);
-  }
-}
-
 // Exact top-k of one visible score row (staged in shared memory) with the histogram path.
 // Returns false (having written nothing but shared memory) when every key is equal or the
 // boundary bin holds more rows than the candidate buffer (massive ties); the caller then runs
 // the streaming path.
-__device__ bool topk_row_hist(Shared& sh, uint32_t* bitmap, const float* srow, int n, int k_top, int32_t* out,
+__device__ bool topk_row_hist(Shared& sh, uint32_t* bitmap, float* srow, int n, int k_top, int32_t* out,
                               int32_t* count_out) {
   const int tid = threadIdx.x;
-  // pass A: key range
+  const int nv = (n + 3) >> 2;  // 4-row vectors (the staged row is padded to a whole vector)
+  // pass A: key range; the staged scores are replaced by their ordered keys, which the later
+  // passes read as they are (the streaming fallback reads the row from global memory)
+  uint4* skey = reinterpret_cast<uint4*>(srow);
   uint32_t mn = 0xFFFFFFFFu, mx = 0;
-  smem_row_pass(srow, n, [&](int, const uint32_t (&k4)[4], const bool (&v4)[4]) {
+  for (int v = tid; v < nv; v += kThreads) {
+    const float4 x = reinterpret_cast<const float4*>(srow)[v];
+    const uint4 k = make_uint4(ordered_key(x.x), ordered_key(x.y), ordered_key(x.z), ordered_key(x.w));
+    skey[v] = k;
+    const int j = 4 * v;
+    const uint32_t k4[4] = {k.x, k.y, k.z, k.w};
 #pragma unroll
     for (int c = 0; c < 4; ++c)
-      if (v4[c]) {
+      if (j + c < n) {
         mn = min(mn, k4[c]);
         mx = max(mx, k4[c]);
       }
-  });
+  }
   uint32_t kmin, kmax;
   block_minmax32(mn, mx, sh, &kmin, &kmax);
   if (kmin == kmax) return false;  // one value everywhere: every row ties
   const uint64_t range = static_cast<uint64_t>(kmax - kmin) + 1;
-  const uint64_t m64 = (static_cast<uint64_t>(kBins) << 32) / range;
-  const uint32_t mult = m64 > 0xFFFFFFFFull ? 0xFFFFFFFFu : static_cast<uint32_t>(m64);
+  // at most kBins key values: the capped multiplier 2^32 - 1 gives bin max(d - 1, 0), d = key - kmin,
+  // still monotone and below kBins
+  const uint32_t mult = range <= (uint64_t)kBins ? 0xFFFFFFFFu : bin_mult(range, kBins);
   // pass B: histogram
   for (int i = tid; i < kBins; i += kThreads) sh.bins[i] = 0;
   __syncthreads();
-  smem_row_pass(srow, n, [&](int, const uint32_t (&k4)[4], const bool (&v4)[4]) {
+  for (int v = tid; v < nv; v += kThreads) {
+    const uint4 k = skey[v];
+    const int j = 4 * v;
+    const uint32_t k4[4] = {k.x, k.y, k.z, k.w};
 #pragma unroll
     for (int c = 0; c < 4; ++c)
-      if (v4[c]) atomicAdd(&sh.bins[bin_of(k4[c], kmin, mult)], 1u);
-  });
+      if (j + c < n) atomicAdd(&sh.bins[bin_of(k4[c], kmin, mult)], 1u);
+  }
   __syncthreads();
   // boundary bin: thread i owns bins [kBins - 8(i+1), kBins - 8i), scanned from the top
   constexpr int kPer = kBins / kThreads;
@@ -439,7 +447,6 @@ __device__ bool topk_row_hist(Shared& sh, uint32_t* bitmap, const float* srow, i
   for (int i = tid; i < nw; i += kThreads) bitmap[i] = 0;
   if (tid == 0) sh.count = 0;
   __syncthreads();
-  const int nv = (n + 3) >> 2;
   const int nv_pad = (nv + kThreads - 1) / kThreads * kThreads;  // whole warps take part in append
   for (int v = tid; v < nv_pad; v += kThreads) {
     const int j = 4 * v;
@@ -447,11 +454,11 @@ __device__ bool topk_row_hist(Shared& sh, uint32_t* bitmap, const float* srow, i
     bool b4[4] = {false, false, false, false};
     uint32_t nib = 0;
     if (v < nv) {
-      const float4 x = reinterpret_cast<const float4*>(srow)[v];
-      k4[0] = ordered_key(x.x);
-      k4[1] = ordered_key(x.y);
-      k4[2] = ordered_key(x.z);
-      k4[3] = ordered_key(x.w);
+      const uint4 k = skey[v];
+      k4[0] = k.x;
+      k4[1] = k.y;
+      k4[2] = k.z;
+      k4[3] = k.w;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const bool valid = j + q < n;
@@ -463,7 +470,8 @@ __device__ bool topk_row_hist(Shared& sh, uint32_t* bitmap, const float* srow, i
 #pragma unroll
     for (int q = 0; q < 4; ++q) r4[q] = (uint32_t)(j + q);
     if (nib) atomicOr(&bitmap[j >> 5], nib << (j & 31));
-    append(sh, k4, r4, b4);
+    // the boundary bin holds few rows: most warps have none of them in a step and skip the ballots
+    if (__any_sync(0xffffffffu, b4[0] || b4[1] || b4[2] || b4[3])) append(sh, k4, r4, b4);
   }
   __syncthreads();
   // the boundary bin contributes its (k_top - above_b) best rows in the composite order
@@ -689,7 +697,7 @@ __global__ void __launch_bounds__(B) topk_reg_kernel(const KParams p) {
     }
     const uint64_t range = (uint64_t)(hi - lo) + 1u;
     const bool ident = range <= (uint64_t)NB;
-    const uint32_t mult = ident ? 0u : (uint32_t)(((uint64_t)NB << 32) / range);
+    const uint32_t mult = ident ? 0u : bin_mult(range, NB);
 #pragma unroll
     for (int i = 0; i < NPT; ++i)
       if ((cand >> i) & 1u) {
@@ -935,7 +943,7 @@ __global__ void __launch_bounds__(kThreads) long_hist_kernel(const KParams p) {
   const uint32_t kmin = block_min_u32(mn, red);
   const uint32_t kmax = block_max_u32(mx, red);
   const uint64_t range = (uint64_t)kmax - kmin + 1;
-  const uint32_t mult = range <= (uint64_t)kGBins ? 0u : (uint32_t)(((uint64_t)kGBins << 32) / range);
+  const uint32_t mult = range <= (uint64_t)kGBins ? 0u : bin_mult(range, kGBins);
   for (int i = threadIdx.x; i < kGBins; i += kThreads) sh_hist[i] = 0;
   __syncthreads();
 #pragma unroll
@@ -1181,7 +1189,7 @@ __global__ void __launch_bounds__(kThreads) long_coop_kernel(const KParams p) {
   const uint32_t kmin = block_min_u32(mn, red);
   const uint32_t kmax = block_max_u32(mx, red);
   const uint64_t range = (uint64_t)kmax - kmin + 1;
-  const uint32_t mult = range <= (uint64_t)kGBins ? 0u : (uint32_t)(((uint64_t)kGBins << 32) / range);
+  const uint32_t mult = range <= (uint64_t)kGBins ? 0u : bin_mult(range, kGBins);
   for (int i = threadIdx.x; i < kGBins; i += kThreads) sh_hist[i] = 0;
   __syncthreads();
 #pragma unroll
