@@ -1265,6 +1265,59 @@ __global__ void __launch_bounds__(kThreads) long_coop_kernel(const KParams p) {
   }
   if (!token_barrier(counter, 3u * P, p.status, 62)) return;
 
+  const int m_cand = (int)__ldcg(&ctl->ncand);  // the same value in every slice of the token
+  if (m_cand <= kThreads && P <= kThreads) {
+    // few boundary rows (the usual case): every slice ranks them itself (candidate j is in iff
+    // fewer than `need` candidates beat it), so each knows every slice's count without another
+    // barrier, adds its own winners to its words and writes its rows after the earlier slices'
+    pdl_trigger();  // this slice has passed its last barrier
+    __shared__ uint32_t add[kThreads];   // winners among the candidates, per slice
+    __shared__ uint32_t words[kSliceRows / 32];
+    const int need = p.k_top - (int)above;
+    add[threadIdx.x] = 0;
+    if (threadIdx.x < kSliceRows / 32) words[threadIdx.x] = 0;
+    for (int j = threadIdx.x; j < m_cand; j += kThreads) {
+      sh.key[j] = __ldcg(ckey + j);
+      sh.row[j] = __ldcg(crow + j);
+    }
+    __syncthreads();
+    if ((int)threadIdx.x < m_cand) {
+      const uint64_t mine = composite(sh.key[threadIdx.x], sh.row[threadIdx.x]);
+      int rank = 0;
+      for (int j = 0; j < m_cand; ++j) rank += composite(sh.key[j], sh.row[j]) > mine;
+      if (rank < need) {
+        const uint32_t r = sh.row[threadIdx.x];
+        atomicAdd(&add[r / kSliceRows], 1u);
+        if ((int)r >= lo && (int)r < hi) atomicOr(&words[(r - lo) >> 5], 1u << (r & 31));
+      }
+    }
+    __syncthreads();
+    uint32_t before = 0;
+    for (int i = threadIdx.x; i < part; i += kThreads) before += __ldcg(scnt + i) + add[i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+    if (lane == 0) red[warp] = before;
+    __syncthreads();
+    uint32_t offset = 0;
+    for (int w = 0; w < kWarps; ++w) offset += red[w];
+    if (part == 0 && cnt_out && threadIdx.x == 0) *cnt_out = p.k_top;
+    constexpr int kSliceWords = kSliceRows / 32;
+    const int w0 = lo >> 5;
+    const uint32_t word = (threadIdx.x < kSliceWords && lo + 32 * threadIdx.x < hi)
+                              ? (__ldcg(bm + w0 + threadIdx.x) | words[threadIdx.x])
+                              : 0u;
+    uint32_t total;
+    const uint32_t incl = block_scan((uint32_t)__popc(word), sh, &total);
+    uint32_t pos = offset + incl - (uint32_t)__popc(word);
+    uint32_t bits = word;
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1;
+      out[pos++] = (w0 + (int)threadIdx.x) * 32 + b;
+    }
+    return;
+  }
+
   // phase 4: slice 0 ranks the boundary bin's rows and adds the missing ones (or, when more than
   // kCandCap rows share the bin, ranks and emits the whole row itself)
   if (part == 0) {
