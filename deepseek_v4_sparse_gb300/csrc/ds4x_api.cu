@@ -150,21 +150,30 @@ int run_index_and_attend(const void* q, const void* w, const void* k, const int3
   const size_t score_bytes = round256((size_t)T * (size_t)S * sizeof(float));
   const size_t topk_bytes = S > 0 ? round256(topk_workspace_bytes(T, S, k_top)) : 0;
   int rc = DS4X_OK;
-  // the long-row top-k's barrier counters sit at the start of its scratch; the scorer zeroes them
+  // the long-row top-k's barrier counters sit at the start of its scratch; the scorer zeroes them.
+  // One token over a long row (a decode step): the scorer zeroes the token's whole top-k scratch and
+  // hands over the key range of the scores it wrote, so the top-k starts at its histogram phase.
   const bool zero_counters = S > 0 && topk_bytes > 0;
+  const int n_slots = S > 0 ? score_grid(T, H, S) : 0;
+  const bool range_mode = zero_counters && topk_range_mode(T, S, k_top, n_slots);
+  uint32_t* range_slots = range_mode ? reinterpret_cast<uint32_t*>(ws + score_bytes + topk_range_slots_offset(T, S))
+                                     : nullptr;
   if (S > 0) {
     // scores only for tokens that the shortcut does not cover; masked rows are never read
     ScoreArgs sa{q, w, k, positions, reinterpret_cast<float*>(ws), (int64_t)S, T, H, D, S, ratio, k_top, 0};
     if (zero_counters) {
       sa.zero_words = reinterpret_cast<uint32_t*>(ws + score_bytes);
-      sa.n_zero = T;
+      sa.n_zero = range_mode ? (int)topk_range_zero_words(T, S) : T;
     }
+    sa.range_slots = range_slots;
     rc = launch_score(sa, st);
   }
   if (rc == DS4X_OK) {
     TopkArgs ta{reinterpret_cast<float*>(ws), (int64_t)(S > 0 ? S : 1), positions, T, S, ratio, k_top, indices,
                 nullptr, S > 0 ? ws + score_bytes : nullptr, S > 0 ? workspace_bytes - score_bytes : 0};
     ta.counters_zeroed = zero_counters ? 1 : 0;
+    ta.range_slots = range_slots;
+    ta.n_range_slots = range_mode ? n_slots : 0;
     rc = launch_topk(ta, st);
   }
   if (rc == DS4X_OK) {

@@ -66,9 +66,12 @@ struct ScoreArgs {
   int write_masked;   // 1: write -inf on masked rows, including whole masked tiles
   uint32_t* zero_words = nullptr;  // fused path: words the kernel zeroes once the previous kernel is done
   int n_zero = 0;                  // (the top-k's barrier counters, so no memset sits between the launches)
+  uint32_t* range_slots = nullptr; // T = 1: per CTA, min and max ordered key of the visible scores it wrote
 };
 int launch_score(const ScoreArgs& a, cudaStream_t stream);
 bool score_shape_supported(int H, int D);
+// CTAs the scorer launches for T tokens of H heads over S rows (the range slots it writes).
+int score_grid(int T, int H, int S);
 
 struct TopkArgs {
   const float* scores;
@@ -80,9 +83,19 @@ struct TopkArgs {
   void* workspace;
   size_t workspace_bytes;
   int counters_zeroed = 0;  // 1: the workspace's barrier counters were zeroed by the kernel before (fused path)
+  // range mode (one token whose row the cooperative kernel splits): the scorer zeroed the token's
+  // scratch and wrote n_range_slots (min, max) pairs of ordered keys at range_slots
+  const uint32_t* range_slots = nullptr;
+  int n_range_slots = 0;
 };
 size_t topk_workspace_bytes(int T, int S, int k_top);
 int launch_topk(const TopkArgs& a, cudaStream_t stream);
+// Range mode applies (T = 1, the row split into slices, one cooperative launch, a scorer of at
+// most the supported number of CTAs): then the scorer zeroes the first topk_range_zero_words words
+// of the top-k scratch and writes its n_slots range slots at byte offset topk_range_slots_offset.
+bool topk_range_mode(int T, int S, int k_top, int n_slots);
+size_t topk_range_zero_words(int T, int S);
+size_t topk_range_slots_offset(int T, int S);
 
 // The raw sliding window joined to the pooled rows (window = 0 or L = 0: none): a token at p also
 // attends to kv_local row r for every position a = local_pos0 + r with p - window < a <= p.

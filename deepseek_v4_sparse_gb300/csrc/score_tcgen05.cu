@@ -80,6 +80,8 @@ struct Cfg {
   static_assert(D % 64 == 0, "D must be a multiple of 64");
   static_assert(NK >= 4 && SMEM <= kSmemBudget, "shared memory");
   static_assert(TMEM_COLS <= 512, "TMEM");
+  // barriers, the TMEM address and the per-warp key ranges fit the 512 bytes set aside for them
+  static_assert((2 * NK + 2 * NQ + 2 * NACC + 2 * kGroups) * 8 + 16 + 2 * kEpiWarps * 4 <= 512, "barrier area");
 };
 
 struct Params {
@@ -93,8 +95,9 @@ struct Params {
   int skip_k_top;
   int write_masked;
   int* status;
-  uint32_t* zero_words;  // zeroed by CTA 0 once the previous kernel is done
+  uint32_t* zero_words;  // zeroed (by all CTAs) once the previous kernel is done
   int n_zero;
+  uint32_t* range_slots;  // T = 1: [grid][2] min and max ordered key of the visible scores each CTA wrote
 };
 
 __device__ __forceinline__ int n_visible(const Params& p, int t) {
@@ -176,6 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* wdone = aempty + C::NACC;  // [epilogue group] its 4 warps are done with the group's w
   uint64_t* wready = wdone + kGroups;  // [epilogue group] the next token group's w is written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wready + kGroups);
+  uint32_t* red_s = tmem_slot + 4;  // [2][kEpiWarps] per-warp key range (range mode)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -210,8 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();  // everything above touched only this CTA's own resources
   pdl_trigger();
-  if (blockIdx.x == 0)
-    for (int i = threadIdx.x; i < p.n_zero; i += blockDim.x) p.zero_words[i] = 0u;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.n_zero; i += gridDim.x * blockDim.x) p.zero_words[i] = 0u;
 
   const long long beg = (long long)blockIdx.x * p.total_items / gridDim.x;
   const long long end = (long long)(blockIdx.x + 1) * p.total_items / gridDim.x;
@@ -373,6 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int cur_g = -1, rows = 0;
     uint32_t a_it = 0, gc = 0;  // gc: group changes so far (the w barriers' phase)
     int nvis[C::TOKW];
+    uint32_t kmn = 0xFFFFFFFFu, kmx = 0u;  // range mode: ordered keys of the visible scores written
     if (beg < end) prefetch((int)(beg / p.n_stiles));
     int g = (int)(beg / p.n_stiles), st = (int)(beg % p.n_stiles) - 1;
     GroupRowsAhead<C::TPT> ahead;
@@ -451,10 +455,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         unpack_f2(a23, x2, x3);
         const float acc = (x0 + x1) + (x2 + x3);
         if (t0 + j < p.T && row < p.S) p.scores[(int64_t)(t0 + j) * p.ld + row] = row < nvis[j] ? acc : -INFINITY;
+        if (row < nvis[j]) {  // the top-k's key order: larger score, larger key
+          const uint32_t u = __float_as_uint(acc);
+          const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+          kmn = min(kmn, key);
+          kmx = max(kmx, key);
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&aempty[ab]);
+    }
+    if (p.range_slots) {
+      // this CTA's key range: over the warp, then over the epilogue warps
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        kmn = min(kmn, __shfl_xor_sync(0xffffffffu, kmn, o));
+        kmx = max(kmx, __shfl_xor_sync(0xffffffffu, kmx, o));
+      }
+      if (lane == 0) {
+        red_s[e] = kmn;
+        red_s[kEpiWarps + e] = kmx;
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
+      if (e == 0 && lane == 0) {
+        uint32_t a = red_s[0], b = red_s[kEpiWarps];
+        for (int i = 1; i < kEpiWarps; ++i) {
+          a = min(a, red_s[i]);
+          b = max(b, red_s[kEpiWarps + i]);
+        }
+        p.range_slots[2 * blockIdx.x] = a;
+        p.range_slots[2 * blockIdx.x + 1] = b;
+      }
     }
   }
 
@@ -481,6 +513,12 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// One persistent CTA per SM, or one per work item when there are fewer.
+int grid_for(long long total_items) {
+  const int sms = device_sm_count();
+  return (int)(total_items < sms ? total_items : sms);
+}
+
 template <int H, int D, int TN>
 int launch_impl(const ScoreArgs& a, cudaStream_t stream) {
   using C = Cfg<H, D, TN>;
@@ -504,8 +542,8 @@ int launch_impl(const ScoreArgs& a, cudaStream_t stream) {
   p.status = device_status_ptr();
   p.zero_words = a.zero_words;
   p.n_zero = a.zero_words ? a.n_zero : 0;
-  const int sms = device_sm_count();
-  const int grid = (int)(p.total_items < sms ? p.total_items : sms);
+  p.range_slots = a.range_slots;
+  const int grid = grid_for(p.total_items);
   const cudaError_t e = launch_pdl(score_kernel<H, D, TN>, dim3(grid), dim3(kThreads), (size_t)C::SMEM, stream, tq, tk, p);
   count_launch();
   return e == cudaSuccess ? DS4X_OK : DS4X_ERR_CUDA;
@@ -520,6 +558,14 @@ int launch_shape(const ScoreArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+int score_grid(int T, int H, int S) {
+  if (T <= 0 || S <= 0 || H <= 0) return 0;
+  const int TN = (int64_t)T * H <= narrow_tile(H) ? narrow_tile(H) : kTileWide;  // as launch_shape chooses
+  const long long tpt = TN / H;
+  const long long n_groups = (T + tpt - 1) / tpt;
+  return grid_for(n_groups * ((S + kTileS - 1) / kTileS));
+}
 
 bool score_shape_supported(int H, int D) {
   return (H == 16 || H == 32 || H == 64 || H == 128) && (D == 64 || D == 128);

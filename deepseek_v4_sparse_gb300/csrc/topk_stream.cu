@@ -525,6 +525,10 @@ struct KParams {
   uint32_t* gbar;       // one-launch long-row mode: a barrier counter per token (zeroed before the launch)
   int nslice;           // long-row mode: CTAs per token
   int* status;
+  // one-launch long-row mode, one token: the key range comes as n_range_slots (min, max) pairs
+  // written by the scorer, which also zeroed the token's scratch (nullptr: the kernel does both)
+  const uint32_t* range_slots;
+  int n_range_slots;
 };
 
 // One CTA per token: the whole row.
@@ -807,8 +811,9 @@ struct LongCtl {
 };
 
 struct LongLayout {  // byte offsets inside one token's block of the workspace
-  size_t ctl, slots, scnt, hist, bitmap, ckey, crow, total;
+  size_t ctl, slots, scnt, hist, bitmap, ckey, crow, rslots, total;
 };
+constexpr int kMaxRangeSlots = 1024;  // scorer CTAs whose key ranges the one-token mode takes
 
 __host__ __device__ inline size_t align_up(size_t n, size_t a) { return (n + a - 1) / a * a; }
 
@@ -831,6 +836,8 @@ __host__ __device__ inline LongLayout long_layout(int S) {
   o += (size_t)kCandCap * sizeof(uint32_t);
   L.crow = o;
   o += (size_t)kCandCap * sizeof(uint32_t);
+  L.rslots = o;  // outside the zeroed part [ctl, bitmap end): the scorer writes it while others zero
+  o += (size_t)2 * kMaxRangeSlots * sizeof(uint32_t);
   L.total = align_up(o, 256);
   return L;
 }
@@ -1154,37 +1161,47 @@ __global__ void __launch_bounds__(kThreads) long_coop_kernel(const KParams p) {
   uint32_t* counter = p.gbar + t;
   const int W = (p.S + 31) / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // range mode: the scorer zeroed this token's scratch and wrote the key ranges of what it scored,
+  // so phase 1 and its grid barrier fall away (nb counts the grid barriers passed)
+  const bool given = p.range_slots != nullptr;
+  uint32_t nb = 0;
 
   // phase 1: zero this slice's share of the scratch; the slice's keys; their min and max
-  for (int i = part * kThreads + threadIdx.x; i < kGBins; i += P * kThreads) hist[i] = 0;
-  for (int i = part * kThreads + threadIdx.x; i < W; i += P * kThreads) bm[i] = 0;
-  if (part == 0 && threadIdx.x < (int)(sizeof(LongCtl) / 4)) reinterpret_cast<uint32_t*>(ctl)[threadIdx.x] = 0;
+  if (!given) {
+    for (int i = part * kThreads + threadIdx.x; i < kGBins; i += P * kThreads) hist[i] = 0;
+    for (int i = part * kThreads + threadIdx.x; i < W; i += P * kThreads) bm[i] = 0;
+    if (part == 0 && threadIdx.x < (int)(sizeof(LongCtl) / 4)) reinterpret_cast<uint32_t*>(ctl)[threadIdx.x] = 0;
+  }
   const int lo = part * kSliceRows, hi = min(n, lo + kSliceRows);
   const float* row = p.scores + (int64_t)t * p.ld;
   uint32_t k[kSlicePer];
   bool v[kSlicePer];
   load_slice(row, lo, hi, k, v);
   uint32_t mn = 0xFFFFFFFFu, mx = 0;
+  const uint32_t* rs = given ? p.range_slots : slots;
+  const int nrs = given ? p.n_range_slots : P;
+  if (!given) {
 #pragma unroll
-  for (int i = 0; i < kSlicePer; ++i)
-    if (v[i]) {
-      mn = min(mn, k[i]);
-      mx = max(mx, k[i]);
+    for (int i = 0; i < kSlicePer; ++i)
+      if (v[i]) {
+        mn = min(mn, k[i]);
+        mx = max(mx, k[i]);
+      }
+    mn = block_min_u32(mn, red);
+    mx = block_max_u32(mx, red);
+    if (threadIdx.x == 0) {
+      slots[2 * part] = mn;
+      slots[2 * part + 1] = mx;
     }
-  mn = block_min_u32(mn, red);
-  mx = block_max_u32(mx, red);
-  if (threadIdx.x == 0) {
-    slots[2 * part] = mn;
-    slots[2 * part + 1] = mx;
+    if (!token_barrier(counter, ++nb * (uint32_t)P, p.status, 60)) return;
   }
-  if (!token_barrier(counter, (uint32_t)P, p.status, 60)) return;
 
   // phase 2: the row's key range from the slots; histogram of the slice into the token's
   mn = 0xFFFFFFFFu;
   mx = 0;
-  for (int i = threadIdx.x; i < P; i += kThreads) {
-    mn = min(mn, __ldcg(slots + 2 * i));
-    mx = max(mx, __ldcg(slots + 2 * i + 1));
+  for (int i = threadIdx.x; i < nrs; i += kThreads) {
+    mn = min(mn, __ldcg(rs + 2 * i));
+    mx = max(mx, __ldcg(rs + 2 * i + 1));
   }
   const uint32_t kmin = block_min_u32(mn, red);
   const uint32_t kmax = block_max_u32(mx, red);
@@ -1198,7 +1215,7 @@ __global__ void __launch_bounds__(kThreads) long_coop_kernel(const KParams p) {
   __syncthreads();
   for (int i = threadIdx.x; i < kGBins; i += kThreads)
     if (sh_hist[i]) atomicAdd(&hist[i], sh_hist[i]);
-  if (!token_barrier(counter, 2u * P, p.status, 61)) return;
+  if (!token_barrier(counter, ++nb * (uint32_t)P, p.status, 61)) return;
 
   // phase 3: every slice finds the boundary bin b* from the token's histogram, writes its words
   // of the bitmap (rows in bins above b*) and collects its rows in b*
@@ -1263,7 +1280,7 @@ __global__ void __launch_bounds__(kThreads) long_coop_kernel(const KParams p) {
     for (int w = 0; w < kWarps; ++w) sum += red[w];
     scnt[part] = sum;
   }
-  if (!token_barrier(counter, 3u * P, p.status, 62)) return;
+  if (!token_barrier(counter, ++nb * (uint32_t)P, p.status, 62)) return;
 
   const int m_cand = (int)__ldcg(&ctl->ncand);  // the same value in every slice of the token
   if (m_cand <= kThreads && P <= kThreads) {
@@ -1357,7 +1374,7 @@ __global__ void __launch_bounds__(kThreads) long_coop_kernel(const KParams p) {
       if (cnt_out && threadIdx.x == 0) *cnt_out = p.k_top;
     }
   }
-  if (!token_barrier(counter, 4u * P, p.status, 63)) return;
+  if (!token_barrier(counter, ++nb * (uint32_t)P, p.status, 63)) return;
   // the next kernel may start its prologue now: every slice has passed its last barrier, so early
   // CTAs of that kernel can no longer keep one of these from being resident
   pdl_trigger();
@@ -1514,6 +1531,22 @@ size_t topk_workspace_bytes(int T, int S, int k_top) {
   return long_counters_bytes(T) + (size_t)T * long_layout(S).total;
 }
 
+bool topk_range_mode(int T, int S, int k_top, int n_slots) {
+  if (T != 1 || long_slices(T, S) <= 1 || n_slots <= 0 || n_slots > kMaxRangeSlots) return false;
+  const size_t msmem = bitmap_smem(S);
+  if (msmem > 220 * 1024 || set_smem_attrs(row_kernel_smem(S), msmem) != cudaSuccess) return false;
+  (void)k_top;
+  return long_coop_fits(T, long_slices(T, S), msmem);
+}
+
+// [barrier counters | the token's control block, slots, counts, histogram and bitmap]
+size_t topk_range_zero_words(int T, int S) {
+  const LongLayout L = long_layout(S);
+  return (long_counters_bytes(T) + L.bitmap + (size_t)((S + 31) / 32) * sizeof(uint32_t)) / sizeof(uint32_t);
+}
+
+size_t topk_range_slots_offset(int T, int S) { return long_counters_bytes(T) + long_layout(S).rslots; }
+
 int launch_topk(const TopkArgs& a, cudaStream_t stream) {
   if (a.T == 0) return DS4X_OK;
   const size_t smem = row_kernel_smem(a.S);
@@ -1534,6 +1567,8 @@ int launch_topk(const TopkArgs& a, cudaStream_t stream) {
   p.long_ws = nullptr;
   p.gbar = nullptr;
   p.status = device_status_ptr();
+  p.range_slots = nullptr;
+  p.n_range_slots = 0;
   if (p.nslice <= 1) {
     if (launch_one_cta_per_token(p, smem, stream) != cudaSuccess) return DS4X_ERR_CUDA;
     count_launch();
@@ -1542,9 +1577,12 @@ int launch_topk(const TopkArgs& a, cudaStream_t stream) {
     if (a.workspace == nullptr || a.workspace_bytes < need) return DS4X_ERR_WORKSPACE;
     p.gbar = static_cast<uint32_t*>(a.workspace);
     p.long_ws = static_cast<uint8_t*>(a.workspace) + long_counters_bytes(a.T);
-    const cudaError_t e = long_coop_fits(a.T, p.nslice, msmem)
-                              ? launch_long_coop(p, stream, msmem, a.counters_zeroed != 0)
-                              : launch_long(p, stream, msmem);
+    const bool coop = long_coop_fits(a.T, p.nslice, msmem);
+    if (coop && a.T == 1 && a.range_slots && a.n_range_slots > 0 && a.n_range_slots <= kMaxRangeSlots) {
+      p.range_slots = a.range_slots;  // the caller's scorer zeroed the scratch (counters_zeroed too)
+      p.n_range_slots = a.n_range_slots;
+    }
+    const cudaError_t e = coop ? launch_long_coop(p, stream, msmem, a.counters_zeroed != 0) : launch_long(p, stream, msmem);
     if (e != cudaSuccess) return DS4X_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? DS4X_OK : DS4X_ERR_CUDA;
@@ -1622,6 +1660,8 @@ extern "C" int ds4x_topk_static_scratch(const float* scores, int64_t ld_scores, 
   p.long_ws = nullptr;
   p.gbar = nullptr;
   p.status = device_status_ptr();
+  p.range_slots = nullptr;
+  p.n_range_slots = 0;
   cudaError_t e;
   if (p.nslice <= 1) {
     e = launch_one_cta_per_token(p, smem, st);
