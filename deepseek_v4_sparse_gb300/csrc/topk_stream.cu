@@ -843,9 +843,13 @@ __host__ __device__ inline LongLayout long_layout(int S) {
 }
 
 // bin of an ordered key over [kmin, kmax]: direct when the range has at most kGBins values
-// (mult == 0), else umulhi(key - kmin, floor(kGBins 2^32 / range)); non-decreasing in the key
+// (mult == 0), else umulhi(key - kmin, floor(kGBins 2^32 / range)); non-decreasing in the key.
+// A key outside [kmin, kmax] lands in an end bin rather than past the table: the range can come
+// from another kernel (the scorer's key ranges), and scores that do not match it (a buffer
+// rewritten in between) must not index shared memory out of bounds.
 __device__ __forceinline__ uint32_t long_bin(uint32_t key, uint32_t kmin, uint32_t mult) {
-  return mult == 0 ? key - kmin : __umulhi(key - kmin, mult);
+  const uint32_t d = key > kmin ? key - kmin : 0u;
+  return min(mult == 0 ? d : __umulhi(d, mult), (uint32_t)(kGBins - 1));
 }
 
 // Block-wide reduction helpers on a few words of static shared memory.
