@@ -31,13 +31,25 @@ def _gpu(x, g, fx, fg, bias, ratio, dtype):
     return host16(rows), host16(fxo), host16(fgo)
 
 
-def check_rows(got, ref, dtype):
-    """fp32 pooling on the GPU, fp64 in the oracle, each rounded once: at most one unit in the
-    last place of the 16-bit result apart."""
+def block_absmax(x, fx, ratio, dtype):
+    """max_i |x_i[d]| over each block's positions (frontier rows first), [n_out, D] float64."""
+    seq = np.concatenate([fx, x]) if fx is not None and fx.shape[0] else x
+    n_out = seq.shape[0] // ratio
+    v = np.abs(synth.bits_to_f32(seq[:n_out * ratio], dtype).astype(np.float64))
+    return v.reshape(n_out, ratio, -1).max(axis=1)
+
+
+def check_rows(got, ref, dtype, xmax, ratio):
+    """fp32 pooling on the GPU, fp64 in the oracle, each rounded once to the 16-bit type.  The
+    GPU's fp32 value of a row differs from the exact one by the rounding of its weighted sum
+    (up to ratio * 2^-24 of the largest term) and of its weights (gate sum and product, the
+    ex2.approx result: about 10 * 2^-24 relative each), i.e. by at most (ratio + 32) * 2^-24 *
+    max_i |x_i| when the block's terms cancel.  The two roundings to 16 bits add one unit in the
+    last place (2^-7 / 2^-10 of |result| at most, 2^-24 below the normal range)."""
     g = synth.bits_to_f32(got, dtype).astype(np.float64)
     r = synth.bits_to_f32(ref, dtype).astype(np.float64)
     ulp = 2.0 ** (-7 if dtype == "bf16" else -10)
-    err = np.abs(g - r) - (ulp * np.abs(r) + 2.0 ** -24)
+    err = np.abs(g - r) - (ulp * np.abs(r) + 2.0 ** -24 + (ratio + 32) * 2.0 ** -24 * xmax)
     assert err.max(initial=-1) <= 0, f"compressor error {np.abs(g - r).max()}"
     # almost every row matches bit for bit; a flip needs the fp32 result within ~1e-7 of a midpoint
     assert np.mean(got == ref) > 0.99
@@ -60,7 +72,7 @@ def test_compress_vs_oracle(dtype, D, ratio, T, f):
     rrows, rfx, rfg = oracle.compress(x, g, bias, dtype, ratio, fx if f else None, fg if f else None)
     assert rows.shape == rrows.shape and fxo.shape == rfx.shape
     if rows.size:
-        check_rows(rows, rrows, dtype)
+        check_rows(rows, rrows, dtype, block_absmax(x, fx, ratio, dtype), ratio)
     assert np.array_equal(fxo, rfx) and np.array_equal(fgo, rfg)
 
 
@@ -104,6 +116,49 @@ def test_compress_streaming_batch_full_size():
     rows, fxo, fgo = _gpu(x, g, fx, fg, bias, ratio, "bf16")
     rrows, rfx, rfg = oracle.compress(x, g, bias, "bf16", ratio, fx, fg)
     assert rows.shape == rrows.shape == ((T + f) // ratio, D)
-    check_rows(rows, rrows, "bf16")
+    check_rows(rows, rrows, "bf16", block_absmax(x, fx, ratio, "bf16"), ratio)
     assert np.array_equal(fxo, rfx) and np.array_equal(fgo, rfg)
 
+
+
+def _streamed(n_out, f, D, ratio):
+    """Whether a call takes the streamed path: ratio <= 4, D a power of two <= 512, and at least
+    two stages (32 KB of x rows each) of whole blocks for every SM after the frontier's block."""
+    if ratio not in (1, 2, 4) or D > 512 or D & (D - 1):
+        return False
+    bps = (16384 // D) // ratio
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return n_out - (1 if f else 0) >= 2 * sms * bps
+
+
+@pytest.mark.parametrize("dtype,D,ratio,T,f", [
+    ("bf16", 512, 4, 20003, 3),   # a held-over block 0, a ragged last stage, a partial block left over
+    ("f16", 128, 4, 40001, 1),    # the indexer's k rows: 128-position stages
+    ("bf16", 512, 2, 12001, 1),
+    ("bf16", 256, 1, 20000, 0),   # ratio 1: every position is a row
+    ("f16", 8, 4, 640002, 2),     # one 8-channel group a row: 2048-position stages
+])
+def test_compress_streamed_batches_vs_oracle(dtype, D, ratio, T, f):
+    assert _streamed((T + f) // ratio, f, D, ratio)
+    x, g, fx, fg, bias = synth.compress_inputs(5, f"cmp_stream_{dtype}_{D}_{ratio}_{T}_{f}", T, D, ratio, dtype, f)
+    rows, fxo, fgo = _gpu(x, g, fx, fg, bias, ratio, dtype)
+    rrows, rfx, rfg = oracle.compress(x, g, bias, dtype, ratio, fx if f else None, fg if f else None)
+    assert rows.shape == rrows.shape and fxo.shape == rfx.shape
+    check_rows(rows, rrows, dtype, block_absmax(x, fx, ratio, dtype), ratio)
+    assert np.array_equal(fxo, rfx) and np.array_equal(fgo, rfg)
+
+
+def test_compress_streamed_and_one_pass_paths_agree_bit_for_bit():
+    # a long batch split so that the middle call streams and the short ones take the one-pass
+    # kernel: every block comes out the same bits as from the one streamed call
+    D, ratio, N = 512, 4, 20000
+    assert _streamed(N // ratio, 0, D, ratio) and not _streamed(249, 1, D, ratio)
+    x, g, _, _, bias = synth.compress_inputs(6, "cmp_paths", N, D, ratio, "bf16")
+    whole, wfx, wfg = _gpu(x, g, x[:0], g[:0], bias, ratio, "bf16")
+    parts, fx, fg = [], x[:0], g[:0]
+    for a, b in ((0, 5), (5, 19005), (19005, N)):
+        r, fx, fg = _gpu(x[a:b], g[a:b], fx, fg, bias, ratio, "bf16")
+        parts.append(r)
+    assert _streamed((19005 - 5 + 1) // ratio, 1, D, ratio)
+    assert np.array_equal(np.concatenate(parts), whole)
+    assert np.array_equal(fx, wfx) and np.array_equal(fg, wfg)
