@@ -1286,35 +1286,42 @@ __global__ void __launch_bounds__(kThreads) long_coop_kernel(const KParams p) {
   }
   if (!token_barrier(counter, ++nb * (uint32_t)P, p.status, 62)) return;
 
-  const int m_cand = (int)__ldcg(&ctl->ncand);  // the same value in every slice of the token
+  // every value the fast path reads from L2, loaded at once (one round trip instead of four):
+  // the candidate count (the same in every slice of the token), the candidates as far as the
+  // fast path takes them (kThreads <= kCandCap: the loads stay inside the buffer, entries past the
+  // count go unused), the slices' counts and this slice's bitmap words
+  constexpr int kSliceWords = kSliceRows / 32;
+  const int w0 = lo >> 5;
+  const int m_cand = (int)__ldcg(&ctl->ncand);
+  const uint32_t my_key = __ldcg(ckey + threadIdx.x), my_row = __ldcg(crow + threadIdx.x);
+  const uint32_t my_scnt = (int)threadIdx.x < P ? __ldcg(scnt + threadIdx.x) : 0u;
+  const bool my_word_in = threadIdx.x < kSliceWords && lo + 32 * (int)threadIdx.x < hi;
+  const uint32_t my_word = my_word_in ? __ldcg(bm + w0 + threadIdx.x) : 0u;
   if (m_cand <= kThreads && P <= kThreads) {
     // few boundary rows (the usual case): every slice ranks them itself (candidate j is in iff
     // fewer than `need` candidates beat it), so each knows every slice's count without another
     // barrier, adds its own winners to its words and writes its rows after the earlier slices'
     pdl_trigger();  // this slice has passed its last barrier
+    static_assert(kThreads <= kCandCap, "speculative candidate loads");
+    __shared__ uint64_t cand[kThreads];  // the candidates' composites
     __shared__ uint32_t add[kThreads];   // winners among the candidates, per slice
-    __shared__ uint32_t words[kSliceRows / 32];
+    __shared__ uint32_t words[kSliceWords];
     const int need = p.k_top - (int)above;
     add[threadIdx.x] = 0;
-    if (threadIdx.x < kSliceRows / 32) words[threadIdx.x] = 0;
-    for (int j = threadIdx.x; j < m_cand; j += kThreads) {
-      sh.key[j] = __ldcg(ckey + j);
-      sh.row[j] = __ldcg(crow + j);
-    }
+    if (threadIdx.x < kSliceWords) words[threadIdx.x] = 0;
+    const uint64_t mine = composite(my_key, my_row);
+    if ((int)threadIdx.x < m_cand) cand[threadIdx.x] = mine;
     __syncthreads();
     if ((int)threadIdx.x < m_cand) {
-      const uint64_t mine = composite(sh.key[threadIdx.x], sh.row[threadIdx.x]);
       int rank = 0;
-      for (int j = 0; j < m_cand; ++j) rank += composite(sh.key[j], sh.row[j]) > mine;
+      for (int j = 0; j < m_cand; ++j) rank += cand[j] > mine;
       if (rank < need) {
-        const uint32_t r = sh.row[threadIdx.x];
-        atomicAdd(&add[r / kSliceRows], 1u);
-        if ((int)r >= lo && (int)r < hi) atomicOr(&words[(r - lo) >> 5], 1u << (r & 31));
+        atomicAdd(&add[my_row / kSliceRows], 1u);
+        if ((int)my_row >= lo && (int)my_row < hi) atomicOr(&words[(my_row - lo) >> 5], 1u << (my_row & 31));
       }
     }
     __syncthreads();
-    uint32_t before = 0;
-    for (int i = threadIdx.x; i < part; i += kThreads) before += __ldcg(scnt + i) + add[i];
+    uint32_t before = (int)threadIdx.x < part ? my_scnt + add[threadIdx.x] : 0u;  // P <= kThreads
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
     if (lane == 0) red[warp] = before;
@@ -1322,11 +1329,7 @@ __global__ void __launch_bounds__(kThreads) long_coop_kernel(const KParams p) {
     uint32_t offset = 0;
     for (int w = 0; w < kWarps; ++w) offset += red[w];
     if (part == 0 && cnt_out && threadIdx.x == 0) *cnt_out = p.k_top;
-    constexpr int kSliceWords = kSliceRows / 32;
-    const int w0 = lo >> 5;
-    const uint32_t word = (threadIdx.x < kSliceWords && lo + 32 * threadIdx.x < hi)
-                              ? (__ldcg(bm + w0 + threadIdx.x) | words[threadIdx.x])
-                              : 0u;
+    const uint32_t word = my_word_in ? (my_word | words[threadIdx.x]) : 0u;
     uint32_t total;
     const uint32_t incl = block_scan((uint32_t)__popc(word), sh, &total);
     uint32_t pos = offset + incl - (uint32_t)__popc(word);
@@ -1394,9 +1397,7 @@ __global__ void __launch_bounds__(kThreads) long_coop_kernel(const KParams p) {
   __syncthreads();
   uint32_t offset = 0;
   for (int w = 0; w < kWarps; ++w) offset += red[w];
-  constexpr int kSliceWords = kSliceRows / 32;
-  const int w0 = lo >> 5;
-  const uint32_t word = (threadIdx.x < kSliceWords && lo + 32 * threadIdx.x < hi) ? __ldcg(bm + w0 + threadIdx.x) : 0u;
+  const uint32_t word = my_word_in ? __ldcg(bm + w0 + threadIdx.x) : 0u;  // phase 4 may have added bits
   uint32_t total;
   const uint32_t incl = block_scan((uint32_t)__popc(word), sh, &total);
   uint32_t pos = offset + incl - (uint32_t)__popc(word);
