@@ -141,6 +141,27 @@ def _stream(stream):
     return ctypes.c_void_p(int(stream))
 
 
+# Buffers of host-entry calls whose work may still be running: the copies read and write host memory
+# asynchronously, and PyTorch recycles a freed page-locked block (or a device block of another
+# stream) without knowing about copies it did not issue, so each call's tensors stay referenced
+# until an event recorded after it on its stream has completed.
+_inflight = []
+
+
+def _keep_until_done(stream, tensors):
+    torch = _torch()
+    if stream is None:
+        s = torch.cuda.current_stream()
+    elif isinstance(stream, torch.cuda.Stream):
+        s = stream
+    else:
+        s = torch.cuda.ExternalStream(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    ev = torch.cuda.Event()
+    ev.record(s)
+    _inflight[:] = [(e, t) for (e, t) in _inflight if not e.query()]
+    _inflight.append((ev, tuple(x for x in tensors if x is not None)))
+
+
 def _kv_dtype(t) -> int:
     torch = _torch()
     if t.dtype == torch.float16:
@@ -282,8 +303,9 @@ def index_and_attend_host(q, w, k, positions, q_attn, kv, ratio: int, k_top: int
                           scale: float | None = None, n_chunks: int = 0, indices=None, out=None, lse=None,
                           device_buffer=None, want_lse: bool = True, device=None, stream=None):
     """The whole path on host (CPU) tensors: copies in, computes, copies out, overlapped by sub-chunks
-    of tokens.  Outputs are page-locked CPU tensors, valid once `stream` is synchronised.
-    Returns (indices, out, lse)."""
+    of tokens.  Outputs are page-locked CPU tensors, valid once `stream` is synchronised.  The copies
+    run after the call returns: every tensor passed or created here stays referenced until the
+    call's work on `stream` is done.  Returns (indices, out, lse)."""
     torch = _torch()
     dt = _kv_dtype(q_attn)
     T, H, D = q.shape
@@ -306,6 +328,7 @@ def index_and_attend_host(q, w, k, positions, q_attn, kv, ratio: int, k_top: int
         H, D, S, ratio, k_top, Hq, Dkv, scale, _host_ptr(indices), _host_ptr(out), _host_ptr(lse), n_chunks,
         _ptr(device_buffer), dbytes, _stream(stream))
     _check("ds4x_index_and_attend_host", rc)
+    _keep_until_done(stream, (q, w, k, positions, q_attn, kv, indices, out, lse, device_buffer))
     return indices, out, lse
 
 
@@ -404,6 +427,7 @@ def index_and_attend_local_host(q, w, k, positions, q_attn, kv, kv_local, ratio:
         _host_ptr(kv_local), dt, T, H, D, S, ratio, k_top, Hq, Dkv, local_pos0, L, window, scale,
         _host_ptr(indices), _host_ptr(out), _host_ptr(lse), n_chunks, _ptr(device_buffer), dbytes, _stream(stream))
     _check("ds4x_index_and_attend_local_host", rc)
+    _keep_until_done(stream, (q, w, k, positions, q_attn, kv, kv_local, indices, out, lse, device_buffer))
     return indices, out, lse
 
 

@@ -87,7 +87,8 @@ struct Params {
   uint16_t* out;
   float* lse;
   int* status;
-  float* part_o;   // split mode: per item, sum_j 2^(x_j - m) kv_j  [items, 64, 512] fp32 (unnormalized)
+  uint16_t* part;  // split mode: per item, sum_j 2^(x_j - m) kv_j / l  [items, 64, 512] in the kv dtype
+                   // (a convex combination of kv rows: it cannot leave the dtype's range)
   float* part_ml;  // split mode: per item, m [64] then l [64] (m in log2 units of the scaled logits)
   int T, S, k_top, nchunks;
   int npc;                      // chunks [0, npc) hold pooled rows, [npc, nchunks) the window's
@@ -629,7 +630,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (p.lse) p.lse[(int64_t)t * kHq + hh] = l > 0.f ? (lrow[kHq + hh] + log2f(l)) * 0.69314718055994531f : -INFINITY;
         }
       }
-      uint32_t* orow = reinterpret_cast<uint32_t*>(p.out + (int64_t)t * kHq * kDkv);
+      // an item of a split token writes its normalized part, in the output's layout and dtype
+      uint32_t* orow = reinterpret_cast<uint32_t*>(p.nsplit > 1 ? p.part + (int64_t)it * kHq * kDkv
+                                                                 : p.out + (int64_t)t * kHq * kDkv);
 #pragma unroll 1
       for (int db = 0; db < kPairs; ++db) {
         const int os = oslot(tok_i, db);
@@ -652,12 +655,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&oempty[os]);
-        if (p.nsplit > 1) {  // split item: unnormalized fp32 sums, merged by the combine kernel
-          float* po = p.part_o + (int64_t)it * kHq * kDkv + db * 128 + quad * 32 + lane;
-#pragma unroll
-          for (int h = 0; h < kHq; ++h) po[h * kDkv] = v[h];
-          continue;
-        }
         const int d_even = db * 128 + quad * 32 + (lane & ~1);
 #pragma unroll
         for (int h0 = 0; h0 < kHq; h0 += 2) {
@@ -706,10 +703,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Merge of a token's split items (one block per (token, head), 4 dims a thread): item i holds
-// O_i = sum_j 2^(x_j - m_i) kv_j and l_i = sum_j 2^(x_j - m_i) over its rows, so
-//   out = sum_i 2^(m_i - M) O_i / sum_i 2^(m_i - M) l_i,  M = max_i m_i,  lse = ln 2 (M + log2 L).
+// P_i = O_i / l_i, O_i = sum_j 2^(x_j - m_i) kv_j and l_i = sum_j 2^(x_j - m_i) over its rows, so
+//   out = sum_i 2^(m_i - M) l_i P_i / L,  L = sum_i 2^(m_i - M) l_i,  M = max_i m_i,  lse = ln 2 (M + log2 L).
 template <bool kBf16>
-__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_o,
+__device__ __forceinline__ float4 load4_16(const uint16_t* src) {
+  const uint2 u = *reinterpret_cast<const uint2*>(src);
+  if constexpr (kBf16) {
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x), b = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+    return make_float4(__low2float(a), __high2float(a), __low2float(b), __high2float(b));
+  } else {
+    const __half2 a = *reinterpret_cast<const __half2*>(&u.x), b = *reinterpret_cast<const __half2*>(&u.y);
+    return make_float4(__low2float(a), __high2float(a), __low2float(b), __high2float(b));
+  }
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict__ part,
                                                       const float* __restrict__ part_ml, int nsplit,
                                                       uint16_t* __restrict__ out, float* __restrict__ lse) {
   pdl_wait();
@@ -727,8 +736,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
     if (i < nsplit) {
       m[i] = ml[i * 2 * kHq + h];
       l[i] = ml[i * 2 * kHq + kHq + h];
-      o[i] = *reinterpret_cast<const float4*>(part_o + (((int64_t)t * nsplit + i) * kHq + h) * kDkv +
-                                              4 * threadIdx.x);
+      o[i] = load4_16<kBf16>(part + (((int64_t)t * nsplit + i) * kHq + h) * kDkv + 4 * threadIdx.x);
     }
   }
   float mx = -INFINITY;
@@ -738,8 +746,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int i = 0; i < kMaxSplit; ++i) {
-    const float wgt = (m[i] == -INFINITY) ? 0.f : exp2f(m[i] - mx);
-    L += wgt * l[i];
+    const float wgt = (m[i] == -INFINITY) ? 0.f : exp2f(m[i] - mx) * l[i];
+    L += wgt;
     acc.x += wgt * o[i].x;
     acc.y += wgt * o[i].y;
     acc.z += wgt * o[i].z;
@@ -772,7 +780,7 @@ void split_plan(int T, int nch, int sms, int& nsplit, int& cps) {
 
 size_t partial_bytes_for(int T, int nsplit) {
   if (nsplit <= 1) return 0;
-  return (size_t)T * nsplit * ((size_t)kHq * kDkv * 4 + 2 * kHq * 4);
+  return (size_t)T * nsplit * ((size_t)kHq * kDkv * 2 + 2 * kHq * 4);
 }
 
 
@@ -816,7 +824,7 @@ int launch_impl(const AttnArgs& a, cudaStream_t stream) {
   const int sms = device_sm_count();
   p.nsplit = 1;
   p.cps = p.nchunks;
-  p.part_o = nullptr;
+  p.part = nullptr;
   p.part_ml = nullptr;
   if (a.partial) {
     int ns, cps;
@@ -825,8 +833,8 @@ int launch_impl(const AttnArgs& a, cudaStream_t stream) {
     if (ns > 1 && a.partial_bytes >= need) {
       p.nsplit = ns;
       p.cps = cps;
-      p.part_o = static_cast<float*>(a.partial);
-      p.part_ml = p.part_o + (size_t)a.T * ns * kHq * kDkv;
+      p.part = static_cast<uint16_t*>(a.partial);
+      p.part_ml = reinterpret_cast<float*>(p.part + (size_t)a.T * ns * kHq * kDkv);
     }
   }
   p.items = a.T * p.nsplit;
@@ -836,7 +844,7 @@ int launch_impl(const AttnArgs& a, cudaStream_t stream) {
     return DS4X_ERR_CUDA;
   count_launch();
   if (p.nsplit > 1) {
-    if (launch_pdl(combine_kernel<kBf16>, dim3(a.T * kHq), dim3(kDkv / 4), 0, stream, p.part_o, p.part_ml, p.nsplit,
+    if (launch_pdl(combine_kernel<kBf16>, dim3(a.T * kHq), dim3(kDkv / 4), 0, stream, p.part, p.part_ml, p.nsplit,
                    static_cast<uint16_t*>(a.out), a.lse) != cudaSuccess)
       return DS4X_ERR_CUDA;
     count_launch();

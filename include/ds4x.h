@@ -197,7 +197,8 @@ size_t ds4x_workspace_bytes(int32_t T, int32_t S, int32_t k_top);
  *   Ordering: the copies start after all work enqueued on `stream` before the call; on return
  *   everything is enqueued and `stream` waits for the last copy out, so a synchronisation of
  *   `stream` (or any work enqueued on it later) sees the outputs in host memory.  The host
- *   buffers must not be touched until then.
+ *   buffers and device_buffer must stay allocated and untouched until then (the copies run after
+ *   the call returns).
  *   Errors: as ds4x_index_and_attend; DS4X_ERR_WORKSPACE when device_bytes is too small,
  *   DS4X_ERR_INVALID for NULL or misaligned pointers or n_chunks < 0.
  * ------------------------------------------------------------------------- */
