@@ -876,6 +876,29 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* red) {
   return r;
 }
 
+// Block-wide min and max together (two barriers; red_mn / red_mx stay unwritten until every
+// thread has passed a later barrier).
+__device__ __forceinline__ void block_minmax_u32(uint32_t& mn, uint32_t& mx, uint32_t* red_mn, uint32_t* red_mx) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) {
+    red_mn[threadIdx.x >> 5] = mn;
+    red_mx[threadIdx.x >> 5] = mx;
+  }
+  __syncthreads();
+  mn = red_mn[0];
+  mx = red_mx[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) {
+    mn = min(mn, red_mn[w]);
+    mx = max(mx, red_mx[w]);
+  }
+}
+
 // the thread's rows lo + i * kThreads + threadIdx.x of the slice as ordered keys (all loads issued
 // before any is used); rows at or past hi are flagged invalid
 __device__ __forceinline__ void load_slice(const float* row, int lo, int hi, uint32_t (&k)[kSlicePer],
@@ -1144,6 +1167,7 @@ __global__ void __launch_bounds__(kThreads) long_coop_kernel(const KParams p) {
   uint32_t* sbm = reinterpret_cast<uint32_t*>(smem_raw + sizeof(Shared));  // whole-row fallback only
   __shared__ uint32_t sh_hist[kGBins];
   __shared__ uint32_t red[kWarps];
+  __shared__ uint32_t red2[kWarps];
   __shared__ uint32_t sh_b[3];
   const int t = blockIdx.y, part = blockIdx.x, P = gridDim.x;
   const int n = n_visible(p.positions, t, p.ratio, p.S);
@@ -1178,12 +1202,20 @@ __global__ void __launch_bounds__(kThreads) long_coop_kernel(const KParams p) {
   }
   const int lo = part * kSliceRows, hi = min(n, lo + kSliceRows);
   const float* row = p.scores + (int64_t)t * p.ld;
+  const uint32_t* rs = given ? p.range_slots : slots;
+  const int nrs = given ? p.n_range_slots : P;
+  // range mode: the scorer's key ranges are loaded together with the slice (one round trip to L2)
+  uint32_t gmn = 0xFFFFFFFFu, gmx = 0;
+  if (given)
+    for (int i = threadIdx.x; i < nrs; i += kThreads) {
+      gmn = min(gmn, __ldcg(rs + 2 * i));
+      gmx = max(gmx, __ldcg(rs + 2 * i + 1));
+    }
   uint32_t k[kSlicePer];
   bool v[kSlicePer];
   load_slice(row, lo, hi, k, v);
+  for (int i = threadIdx.x; i < kGBins; i += kThreads) sh_hist[i] = 0;  // ordered by the next barrier
   uint32_t mn = 0xFFFFFFFFu, mx = 0;
-  const uint32_t* rs = given ? p.range_slots : slots;
-  const int nrs = given ? p.n_range_slots : P;
   if (!given) {
 #pragma unroll
     for (int i = 0; i < kSlicePer; ++i)
@@ -1191,28 +1223,23 @@ __global__ void __launch_bounds__(kThreads) long_coop_kernel(const KParams p) {
         mn = min(mn, k[i]);
         mx = max(mx, k[i]);
       }
-    mn = block_min_u32(mn, red);
-    mx = block_max_u32(mx, red);
+    block_minmax_u32(mn, mx, red, red2);
     if (threadIdx.x == 0) {
       slots[2 * part] = mn;
       slots[2 * part + 1] = mx;
     }
     if (!token_barrier(counter, ++nb * (uint32_t)P, p.status, 60)) return;
+    for (int i = threadIdx.x; i < nrs; i += kThreads) {
+      gmn = min(gmn, __ldcg(rs + 2 * i));
+      gmx = max(gmx, __ldcg(rs + 2 * i + 1));
+    }
   }
 
   // phase 2: the row's key range from the slots; histogram of the slice into the token's
-  mn = 0xFFFFFFFFu;
-  mx = 0;
-  for (int i = threadIdx.x; i < nrs; i += kThreads) {
-    mn = min(mn, __ldcg(rs + 2 * i));
-    mx = max(mx, __ldcg(rs + 2 * i + 1));
-  }
-  const uint32_t kmin = block_min_u32(mn, red);
-  const uint32_t kmax = block_max_u32(mx, red);
+  block_minmax_u32(gmn, gmx, red, red2);  // its barriers also order the zeroed sh_hist
+  const uint32_t kmin = gmn, kmax = gmx;
   const uint64_t range = (uint64_t)kmax - kmin + 1;
   const uint32_t mult = range <= (uint64_t)kGBins ? 0u : bin_mult(range, kGBins);
-  for (int i = threadIdx.x; i < kGBins; i += kThreads) sh_hist[i] = 0;
-  __syncthreads();
 #pragma unroll
   for (int i = 0; i < kSlicePer; ++i)
     if (v[i]) atomicAdd(&sh_hist[long_bin(k[i], kmin, mult)], 1u);
