@@ -162,8 +162,10 @@ int ds4x_sparse_attn(const void* q_attn, const void* kv, ds4x_dtype dtype,
  *   q, w, k fp16 as in ds4x_indexer_score; q_attn, kv, out of kv_dtype.
  *   When the tokens fill less than half of the GPU's SMs (2T <= SM count, e.g. decode), the
  *   attention of each token is split over several CTAs by chunks of its selected rows and the
- *   parts are merged by their softmax statistics; out and lse then differ from the unsplit
- *   result only by fp32 rounding order.  The workspace holds
+ *   parts are merged by their softmax statistics.  Each part is normalized by its own row sum
+ *   and stored in kv_dtype (a convex combination of kv rows: inside the dtype's range), so out
+ *   and lse then differ from the unsplit result by fp32 rounding order and that one rounding of
+ *   the parts.  The workspace holds
  *   [scores T x S fp32 | top-k scratch | split-attention scratch] (256-byte aligned parts).
  * ------------------------------------------------------------------------- */
 int ds4x_index_and_attend(const void* q, const void* w, const void* k, const int32_t* positions,
