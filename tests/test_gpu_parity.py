@@ -246,13 +246,14 @@ def test_topk_one_cta_rounds_exact(S, pad):
     assert np.array_equal(cnt.cpu().numpy(), ref_cnt)
 
 
-@pytest.mark.parametrize("S", [2048, 8192, 12000, 16384])
+@pytest.mark.parametrize("S", [2048, 8192, 12000, 16384, 40000, 65536])
 @pytest.mark.parametrize("k_top", [300, 512, 1024])
 def test_topk_many_tokens_exact(S, k_top):
-    # at least one token per SM, so every row takes the one-token-per-CTA kernels (a warp per token up
-    # to 2048 rows; eight warps per token, one segment each, up to 16384): N(0,1) rows, small
-    # integers (long runs of ties), a row whose best scores all sit in one segment, a row of equal
-    # scores, and visible counts from just above k_top to the whole row
+    # at least one token per SM, so every row takes the one-CTA-per-token kernels: keys in registers
+    # up to 4096 rows, the row staged in shared memory up to 32768, the streaming one-pass select
+    # (running threshold, ballot compaction) beyond.  N(0,1) rows, small integers (long runs of
+    # ties), a row whose best scores all sit in one eighth of it, a row of equal scores, and visible
+    # counts from just above k_top to the whole row
     T = 160
     rng = np.random.default_rng(S * 7 + k_top)
     sc = rng.standard_normal((T, S)).astype(np.float32)
