@@ -1,6 +1,8 @@
 """The decode loop (one token per step, rows appended as positions complete them) and the split
 attention it runs on (a token's chunks spread over CTAs and merged by their softmax statistics),
 against the CPU oracle."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -102,11 +104,13 @@ def test_decode_full_size_whole_call_sampled():
         check_attn(gout[i:i + 1], ref_out, wl.kv_dtype, glse[i:i + 1], ref_lse)
 
 
-@pytest.mark.parametrize("T,k_top", [(1, 512), (16, 512), (50, 512), (76, 512), (1, 300)])
-def test_split_attention_matches_oracle(T, k_top):
+@pytest.mark.parametrize("T,k_top,kv_dtype", [(1, 512, "bf16"), (16, 512, "bf16"), (50, 512, "bf16"), (76, 512, "bf16"),
+                                               (1, 300, "bf16"), (1, 512, "f16"), (16, 512, "f16")])
+def test_split_attention_matches_oracle(T, k_top, kv_dtype):
     # few tokens: the fused path splits each token's attention over CTAs (uneven splits at
-    # T = 50, a partial last chunk at k_top = 300) and merges the parts
-    wl = synth.WORKLOADS["prefill_8k"]
+    # T = 50, a partial last chunk at k_top = 300) and merges the parts, which are stored in the
+    # kv dtype (both dtypes)
+    wl = dataclasses.replace(synth.WORKLOADS["prefill_8k"], kv_dtype=kv_dtype)
     inp = synth.make_inputs(wl, seed=3, T=T, pos0=wl.pos0 + wl.T - T)
     d = to_device(inp)
     assert ds4x.workspace_bytes(T, wl.S, k_top) >= T * wl.S * 4
