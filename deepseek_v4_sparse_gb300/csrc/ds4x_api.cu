@@ -155,7 +155,9 @@ int run_index_and_attend(const void* q, const void* w, const void* k, const int3
   // hands over the key range of the scores it wrote, so the top-k starts at its histogram phase.
   const bool zero_counters = S > 0 && topk_bytes > 0;
   const int n_slots = S > 0 ? score_grid(T, H, S) : 0;
-  const bool range_mode = zero_counters && topk_range_mode(T, S, k_top, n_slots);
+  // (the range slots are written and read as 16-byte words)
+  const bool range_mode = zero_counters && topk_range_mode(T, S, k_top, n_slots) &&
+                          aligned16(ws + score_bytes + topk_range_slots_offset(T, S));
   uint32_t* range_slots = range_mode ? reinterpret_cast<uint32_t*>(ws + score_bytes + topk_range_slots_offset(T, S))
                                      : nullptr;
   if (S > 0) {

@@ -66,7 +66,10 @@ struct ScoreArgs {
   int write_masked;   // 1: write -inf on masked rows, including whole masked tiles
   uint32_t* zero_words = nullptr;  // fused path: words the kernel zeroes once the previous kernel is done
   int n_zero = 0;                  // (the top-k's barrier counters, so no memset sits between the launches)
-  uint32_t* range_slots = nullptr; // T = 1: per CTA, min and max ordered key of the visible scores it wrote
+  // T = 1: per CTA a slot of 4 words (16-byte aligned): the min and max ordered key of the visible
+  // scores it wrote, the fourth largest of its threads' maximum keys (0 when fewer than four threads
+  // saw a visible row), 0
+  uint32_t* range_slots = nullptr;
 };
 int launch_score(const ScoreArgs& a, cudaStream_t stream);
 bool score_shape_supported(int H, int D);
@@ -84,7 +87,7 @@ struct TopkArgs {
   size_t workspace_bytes;
   int counters_zeroed = 0;  // 1: the workspace's barrier counters were zeroed by the kernel before (fused path)
   // range mode (one token whose row the cooperative kernel splits): the scorer zeroed the token's
-  // scratch and wrote n_range_slots (min, max) pairs of ordered keys at range_slots
+  // scratch and wrote n_range_slots slots of 4 words at range_slots (see ScoreArgs::range_slots)
   const uint32_t* range_slots = nullptr;
   int n_range_slots = 0;
 };

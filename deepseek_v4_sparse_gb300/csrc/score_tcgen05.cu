@@ -69,7 +69,7 @@ struct Cfg {
   static constexpr int Q_BYTES = TN * D * 2;       // one q tile
   static constexpr int QB_BYTES = TN * 128;        // one 64-wide block of the q tile
   static constexpr int NQ = 2;                        // q tile buffers
-  static constexpr int FIXED = NQ * Q_BYTES + kGroups * kWStage * 4 + 512;  // q, w of the epilogue groups, barriers
+  static constexpr int FIXED = NQ * Q_BYTES + kGroups * kWStage * 4 + 640;  // q, w of the epilogue groups, barriers
   static constexpr int NK_FIT = (kSmemBudget - FIXED) / kBlockBytes;
   static constexpr int NK = NK_FIT < 12 ? NK_FIT : 12;  // k stages (one 64-wide block each)
   static constexpr int SMEM = FIXED + NK * kBlockBytes;
@@ -80,8 +80,9 @@ struct Cfg {
   static_assert(D % 64 == 0, "D must be a multiple of 64");
   static_assert(NK >= 4 && SMEM <= kSmemBudget, "shared memory");
   static_assert(TMEM_COLS <= 512, "TMEM");
-  // barriers, the TMEM address and the per-warp key ranges fit the 512 bytes set aside for them
-  static_assert((2 * NK + 2 * NQ + 2 * NACC + 2 * kGroups) * 8 + 16 + 2 * kEpiWarps * 4 <= 512, "barrier area");
+  // barriers, the TMEM address, the per-warp key ranges and four largest keys fit the 640 bytes
+  // set aside for them
+  static_assert((2 * NK + 2 * NQ + 2 * NACC + 2 * kGroups) * 8 + 16 + 6 * kEpiWarps * 4 <= 640, "barrier area");
 };
 
 struct Params {
@@ -97,8 +98,24 @@ struct Params {
   int* status;
   uint32_t* zero_words;  // zeroed (by all CTAs) once the previous kernel is done
   int n_zero;
-  uint32_t* range_slots;  // T = 1: [grid][2] min and max ordered key of the visible scores each CTA wrote
+  // T = 1: [grid][4] per CTA the min and max ordered key of the visible scores it wrote, the fourth
+  // largest of its epilogue threads' maximum keys, 0
+  uint32_t* range_slots;
 };
+
+// The warp's values in descending order: lane i returns the i-th largest (bitonic network).
+__device__ __forceinline__ uint32_t warp_sort_desc(uint32_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const uint32_t o = __shfl_xor_sync(0xffffffffu, v, j);
+      v = (((lane & k) == 0) == ((lane & j) == 0)) ? max(v, o) : min(v, o);
+    }
+  }
+  return v;
+}
 
 __device__ __forceinline__ int n_visible(const Params& p, int t) {
   const int pos = __ldg(p.positions + t);
@@ -180,6 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* wready = wdone + kGroups;  // [epilogue group] the next token group's w is written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wready + kGroups);
   uint32_t* red_s = tmem_slot + 4;  // [2][kEpiWarps] per-warp key range (range mode)
+  uint32_t* red4 = red_s + 2 * kEpiWarps;  // [kEpiWarps][4] per-warp four largest thread maxima
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -467,7 +485,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&aempty[ab]);
     }
     if (p.range_slots) {
-      // this CTA's key range: over the warp, then over the epilogue warps
+      // this CTA's key range, over the warp and then over the epilogue warps; and the fourth
+      // largest of the threads' maximum keys (a thread without visible rows holds 0): the four
+      // largest of each warp, then of those. At least four of this CTA's visible scores have a key
+      // at or above it (four distinct threads' maxima), which lets the top-k bound the row's
+      // k_top-th key from below before it reads a score.
+      const uint32_t srt = warp_sort_desc(kmx);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         kmn = min(kmn, __shfl_xor_sync(0xffffffffu, kmn, o));
@@ -477,15 +500,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         red_s[e] = kmn;
         red_s[kEpiWarps + e] = kmx;
       }
+      if (lane < 4) red4[4 * e + lane] = srt;
       asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
-      if (e == 0 && lane == 0) {
-        uint32_t a = red_s[0], b = red_s[kEpiWarps];
-        for (int i = 1; i < kEpiWarps; ++i) {
-          a = min(a, red_s[i]);
-          b = max(b, red_s[kEpiWarps + i]);
+      if (e == 0) {
+        static_assert(4 * kEpiWarps == 32, "one warp sorts the warps' four largest");
+        const uint32_t r4 = __shfl_sync(0xffffffffu, warp_sort_desc(red4[lane]), 3);
+        if (lane == 0) {
+          uint32_t a = red_s[0], b = red_s[kEpiWarps];
+          for (int i = 1; i < kEpiWarps; ++i) {
+            a = min(a, red_s[i]);
+            b = max(b, red_s[kEpiWarps + i]);
+          }
+          reinterpret_cast<uint4*>(p.range_slots)[blockIdx.x] = make_uint4(a, b, r4, 0u);
         }
-        p.range_slots[2 * blockIdx.x] = a;
-        p.range_slots[2 * blockIdx.x + 1] = b;
       }
     }
   }

@@ -808,12 +808,16 @@ constexpr int kCandCap = 8192;
 struct LongCtl {
   uint32_t kmin, mult, bstar, above;
   uint32_t ncand, done2, done3, whole;  // whole: one-launch mode, slice 0 emitted the whole row
+  uint32_t npre;                        // range mode: rows at or above the lower bound (prefilter)
 };
 
 struct LongLayout {  // byte offsets inside one token's block of the workspace
   size_t ctl, slots, scnt, hist, bitmap, ckey, crow, rslots, total;
 };
 constexpr int kMaxRangeSlots = 1024;  // scorer CTAs whose key ranges the one-token mode takes
+constexpr int kPreCap = 2048;         // prefilter candidates every slice ranks (kept in ckey / crow)
+constexpr int kPrePer = kPreCap / kThreads;
+static_assert(kPreCap <= kCandCap && kPreCap % kThreads == 0, "prefilter candidates");
 
 __host__ __device__ inline size_t align_up(size_t n, size_t a) { return (n + a - 1) / a * a; }
 
@@ -836,8 +840,9 @@ __host__ __device__ inline LongLayout long_layout(int S) {
   o += (size_t)kCandCap * sizeof(uint32_t);
   L.crow = o;
   o += (size_t)kCandCap * sizeof(uint32_t);
+  o = align_up(o, 16);
   L.rslots = o;  // outside the zeroed part [ctl, bitmap end): the scorer writes it while others zero
-  o += (size_t)2 * kMaxRangeSlots * sizeof(uint32_t);
+  o += (size_t)4 * kMaxRangeSlots * sizeof(uint32_t);
   L.total = align_up(o, 256);
   return L;
 }
@@ -897,6 +902,32 @@ __device__ __forceinline__ void block_minmax_u32(uint32_t& mn, uint32_t& mx, uin
     mn = min(mn, red_mn[w]);
     mx = max(mx, red_mx[w]);
   }
+}
+
+// The block's values, one a thread, in descending order: thread i returns the i-th largest.
+// A bitonic network; partners 32 or more apart trade through xs (2 x kThreads words, the halves
+// taken in turn, so one barrier a step suffices: a half is rewritten only after the next barrier).
+__device__ __forceinline__ uint32_t block_sort_desc(uint32_t v, uint32_t* xs) {
+  const int i = threadIdx.x;
+  int half = 0;
+#pragma unroll
+  for (int k = 2; k <= kThreads; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      uint32_t o;
+      if (j >= 32) {
+        uint32_t* x = xs + half * kThreads;
+        x[i] = v;
+        __syncthreads();
+        o = x[i ^ j];
+        half ^= 1;
+      } else {
+        o = __shfl_xor_sync(0xffffffffu, v, j);
+      }
+      v = (((i & k) == 0) == ((i & j) == 0)) ? max(v, o) : min(v, o);
+    }
+  }
+  return v;
 }
 
 // the thread's rows lo + i * kThreads + threadIdx.x of the slice as ordered keys (all loads issued
@@ -1169,6 +1200,11 @@ __global__ void __launch_bounds__(kThreads) long_coop_kernel(const KParams p) {
   __shared__ uint32_t red[kWarps];
   __shared__ uint32_t red2[kWarps];
   __shared__ uint32_t sh_b[3];
+  constexpr int kSliceWords = kSliceRows / 32;
+  __shared__ uint64_t cand[kThreads];  // boundary-bin candidates' composites
+  __shared__ uint32_t add[kThreads];   // winners among the candidates, per slice
+  __shared__ uint32_t words[kSliceWords];
+  __shared__ uint32_t n_in_b;
   const int t = blockIdx.y, part = blockIdx.x, P = gridDim.x;
   const int n = n_visible(p.positions, t, p.ratio, p.S);
   int32_t* out = p.indices + (int64_t)t * p.k_top;
@@ -1190,7 +1226,8 @@ __global__ void __launch_bounds__(kThreads) long_coop_kernel(const KParams p) {
   const int W = (p.S + 31) / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // range mode: the scorer zeroed this token's scratch and wrote the key ranges of what it scored,
-  // so phase 1 and its grid barrier fall away (nb counts the grid barriers passed)
+  // so phase 1 and its grid barrier fall away (nb counts the grid barriers passed); with a bound on
+  // the row's k_top-th key from those slots, the prefilter below usually replaces phases 2 to 5
   const bool given = p.range_slots != nullptr;
   uint32_t nb = 0;
 
@@ -1201,15 +1238,21 @@ __global__ void __launch_bounds__(kThreads) long_coop_kernel(const KParams p) {
     if (part == 0 && threadIdx.x < (int)(sizeof(LongCtl) / 4)) reinterpret_cast<uint32_t*>(ctl)[threadIdx.x] = 0;
   }
   const int lo = part * kSliceRows, hi = min(n, lo + kSliceRows);
+  const int w0 = lo >> 5;  // this slice's first bitmap word
+  const bool my_word_in = threadIdx.x < kSliceWords && lo + 32 * (int)threadIdx.x < hi;
   const float* row = p.scores + (int64_t)t * p.ld;
-  const uint32_t* rs = given ? p.range_slots : slots;
   const int nrs = given ? p.n_range_slots : P;
-  // range mode: the scorer's key ranges are loaded together with the slice (one round trip to L2)
-  uint32_t gmn = 0xFFFFFFFFu, gmx = 0;
+  // range mode: the scorer's slots are loaded together with the slice (one round trip to L2); when
+  // the prefilter runs (at most kThreads slots) a thread takes at most one slot and keeps its bound
+  const int m_rep = (p.k_top + 3) / 4;  // slots whose fourth-largest keys bound the k_top-th key
+  const bool prefilter = given && p.k_top > 0 && nrs <= kThreads && m_rep <= nrs;
+  uint32_t gmn = 0xFFFFFFFFu, gmx = 0, rep = 0;
   if (given)
     for (int i = threadIdx.x; i < nrs; i += kThreads) {
-      gmn = min(gmn, __ldcg(rs + 2 * i));
-      gmx = max(gmx, __ldcg(rs + 2 * i + 1));
+      const uint4 sl = __ldcg(reinterpret_cast<const uint4*>(p.range_slots) + i);
+      gmn = min(gmn, sl.x);
+      gmx = max(gmx, sl.y);
+      rep = sl.z;
     }
   uint32_t k[kSlicePer];
   bool v[kSlicePer];
@@ -1230,8 +1273,145 @@ __global__ void __launch_bounds__(kThreads) long_coop_kernel(const KParams p) {
     }
     if (!token_barrier(counter, ++nb * (uint32_t)P, p.status, 60)) return;
     for (int i = threadIdx.x; i < nrs; i += kThreads) {
-      gmn = min(gmn, __ldcg(rs + 2 * i));
-      gmx = max(gmx, __ldcg(rs + 2 * i + 1));
+      gmn = min(gmn, __ldcg(slots + 2 * i));
+      gmx = max(gmx, __ldcg(slots + 2 * i + 1));
+    }
+  }
+
+  // Prefilter (range mode). Each of the scorer's CTAs reported the fourth largest of its threads'
+  // maximum keys, so at least four of its visible scores are at or above that report. Take L, the
+  // m_rep-th largest report (m_rep = ceil(k_top / 4)): at least 4 m_rep >= k_top visible scores
+  // are at or above L, hence so is the k_top-th largest key, and every row of the top-k has a key
+  // at or above L. The slices collect those rows (about twice k_top in a row of independent
+  // scores) in one list, pass one grid barrier, and each slice then ranks the whole list itself:
+  // a histogram of its keys over [L, max], the boundary bin's rows ranked exactly. Each slice
+  // knows from the list alone how many selected rows lie before it and writes its own rows in
+  // ascending order. Exactness rests on the count alone: whatever the reports, when the list holds
+  // at least k_top rows, the k_top-th largest key is at or above L. When it holds fewer (scores
+  // that do not match the reports), more than kPreCap, or the boundary bin more than kThreads
+  // rows, every slice sees the same counts and all go on with the histogram phases below.
+  if (prefilter) {
+    block_minmax_u32(gmn, gmx, red, red2);
+    const uint32_t srt = block_sort_desc(rep, sh.key);  // threads past the slots hold 0
+    if ((int)threadIdx.x == m_rep - 1) sh_b[2] = srt;
+    if (threadIdx.x == 0) n_in_b = 0;
+    if (threadIdx.x < kSliceWords) words[threadIdx.x] = 0;
+    __syncthreads();
+    const uint32_t L = sh_b[2];
+    {  // this slice's rows at or above L into the list: one atomic a warp
+      uint32_t bal[kSlicePer], tot = 0;
+#pragma unroll
+      for (int i = 0; i < kSlicePer; ++i) {
+        bal[i] = __ballot_sync(0xffffffffu, v[i] && k[i] >= L);
+        tot += __popc(bal[i]);
+      }
+      if (tot) {
+        uint32_t base = 0;
+        if (lane == 0) base = atomicAdd(&ctl->npre, tot);
+        base = __shfl_sync(0xffffffffu, base, 0);
+        const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+        for (int i = 0; i < kSlicePer; ++i) {
+          if ((bal[i] >> lane) & 1u) {
+            const uint32_t slot = base + __popc(bal[i] & lt);
+            if (slot < (uint32_t)kPreCap) {
+              ckey[slot] = k[i];
+              crow[slot] = (uint32_t)(lo + i * kThreads + (int)threadIdx.x);
+            }
+          }
+          base += __popc(bal[i]);
+        }
+      }
+    }
+    if (!token_barrier(counter, ++nb * (uint32_t)P, p.status, 64)) return;
+    // the count and the whole list at once (entries past the count are not used)
+    const int C = (int)__ldcg(&ctl->npre);
+    uint32_t ck[kPrePer], cr[kPrePer];
+#pragma unroll
+    for (int i = 0; i < kPrePer; ++i) {
+      ck[i] = __ldcg(ckey + threadIdx.x + i * kThreads);
+      cr[i] = __ldcg(crow + threadIdx.x + i * kThreads);
+    }
+    if (C >= p.k_top && C <= kPreCap) {
+      const uint64_t crange = (uint64_t)max(gmx, L) - L + 1;
+      const uint32_t cmult = crange <= (uint64_t)kGBins ? 0u : bin_mult(crange, kGBins);
+      uint32_t cb[kPrePer];
+#pragma unroll
+      for (int i = 0; i < kPrePer; ++i) {
+        cb[i] = long_bin(ck[i], L, cmult);
+        if ((int)threadIdx.x + i * kThreads < C) atomicAdd(&sh_hist[cb[i]], 1u);
+      }
+      __syncthreads();
+      {  // the boundary bin: suffix counts from the top bin down
+        constexpr int kPer = kGBins / kThreads;
+        uint32_t c[kPer], own = 0;
+        const int top = kGBins - kPer * threadIdx.x;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          c[i] = sh_hist[top - 1 - i];
+          own += c[i];
+        }
+        uint32_t total;
+        const uint32_t incl = block_scan(own, sh, &total);
+        uint32_t run = incl - own;
+        const uint32_t need = (uint32_t)p.k_top;
+        if (run < need && incl >= need) {
+#pragma unroll
+          for (int i = 0; i < kPer; ++i) {
+            if (run + c[i] >= need) {
+              sh_b[0] = (uint32_t)(top - 1 - i);
+              sh_b[1] = run;
+              break;
+            }
+            run += c[i];
+          }
+        }
+        __syncthreads();
+      }
+      const uint32_t bstar = sh_b[0], above = sh_b[1];
+      const uint32_t nstar = sh_hist[bstar];
+      if (nstar <= (uint32_t)kThreads) {
+        pdl_trigger();  // this slice has passed its last barrier
+        // a selected row: counted when it lies before this slice, marked when in it
+        uint32_t before = 0;
+        auto take = [&](uint32_t r) {
+          if (r < (uint32_t)lo) ++before;
+          else if (r < (uint32_t)hi) atomicOr(&words[(r - lo) >> 5], 1u << (r & 31));
+        };
+#pragma unroll
+        for (int i = 0; i < kPrePer; ++i) {
+          if ((int)threadIdx.x + i * kThreads >= C || cb[i] < bstar) continue;
+          if (cb[i] > bstar) take(cr[i]);
+          else cand[atomicAdd(&n_in_b, 1u)] = composite(ck[i], cr[i]);
+        }
+        __syncthreads();
+        if (threadIdx.x < nstar) {  // in iff fewer than need boundary rows beat it
+          const uint64_t mine = cand[threadIdx.x];
+          int rank = 0;
+          for (int j = 0; j < (int)nstar; ++j) rank += cand[j] > mine;
+          if (rank < p.k_top - (int)above) take(~static_cast<uint32_t>(mine));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+        if (lane == 0) red[warp] = before;
+        __syncthreads();
+        uint32_t offset = 0;
+        for (int w = 0; w < kWarps; ++w) offset += red[w];
+        if (part == 0 && cnt_out && threadIdx.x == 0) *cnt_out = p.k_top;
+        const uint32_t word = my_word_in ? words[threadIdx.x] : 0u;
+        uint32_t total;
+        const uint32_t incl = block_scan((uint32_t)__popc(word), sh, &total);
+        uint32_t pos = offset + incl - (uint32_t)__popc(word);
+        uint32_t bits = word;
+        while (bits) {
+          const int b = __ffs(bits) - 1;
+          bits &= bits - 1;
+          out[pos++] = (w0 + (int)threadIdx.x) * 32 + b;
+        }
+        return;
+      }
+      __syncthreads();  // every thread has read the histogram
+      for (int i = threadIdx.x; i < kGBins; i += kThreads) sh_hist[i] = 0;  // ordered by phase 2's barriers
     }
   }
 
@@ -1317,12 +1497,9 @@ __global__ void __launch_bounds__(kThreads) long_coop_kernel(const KParams p) {
   // the candidate count (the same in every slice of the token), the candidates as far as the
   // fast path takes them (kThreads <= kCandCap: the loads stay inside the buffer, entries past the
   // count go unused), the slices' counts and this slice's bitmap words
-  constexpr int kSliceWords = kSliceRows / 32;
-  const int w0 = lo >> 5;
   const int m_cand = (int)__ldcg(&ctl->ncand);
   const uint32_t my_key = __ldcg(ckey + threadIdx.x), my_row = __ldcg(crow + threadIdx.x);
   const uint32_t my_scnt = (int)threadIdx.x < P ? __ldcg(scnt + threadIdx.x) : 0u;
-  const bool my_word_in = threadIdx.x < kSliceWords && lo + 32 * (int)threadIdx.x < hi;
   const uint32_t my_word = my_word_in ? __ldcg(bm + w0 + threadIdx.x) : 0u;
   if (m_cand <= kThreads && P <= kThreads) {
     // few boundary rows (the usual case): every slice ranks them itself (candidate j is in iff
@@ -1330,9 +1507,6 @@ __global__ void __launch_bounds__(kThreads) long_coop_kernel(const KParams p) {
     // barrier, adds its own winners to its words and writes its rows after the earlier slices'
     pdl_trigger();  // this slice has passed its last barrier
     static_assert(kThreads <= kCandCap, "speculative candidate loads");
-    __shared__ uint64_t cand[kThreads];  // the candidates' composites
-    __shared__ uint32_t add[kThreads];   // winners among the candidates, per slice
-    __shared__ uint32_t words[kSliceWords];
     const int need = p.k_top - (int)above;
     add[threadIdx.x] = 0;
     if (threadIdx.x < kSliceWords) words[threadIdx.x] = 0;

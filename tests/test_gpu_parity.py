@@ -299,6 +299,52 @@ def test_long_row_topk_exact(case):
         assert np.array_equal(ref_idx[0], np.arange(512))
 
 
+# ------------------------------------------------------- one token over a long row, fused
+def _fused_one_token(inp):
+    d = to_device(inp)
+    wl = inp.wl
+    scores = ds4x.indexer_score(d["q"], d["w"], d["k"], d["positions"], wl.ratio, S=wl.S)
+    fidx, _, _ = ds4x.index_and_attend(d["q"], d["w"], d["k"], d["positions"], d["q_attn"], d["kv"],
+                                       wl.ratio, wl.k_top, S=wl.S, scale=wl.scale)
+    torch.cuda.synchronize()
+    assert ds4x.device_status() == ds4x.OK
+    return scores.cpu().numpy(), fidx.cpu().numpy()
+
+
+@pytest.mark.parametrize("case,S,n", [("random", 65536 + 37, None), ("random", 16384, None),
+                                      ("random", 12000, None), ("partly_visible", 50000, 30001),
+                                      ("all_ties", 20000, None), ("top_ties", 40000, None),
+                                      ("int_ties", 40000, None), ("int_ties", 65536, None)])
+def test_one_token_fused_topk_exact(case, S, n):
+    # One token over a long row in the fused path (a decode step). The scorer hands the top-k a
+    # lower bound on the k_top-th key; the top-k ranks only the rows at or above it when their
+    # count lies in [k_top, its list's capacity] and its boundary bin is small (random and integer
+    # scores), else goes on with its histogram phases (every score equal; 600 rows sharing the
+    # top score; a row of which only part is visible, so the bound falls to the lowest key).
+    # Rows under 16384 have too few scorer CTAs for the bound. The indices must equal the oracle's
+    # top-k of the scores the GPU computed.
+    n = S if n is None else n
+    kind = "int" if case == "int_ties" else "normal"
+    raw = _edge_inputs(f"one_{case}_{S}", [n - 1], S, kind=kind, w_kind="pow2" if kind == "int" else "pos", seed=2)
+    wl = synth.Workload(raw.wl.name, T=1, H=64, D=128, S=S, ratio=1, pos0=0, kind=kind, kv_dtype="bf16")
+    inp = synth.Inputs(wl, raw.q, raw.w, raw.k, raw.positions, raw.q_attn, raw.kv)
+    if case == "all_ties":
+        inp.q[:] = 0
+    if case == "top_ties":  # 600 spread rows become twice the best row: twice its score, exactly
+        scores, _ = _fused_one_token(inp)
+        best = int(np.argmax(scores[0, :n]))
+        k16 = inp.k.view(np.float16)
+        k16[np.arange(17, n, n // 600)[:600]] = k16[best] * np.float16(2)
+    scores, fidx = _fused_one_token(inp)
+    vis = scores[0, :n]
+    if case == "all_ties":
+        assert np.all(vis == 0)
+    if case == "top_ties":
+        assert np.count_nonzero(vis == vis.max()) == 600
+    ref_idx, _ = oracle.topk(scores, inp.positions, S, 1, wl.k_top)
+    assert np.array_equal(fidx, ref_idx)
+
+
 # --------------------------------------- full-size workloads in the benchmark's launch shape
 @pytest.mark.parametrize("name", ["prefill_8k", "prefill_32k", "prefill_64k"])
 def test_full_size_sampled(name):
