@@ -65,3 +65,24 @@ def test_host_path_back_to_back_calls_share_nothing_stale():
         check_index_sets(idx.numpy(), ref_idx, ref_scores, inp.positions, wl.ratio, wl.S, wl.k_top)
         ref_out, ref_lse = oracle.sparse_attn(inp.q_attn, inp.kv, wl.kv_dtype, idx.numpy(), wl.S, wl.scale)
         check_attn(out.view(torch.int16).numpy().view(np.uint16), ref_out, wl.kv_dtype, lse.numpy(), ref_lse)
+
+
+def test_host_path_one_token_sub_chunks_long_row():
+    # two decode-recipe tokens over 32768 rows, one per sub-chunk: each sub-chunk is one token
+    # over a long row (the top-k's one-token mode with the scorer's bounds), the second reusing the
+    # device buffer the first one used
+    wl = synth.WORKLOADS["decode_1m"]
+    S = 32768
+    inp = synth.make_inputs(wl, seed=4, T=2, S=S, pos0=wl.ratio * S + 5, rows=S)
+    idx, out, lse = ds4x.index_and_attend_host(
+        _host16(inp.q, "f16", True), _host16(inp.w, "f16", True), _host16(inp.k, "f16", True),
+        torch.from_numpy(inp.positions.copy()).pin_memory(), _host16(inp.q_attn, wl.kv_dtype, True),
+        _host16(inp.kv, wl.kv_dtype, True), wl.ratio, wl.k_top, S=S, scale=wl.scale, n_chunks=2)
+    torch.cuda.synchronize()
+    assert ds4x.device_status() == ds4x.OK
+    gidx = idx.numpy()
+    ref_scores = oracle.indexer_score(inp.q, inp.w, inp.k, inp.positions, wl.ratio, S=S)
+    ref_idx, _ = oracle.topk(ref_scores, inp.positions, S, wl.ratio, wl.k_top)
+    check_index_sets(gidx, ref_idx, ref_scores, inp.positions, wl.ratio, S, wl.k_top)
+    ref_out, ref_lse = oracle.sparse_attn(inp.q_attn, inp.kv, wl.kv_dtype, gidx, S, wl.scale)
+    check_attn(out.view(torch.int16).numpy().view(np.uint16), ref_out, wl.kv_dtype, lse.numpy(), ref_lse)
