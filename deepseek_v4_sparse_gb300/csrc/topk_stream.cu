@@ -525,8 +525,10 @@ struct KParams {
   uint32_t* gbar;       // one-launch long-row mode: a barrier counter per token (zeroed before the launch)
   int nslice;           // long-row mode: CTAs per token
   int* status;
-  // one-launch long-row mode, one token: the key range comes as n_range_slots (min, max) pairs
-  // written by the scorer, which also zeroed the token's scratch (nullptr: the kernel does both)
+  // one-launch long-row mode, one token: n_range_slots slots of 4 words written by the scorer (the
+  // min and max ordered key of the scores a CTA wrote, the fourth largest of its threads' maximum
+  // keys, 0), which also zeroed the token's scratch (nullptr: the kernel zeroes it and finds the
+  // key range itself)
   const uint32_t* range_slots;
   int n_range_slots;
 };
